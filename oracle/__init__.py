@@ -1,0 +1,255 @@
+"""ctypes front end of the plain CPU oracle (``kvarn_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, the package smoke check and the
+CPU-baseline leg of ``bench.py`` use it; the product path never imports it.
+It shares no code with the CUDA library.  Every function works on numpy
+arrays and is fp64 inside; see the C file for the definitions and sources.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "kvarn_oracle.c")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(BUILD, "libkvarn_oracle.so")
+
+D = 128
+T = 128
+K_LEVELS = 15
+V_LEVELS = 3
+FLAG_CLAMPED = 1
+FLAG_STEP_SAT = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with plain IEEE semantics (no FMA contraction, which
+    gcc enables by default on aarch64)."""
+    os.makedirs(BUILD, exist_ok=True)
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+        tmp = LIB + f".{os.getpid()}.tmp"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+             "-shared", "-Wall", "-o", tmp, SRC, "-lm", "-lpthread"])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, dbl, u8, u16 = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_uint8, ctypes.c_uint16
+        L.ora_e4m3_decode.restype = dbl; L.ora_e4m3_decode.argtypes = [u8]
+        L.ora_e4m3_encode_rne.restype = u8; L.ora_e4m3_encode_rne.argtypes = [dbl]
+        L.ora_e4m3_encode_ru.restype = u8; L.ora_e4m3_encode_ru.argtypes = [dbl]
+        L.ora_f16_decode.restype = dbl; L.ora_f16_decode.argtypes = [u16]
+        L.ora_f16_encode_rd.restype = u16; L.ora_f16_encode_rd.argtypes = [dbl]
+        L.ora_f16_encode_rne.restype = u16; L.ora_f16_encode_rne.argtypes = [dbl]
+        L.ora_bf16_decode.restype = dbl; L.ora_bf16_decode.argtypes = [u16]
+        L.ora_f32_ru.restype = ctypes.c_float; L.ora_f32_ru.argtypes = [dbl]
+        L.ora_hadamard_matrix.argtypes = [P]
+        L.ora_rotate.argtypes = [P, i32, P]
+        L.ora_sinkhorn.argtypes = [P, i32, P, P]
+        L.ora_quantize_tile.restype = i32
+        L.ora_quantize_tile.argtypes = [P, i32, i32, P, P, P, P, P, P, P]
+        L.ora_record_bytes.restype = i32; L.ora_record_bytes.argtypes = [i32]
+        L.ora_pack_record.argtypes = [i32, P, P, P, P, P]
+        L.ora_unpack_record.argtypes = [i32, P, P, P, P, P]
+        L.ora_dequantize_record.argtypes = [i32, P, P]
+        L.ora_attention.argtypes = [P, i32, P, P, i32, dbl, P]
+        L.ora_attention_folded.argtypes = [P, i32, P, P, i32, P, P, i32, dbl, P]
+        L.ora_quantize_batch.argtypes = [P, i32, P, i64, i32, i32, i32, P, P, i32]
+        L.ora_attention_batch.argtypes = [P, i32, P, P, P, P, P, P, P, dbl, i32, P, i32]
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ---------------------------------------------------------------- formats
+def e4m3_decode(code: int) -> float:
+    return lib().ora_e4m3_decode(int(code))
+
+
+def e4m3_encode_rne(x: float) -> int:
+    return int(lib().ora_e4m3_encode_rne(float(x)))
+
+
+def e4m3_encode_ru(x: float) -> int:
+    return int(lib().ora_e4m3_encode_ru(float(x)))
+
+
+def f16_decode(bits: int) -> float:
+    return lib().ora_f16_decode(int(bits))
+
+
+def f16_encode_rd(x: float) -> int:
+    return int(lib().ora_f16_encode_rd(float(x)))
+
+
+def f16_encode_rne(x: float) -> int:
+    return int(lib().ora_f16_encode_rne(float(x)))
+
+
+def f32_ru(x: float) -> float:
+    return float(lib().ora_f32_ru(float(x)))
+
+
+def decode16(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact fp64 values of 16-bit storage (dtype 'f16' or 'bf16')."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- rotation
+def hadamard_matrix() -> np.ndarray:
+    H = np.empty((D, D), np.float64)
+    lib().ora_hadamard_matrix(_p(H))
+    return H
+
+
+def rotate(X: np.ndarray) -> np.ndarray:
+    X = np.ascontiguousarray(X, dtype=np.float64).reshape(-1, D)
+    Y = np.empty_like(X)
+    lib().ora_rotate(_p(X), X.shape[0], _p(Y))
+    return Y
+
+
+def sinkhorn(R: np.ndarray, iters: int = 8):
+    """Returns (u[T], v[D]) log-factors (v not yet centred)."""
+    R = np.ascontiguousarray(R, dtype=np.float64)
+    assert R.shape == (T, D)
+    u = np.empty(T); v = np.empty(D)
+    lib().ora_sinkhorn(_p(R), iters, _p(u), _p(v))
+    return u, v
+
+
+# ---------------------------------------------------------------- tiles
+class Tile:
+    """Quantised tile as the oracle computes it."""
+
+    def __init__(self, g8, a8, b16, code, pre, R, v, flags):
+        self.g8, self.a8, self.b16, self.code = g8, a8, b16, code
+        self.pre, self.R, self.v, self.flags = pre, R, v, flags
+
+    def g(self):
+        return np.array([e4m3_decode(c) for c in self.g8])
+
+    def a(self):
+        return np.array([e4m3_decode(c) for c in self.a8])
+
+    def b(self):
+        return self.b16.view(np.float16).astype(np.float64)
+
+
+def quantize_tile(X: np.ndarray, levels: int, iters: int = 8) -> Tile:
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    assert X.shape == (T, D)
+    g8 = np.empty(D, np.uint8); a8 = np.empty(T, np.uint8); b16 = np.empty(T, np.uint16)
+    code = np.empty((T, D), np.uint8); pre = np.empty((T, D)); R = np.empty((T, D)); v = np.empty(D)
+    f = lib().ora_quantize_tile(_p(X), levels, iters, _p(g8), _p(a8), _p(b16), _p(code), _p(pre), _p(R), _p(v))
+    return Tile(g8, a8, b16, code, pre, R, v, f)
+
+
+def record_bytes(is_v: bool) -> int:
+    return int(lib().ora_record_bytes(int(is_v)))
+
+
+def pack_record(is_v: bool, tile: Tile) -> np.ndarray:
+    rec = np.zeros(record_bytes(is_v), np.uint8)
+    lib().ora_pack_record(int(is_v), _p(tile.g8), _p(tile.a8), _p(tile.b16), _p(np.ascontiguousarray(tile.code)), _p(rec))
+    return rec
+
+
+def unpack_record(is_v: bool, rec: np.ndarray):
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    g8 = np.empty(D, np.uint8); a8 = np.empty(T, np.uint8); b16 = np.empty(T, np.uint16)
+    code = np.empty((T, D), np.uint8)
+    lib().ora_unpack_record(int(is_v), _p(rec), _p(g8), _p(a8), _p(b16), _p(code))
+    return g8, a8, b16, code
+
+
+def dequantize_record(is_v: bool, rec: np.ndarray) -> np.ndarray:
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    out = np.empty((T, D))
+    lib().ora_dequantize_record(int(is_v), _p(rec), _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- attention
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.float64).reshape(-1, D)
+    K = np.ascontiguousarray(K, dtype=np.float64).reshape(-1, D)
+    V = np.ascontiguousarray(V, dtype=np.float64).reshape(-1, D)
+    out = np.empty_like(q)
+    lib().ora_attention(_p(q), q.shape[0], _p(K), _p(V), K.shape[0], float(scale), _p(out))
+    return out
+
+
+def _ptr_array(recs):
+    arr = (ctypes.c_void_p * max(1, len(recs)))()
+    for i, r in enumerate(recs):
+        arr[i] = r.ctypes.data
+    return arr
+
+
+def attention_folded(q, krecs, vrecs, ktail, vtail, scale) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.float64).reshape(-1, D)
+    krecs = [np.ascontiguousarray(r, dtype=np.uint8) for r in krecs]
+    vrecs = [np.ascontiguousarray(r, dtype=np.uint8) for r in vrecs]
+    ktail = np.ascontiguousarray(ktail, dtype=np.float64).reshape(-1, D)
+    vtail = np.ascontiguousarray(vtail, dtype=np.float64).reshape(-1, D)
+    out = np.empty_like(q)
+    ka, va = _ptr_array(krecs), _ptr_array(vrecs)
+    lib().ora_attention_folded(_p(q), q.shape[0], ka, va, len(krecs), _p(ktail), _p(vtail),
+                               ktail.shape[0], float(scale), _p(out))
+    return out
+
+
+def quantize_batch(src_bits: np.ndarray, dtype: str, first: np.ndarray, row_stride: int, is_v: bool,
+                   iters: int = 8, nthreads: int | None = None):
+    """Quantise len(first) tiles read from flat 16-bit storage; returns
+    (records [n, record_bytes], flags [n])."""
+    src_bits = np.ascontiguousarray(src_bits, dtype=np.uint16).reshape(-1)
+    first = np.ascontiguousarray(first, dtype=np.int64)
+    n = first.shape[0]
+    rec = np.zeros((n, record_bytes(is_v)), np.uint8)
+    flags = np.zeros(n, np.int32)
+    nthreads = nthreads or os.cpu_count() or 1
+    lib().ora_quantize_batch(_p(src_bits), 1 if dtype == "bf16" else 0, _p(first), int(row_stride), n,
+                             int(is_v), iters, _p(rec), _p(flags), int(nthreads))
+    return rec, flags
+
+
+def attention_batch(q, krec_lists, vrec_lists, ktails, vtails, n_tail, scale, nthreads=None):
+    """q [U, G, D]; krec_lists/vrec_lists: per unit a list of records;
+    ktails/vtails [U, T, D] fp64 (rows beyond n_tail[u] ignored)."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    U, G = q.shape[0], q.shape[1]
+    flatk = [np.ascontiguousarray(r, dtype=np.uint8) for lst in krec_lists for r in lst]
+    flatv = [np.ascontiguousarray(r, dtype=np.uint8) for lst in vrec_lists for r in lst]
+    n_tiles = np.array([len(lst) for lst in krec_lists], np.int32)
+    off = np.zeros(U, np.int64)
+    off[1:] = np.cumsum(n_tiles)[:-1]
+    ktails = np.ascontiguousarray(ktails, dtype=np.float64)
+    vtails = np.ascontiguousarray(vtails, dtype=np.float64)
+    n_tail = np.ascontiguousarray(n_tail, dtype=np.int32)
+    out = np.empty((U, G, D))
+    nthreads = nthreads or os.cpu_count() or 1
+    lib().ora_attention_batch(_p(q), G, _ptr_array(flatk), _ptr_array(flatv), _p(off), _p(n_tiles),
+                              _p(ktails), _p(vtails), _p(n_tail), float(scale), U, _p(out), int(nthreads))
+    return out

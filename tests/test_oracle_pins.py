@@ -1,0 +1,297 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+None of these compares the oracle with itself: each checks it against a
+library routine (scipy's Sylvester Hadamard matrix, numpy's IEEE float16,
+torch's float8_e4m3fn and float64 attention), a closed form, an invariant,
+or brute force on tiny inputs.  The pages (KVarN write-ups) print no worked
+example, so there is no page-printed value to pin except the preset's
+numbers (tests/golden/pages_preset.json).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+import oracle as O
+from bit_kv_cache_quantize_gb300 import inputs as I
+
+D = T = 128
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def fwht_rows(X):
+    """Independent fast Walsh-Hadamard butterfly, normalised."""
+    Y = np.array(X, dtype=np.float64, copy=True)
+    h = 1
+    while h < D:
+        for i in range(0, D, 2 * h):
+            a = Y[:, i:i + h].copy()
+            b = Y[:, i + h:i + 2 * h].copy()
+            Y[:, i:i + h] = a + b
+            Y[:, i + h:i + 2 * h] = a - b
+        h *= 2
+    return Y / math.sqrt(D)
+
+
+def key_tile(seed=0):
+    w = I.single_tile()
+    w.seed = seed
+    k = I.kv_values(w, "k", 0, 0, T)[:, 0, :]
+    return O.decode16(k.view(torch.int16).numpy().view(np.uint16), "f16")
+
+
+# ----------------------------------------------------------------- rotation
+def test_hadamard_is_sylvester_orthonormal():
+    H = O.hadamard_matrix()
+    assert np.array_equal(H, scipy.linalg.hadamard(D) / math.sqrt(D))
+    assert np.abs(H @ H.T - np.eye(D)).max() < 1e-15
+    assert np.array_equal(H, H.T)
+
+
+def test_rotation_equals_butterfly_and_preserves_norm():
+    rng = np.random.default_rng(1)
+    X = rng.standard_normal((7, D))
+    R = O.rotate(X)
+    assert np.abs(R - fwht_rows(X)).max() < 1e-12
+    assert np.allclose(np.linalg.norm(R, axis=1), np.linalg.norm(X, axis=1), rtol=1e-14)
+    e0 = np.zeros((1, D)); e0[0, 0] = 1.0
+    assert np.abs(O.rotate(e0) - 1 / math.sqrt(D)).max() < 1e-16
+    assert np.abs(O.rotate(R) - X).max() < 1e-12          # H is its own inverse
+
+
+# ----------------------------------------------------------------- sinkhorn
+@pytest.mark.parametrize("iters", [1, 2, 8])
+def test_sinkhorn_closed_form(iters):
+    """R = diag(alpha) M diag(beta), M_tc = (-1)^(t+c), alpha_2k = alpha_2k+1:
+    the first column step gives v = ln beta + ln rms(alpha), the first row
+    step u = ln alpha - ln rms(alpha); every later step is a no-op.  A row
+    step taken first would give other values (beta is not alternating)."""
+    rng = np.random.default_rng(2)
+    alpha = np.repeat(np.exp(rng.normal(0, 0.7, T // 2)), 2)
+    beta = np.exp(rng.normal(0, 0.7, D))
+    M = (-1.0) ** (np.arange(T)[:, None] + np.arange(D)[None, :])
+    R = alpha[:, None] * M * beta[None, :]
+    u, v = O.sinkhorn(R, iters)
+    rms_a = math.sqrt(np.mean(alpha ** 2))
+    assert np.abs(v - (np.log(beta) + math.log(rms_a))).max() < 1e-12
+    assert np.abs(u - (np.log(alpha) - math.log(rms_a))).max() < 1e-12
+
+
+def test_sinkhorn_normalises_rows_and_converges_columns():
+    R = O.rotate(key_tile())
+    dev = []
+    for n in (1, 2, 4, 8):
+        u, v = O.sinkhorn(R, n)
+        Z = R * np.exp(-u)[:, None] * np.exp(-v)[None, :]
+        assert np.abs(Z.std(axis=1) - 1).max() < 1e-12        # last step is a row step
+        dev.append(np.abs(Z.std(axis=0) - 1).max())
+    assert all(b < a for a, b in zip(dev, dev[1:]))
+    assert dev[-1] < 0.02
+
+
+def test_sinkhorn_degenerate_tiles_keep_factors():
+    u, v = O.sinkhorn(np.zeros((T, D)), 8)
+    assert not u.any() and not v.any()
+    row = O.rotate(np.random.default_rng(3).standard_normal((1, D)))
+    same = np.repeat(row, T, axis=0)                           # every token identical
+    u, v = O.sinkhorn(same, 8)
+    assert not v.any()                                         # column std is 0
+    assert np.allclose(u, np.log(row.std()), atol=1e-12)
+
+
+# ----------------------------------------------------------------- formats
+def test_e4m3_decode_matches_torch_exhaustive():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([O.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(ours)) and nan.sum() == 2
+    assert np.array_equal(ref[~nan], ours[~nan])
+    assert O.e4m3_decode(0x7E) == 448.0 and O.e4m3_decode(0x01) == 2.0 ** -9
+
+
+def test_e4m3_encoders():
+    for c in list(range(0x7F)) + list(range(0x81, 0xFF)):
+        assert O.e4m3_encode_rne(O.e4m3_decode(c)) == c
+    table = np.array([O.e4m3_decode(c) for c in range(0x7F)])
+    rng = np.random.default_rng(4)
+    xs = np.concatenate([np.exp(rng.uniform(math.log(2 ** -11), math.log(448), 3000)),
+                         (table[1:] + table[:-1]) / 2])              # exact midpoints too
+    xs = xs.astype(np.float32).astype(np.float64)                    # decisions are on fp32 values
+    ref = torch.from_numpy(xs.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert all(O.e4m3_encode_rne(x) == r for x, r in zip(xs, ref))
+    assert O.e4m3_encode_rne(1e6) == 0x7E and O.e4m3_encode_rne(-1e6) == 0xFE
+    for x in xs:                                                     # round up = brute force
+        want = int(np.nonzero(table >= x)[0][0]) if x <= 448 else 0x7E
+        assert O.e4m3_encode_ru(x) == want
+    assert O.e4m3_encode_ru(0.0) == 0 and O.e4m3_encode_ru(1000.0) == 0x7E
+
+
+def test_f16_decode_and_encoders():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    ours = np.array([O.f16_decode(b) for b in range(65536)])
+    fin = np.isfinite(ref)
+    assert np.array_equal(ref[fin], ours[fin]) and np.array_equal(np.isnan(ref), np.isnan(ours))
+    for b in range(0, 65536, 7):
+        if fin[b] and b != 0x8000:
+            assert O.f16_encode_rd(ref[b]) == b and O.f16_encode_rne(ref[b]) == b
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.uniform(-8, 4.8, 2000),
+                         (ref[1:0x7BFF][:-1] + ref[2:0x7BFF]) / 2])   # midpoints
+    xs = xs[np.abs(xs) < 65504.0]                                    # saturation checked below
+    for x in xs:
+        h = np.float16(x)                                            # numpy: correctly rounded
+        assert O.f16_encode_rne(x) == int(np.array(h).view(np.uint16))
+        if float(h) > x:
+            h = np.nextafter(h, np.float16(-np.inf))
+        assert O.f16_encode_rd(x) == int(np.array(h).view(np.uint16))
+    assert O.f16_encode_rd(1e9) == 0x7BFF and O.f16_encode_rd(-1e9) == 0xFBFF
+
+
+def test_f32_round_up():
+    rng = np.random.default_rng(6)
+    for x in rng.standard_normal(2000) * 10.0 ** rng.uniform(-30, 30, 2000):
+        f = np.float32(x)
+        if float(f) < x:
+            f = np.nextafter(f, np.float32(np.inf))
+        assert O.f32_ru(x) == float(f)
+
+
+# ----------------------------------------------------------------- quantiser
+@pytest.mark.parametrize("levels,seed", [(15, 0), (3, 1), (15, 7), (3, 9)])
+def test_quantize_tile_properties(levels, seed):
+    X = key_tile(seed)
+    if levels == 3:
+        X = X / 20.0 + np.sin(np.arange(D))[None, :]
+    tl = O.quantize_tile(X, levels)
+    assert tl.flags == 0
+    g, a, b = tl.g(), tl.a(), tl.b()
+    # gauge: centred log factors, g = E4M3_rne(fp32(exp v))
+    assert abs(tl.v.sum()) < 1e-10
+    assert all(O.e4m3_encode_rne(float(np.float32(math.exp(x)))) == c for x, c in zip(tl.v, tl.g8))
+    Y = tl.R / g[None, :]
+    assert np.abs(tl.R - O.rotate(X)).max() < 1e-12
+    # range coverage: b <= min Y, b + L a >= max Y
+    assert (b <= Y.min(axis=1)).all() and (b + levels * a >= Y.max(axis=1)).all()
+    # codes in range, equal to the brute-force nearest level except at ties
+    assert tl.code.max() <= levels
+    levels_grid = a[:, None, None] * np.arange(levels + 1)[None, None, :] + b[:, None, None]
+    brute = np.abs(Y[:, :, None] - levels_grid).argmin(axis=2)
+    frac = tl.pre - np.floor(tl.pre)
+    near_tie = np.abs(frac - 0.5) < 1e-5
+    assert np.array_equal(brute[~near_tie], tl.code[~near_tie])
+    # round trip within half a step, per element and per token in the original domain
+    recon = a[:, None] * tl.code + b[:, None]
+    assert (np.abs(Y - recon) <= a[:, None] / 2 * (1 + 1e-6)).all()
+    Xh = O.dequantize_record(levels == 3, O.pack_record(levels == 3, tl))
+    bound = 0.5 * np.sqrt(((g[None, :] * a[:, None]) ** 2).sum(axis=1)) * (1 + 1e-6)
+    assert (np.linalg.norm(Xh - X, axis=1) <= bound).all()
+
+
+def test_quantize_degenerate_tiles():
+    z = O.quantize_tile(np.zeros((T, D)), 15)
+    assert (z.g8 == 0x38).all() and (z.a8 == 0x01).all() and (z.b16 == 0).all() and not z.code.any()
+    same = np.repeat(key_tile()[:1], T, axis=0)
+    s = O.quantize_tile(same, 3)
+    assert (s.g8 == 0x38).all()                                      # no column information: g = 1
+    assert (s.code == s.code[0]).all()
+    big = np.zeros((T, D)); big[5, 9] = 3000.0                      # one huge outlier
+    bt = O.quantize_tile(big, 15)
+    assert bt.flags == 0
+    Xh = O.dequantize_record(False, O.pack_record(False, bt))
+    g, a = bt.g(), bt.a()
+    bound = 0.5 * np.sqrt(((g[None, :] * a[:, None]) ** 2).sum(axis=1)) * (1 + 1e-6)
+    assert (np.linalg.norm(Xh - big, axis=1) <= bound).all()
+    # beyond the format: a per-token step above 448 (the largest E4M3 value)
+    # saturates and the codes clamp; the oracle flags it
+    big[5, 9] = 60000.0
+    sat = O.quantize_tile(big, 15)
+    assert sat.flags & O.FLAG_STEP_SAT and sat.flags & O.FLAG_CLAMPED
+    assert sat.a8[5] == 0x7E and sat.code.max() <= 15
+
+
+# ----------------------------------------------------------------- layout
+def test_record_layout_bytes():
+    tl = O.Tile(np.arange(D, dtype=np.uint8), (np.arange(T) * 3 % 256).astype(np.uint8),
+                (np.arange(T) * 517).astype(np.uint16),
+                ((np.arange(T)[:, None] + 3 * np.arange(D)[None, :]) % 16).astype(np.uint8),
+                None, None, None, 0)
+    rk = O.pack_record(False, tl)
+    assert rk.size == 8704 and O.record_bytes(False) == 8704
+    assert rk[5] == 5 and rk[128 + 7] == 21 and rk[256 + 2 * 9] == (9 * 517) & 0xFF
+    assert rk[257 + 2 * 9] == (9 * 517) >> 8
+    t, i = 11, 13                                                    # byte i of token t
+    assert rk[512 + t * 64 + i] == tl.code[t, 2 * i] | (tl.code[t, 2 * i + 1] << 4)
+    tl.code = tl.code % 4
+    rv = O.pack_record(True, tl)
+    assert rv.size == 4608
+    c, j = 77, 6                                                     # byte j of channel c
+    assert rv[512 + c * 32 + j] == sum(int(tl.code[4 * j + k, c]) << (2 * k) for k in range(4))
+    g8, a8, b16, code = O.unpack_record(True, rv)
+    assert np.array_equal(code, tl.code) and np.array_equal(b16, tl.b16)
+
+
+def test_bits_per_element_against_pages():
+    """The pages give ~2.3 bits/element including the dual FP8 scales and
+    FP16 zero-points, for 4-bit keys / 2-bit values per 128-token tile."""
+    with open(os.path.join(GOLDEN, "pages_preset.json")) as f:
+        p = json.load(f)
+    assert p["tile_tokens"] == T and p["k_bits"] == 4 and p["v_bits"] == 2
+    k_bits = O.record_bytes(False) * 8 / (T * D)
+    v_bits = O.record_bytes(True) * 8 / (T * D)
+    assert (k_bits, v_bits) == (4.25, 2.25)
+    assert abs(v_bits - p["effective_bits_per_element"]) < 0.1        # the V side matches ~2.3
+    assert 3 <= 16 / ((k_bits + v_bits) / 2) <= 5                    # "3-5x" capacity
+
+
+# ----------------------------------------------------------------- attention
+def test_attention_closed_forms():
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((3, D))
+    k1, v1 = rng.standard_normal((1, D)), rng.standard_normal((1, D))
+    assert np.abs(O.attention(q, k1, v1, 0.1) - v1).max() < 1e-15      # one token: o = v
+    K = np.repeat(k1, 9, axis=0); V = rng.standard_normal((9, D))
+    assert np.abs(O.attention(q, K, V, 0.1) - V.mean(0)).max() < 1e-14  # equal keys: mean
+    assert not O.attention(q, np.zeros((0, D)), np.zeros((0, D)), 0.1).any()
+
+
+def test_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((4, D)); K = rng.standard_normal((37, D)) * 3; V = rng.standard_normal((37, D))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=0.3)[0]
+    assert np.abs(O.attention(q, K, V, 0.3) - ref.numpy()).max() < 1e-13
+
+
+@pytest.mark.parametrize("n_tiles,n_tail", [(1, 0), (2, 37), (0, 5), (3, 127)])
+def test_folded_attention_equals_plain(n_tiles, n_tail):
+    rng = np.random.default_rng(10 + n_tiles)
+    krec, vrec, Ks, Vs = [], [], [], []
+    for i in range(n_tiles):
+        Xk = key_tile(20 + i); Xv = rng.standard_normal((T, D))
+        krec.append(O.pack_record(False, O.quantize_tile(Xk, 15)))
+        vrec.append(O.pack_record(True, O.quantize_tile(Xv, 3)))
+        Ks.append(O.dequantize_record(False, krec[-1])); Vs.append(O.dequantize_record(True, vrec[-1]))
+    kt = rng.standard_normal((n_tail, D)); vt = rng.standard_normal((n_tail, D))
+    q = rng.standard_normal((8, D))
+    K = np.concatenate(Ks + [kt]); V = np.concatenate(Vs + [vt])
+    plain = O.attention(q, K, V, 1 / math.sqrt(D))
+    folded = O.attention_folded(q, krec, vrec, kt, vt, 1 / math.sqrt(D))
+    assert np.abs(plain - folded).max() < 1e-9
+
+
+def test_batch_drivers_agree_with_single_calls():
+    w = I.qwen3_4b()
+    k = I.kv_values(w, "k", 0, 0, 2 * T).view(torch.int16).numpy().view(np.uint16)   # [256, 8, 128]
+    first = np.array([0 * D, 3 * D, T * 8 * D + 5 * D], np.int64)                     # (tile, head)
+    rec, flags = O.quantize_batch(k, "bf16", first, 8 * D, False, nthreads=2)
+    flat = k.reshape(-1)
+    for i, f in enumerate(first):
+        X = O.decode16(np.stack([flat[f + r * 8 * D: f + r * 8 * D + D] for r in range(T)]), "bf16")
+        assert np.array_equal(rec[i], O.pack_record(False, O.quantize_tile(X, 15)))
+    assert not flags.any()
