@@ -1,0 +1,180 @@
+// common.cuh -- device helpers shared by the KVarN kernels (sm_103a).
+//
+// Inline-PTX wrappers for the warp-level tensor-core MMA (m16n8k16, fp32
+// accumulate), ldmatrix, 16-byte cp.async, 1-D bulk copies completed on an
+// mbarrier, and the FP8 E4M3 / FP16 conversions the packed format needs.
+#pragma once
+
+#include <cstdint>
+#include <type_traits>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "../../include/kvarn.h"
+
+namespace kvarn {
+
+constexpr int D = 128;               // channels per token (head_dim)
+constexpr int T = 128;               // tokens per tile (one paged block)
+constexpr int K_REC = 8704;          // 512 B header + 128 x 64 B of 4-bit codes
+constexpr int V_REC = 4608;          // 512 B header + 128 x 32 B of 2-bit codes
+constexpr int HEAD_REC = K_REC + V_REC;
+constexpr float INV_SQRT_D = 0.08838834764831845f;  // 1/sqrt(128)
+
+// First error wins; the failing unit skips its work.  Never traps, never waits.
+__device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------------------------ MMA
+// Bits of +1.0 in the 16-bit element type E.
+template <typename E> struct Bits16;
+template <> struct Bits16<__half> { static constexpr uint32_t one = 0x3C00u; };
+template <> struct Bits16<__nv_bfloat16> { static constexpr uint32_t one = 0x3F80u; };
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <typename E>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same_v<E, __half>) mma_f16(c, a, b0, b1);
+  else mma_bf16(c, a, b0, b1);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+
+// ------------------------------------------------------------------ copies
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::);
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes));
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(smem)),
+      "l"(gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false (and the error word set) if the phase never completes.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* err) {
+  for (int i = 0; i < (1 << 22); ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  set_error(err, KVARN_DEV_ERR_TIMEOUT);
+  return false;
+}
+
+// ------------------------------------------------------------------ formats
+__device__ __forceinline__ float e4m3_to_float(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Two E4M3 bytes (low byte first) -> two floats.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  return __half22float2(__half2(h));
+}
+
+// Round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint8_t float_to_e4m3_rn(float x) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Smallest E4M3 value >= x for x >= 0, saturating at 448 (code 0x7E).
+__device__ __forceinline__ uint8_t float_to_e4m3_ru(float x) {
+  if (!(x > 0.f)) return 0;
+  if (x >= 448.f) return 0x7E;
+  uint8_t c = float_to_e4m3_rn(x);
+  if (e4m3_to_float(c) < x) ++c;  // the next code is the next value up
+  return c;
+}
+
+// Reductions over the 4 lanes of a quad (lanes 4k .. 4k+3).
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+__device__ __forceinline__ float quad_min(float x) {
+  x = fminf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fminf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+__device__ __forceinline__ float quad_max(float x) {
+  x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 1));
+  return fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 2));
+}
+
+// fp32 -> 16-bit bits of E, round to nearest even.
+template <typename E>
+__device__ __forceinline__ uint16_t f2bits(float x) {
+  if constexpr (std::is_same_v<E, __half>) return __half_as_ushort(__float2half_rn(x));
+  else return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+template <typename E>
+__device__ __forceinline__ float bits2f(uint16_t b) {
+  if constexpr (std::is_same_v<E, __half>) return __half2float(__ushort_as_half(b));
+  else return __bfloat162float(__ushort_as_bfloat16(b));
+}
+// x -> (hi, lo) in E with hi + lo = x to within E's precision squared.
+template <typename E>
+__device__ __forceinline__ void split_hl(float x, uint16_t& hi, uint16_t& lo) {
+  hi = f2bits<E>(x);
+  lo = f2bits<E>(x - bits2f<E>(hi));
+}
+__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+
+}  // namespace kvarn

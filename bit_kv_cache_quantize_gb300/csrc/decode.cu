@@ -1,0 +1,699 @@
+// decode.cu -- read path of the KVarN cache: split-K paged decode attention
+// over packed 4-bit K / 2-bit V tiles plus the raw open tile, the split-K
+// combine (with the single inverse rotation), and a 16-bit paged decode
+// kernel on the same shapes as a comparison point.
+//
+// Scales are applied at read time (page "Huawei's KVarN puts KV-cache
+// quantization inside vLLM's backend", section "The four-stage pipeline",
+// fourth stage).  With R[t][c] = g[c] (a[t] code + b[t]) and K = R H:
+//   score_t = scale <q, k_t> = a_t <qg, code_t> + b_t S,  qg = (q H scale) * gK,
+//                                                       S = sum_c qg[c]
+//   sum_t p_t v_t = (gV * (sum_t p_t a_t code_t + sum_t p_t b_t)) H
+// so the key rotation and per-channel key scales fold into the query once
+// per tile, the per-token scale/zero into the scores, the per-channel value
+// scales into the accumulator, and one inverse rotation (in the combine)
+// finishes the output.
+//
+// The two contractions per tile (QK: 128 tokens x 128 channels x G queries,
+// PV: 128 channels x 128 tokens x G queries) run as warp MMAs m16n8k16 with
+// the codes unpacked in registers straight into the fragments: rows 0-7 of
+// the A operand are the fp16 high parts of the G <= 8 queries (or
+// probabilities), rows 8-15 their fp16 low parts, so each product is exact
+// to ~2^-22 while the 4-/2-bit codes are exact small integers.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "params.h"
+
+namespace kvarn {
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int PART = D + 2;  // floats per split-K partial: m, l, acc[128]
+
+
+__device__ __forceinline__ float* part_ptr(const DecodeParams& p, int b, int h, int chunk, int g) {
+  return p.ws + ((((int64_t)b * p.num_kv_heads + h) * (p.n_chunks + 1) + chunk) * p.G + g) * PART;
+}
+
+
+// Two fp16 codes (1024 + c) in a half2 -> exact (c0, c1).
+__device__ __forceinline__ uint32_t unbias(uint32_t x) {
+  __half2 h = *reinterpret_cast<__half2*>(&x);
+  h = __hsub2(h, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t nib2(uint32_t w, int s) { return unbias(((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u); }
+__device__ __forceinline__ uint32_t crumb2(uint32_t w, int s) { return unbias(((w >> (2 * s)) & 0x00030003u) | 0x64006400u); }
+
+
+template <typename E>
+__device__ __forceinline__ float to_f(E x) {
+  if constexpr (std::is_same_v<E, __half>) return __half2float(x);
+  else return __bfloat162float(x);
+}
+
+// Shared memory of one packed-decode CTA: per warp two stages of one
+// (tile, head) record pair (K 8704 B + V 4608 B), the rotated queries, and
+// the cross-warp merge area (aliases the stages at the end).
+constexpr int DEC_WARPS = 4;
+constexpr int DEC_STAGES = 2;
+struct DecSmem {
+  alignas(128) unsigned char stage[DEC_WARPS][DEC_STAGES][HEAD_REC];
+  alignas(16) float qr[8][D];
+  uint64_t bar[DEC_WARPS][DEC_STAGES];
+};
+struct DecMerge {
+  float m[DEC_WARPS][8];
+  float l[DEC_WARPS][8];
+  float acc[DEC_WARPS][8][D];
+};
+static_assert(sizeof(DecMerge) <= sizeof(DecSmem::stage), "merge area must fit the stages");
+
+template <typename E>
+__device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
+
+// grid (n_chunks + 1, H_kv, B); chunk n_chunks handles the raw open tile.
+template <typename E>
+__global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
+  const int len = p.seq_lens[b];
+  if (len < 0 || len > T * p.max_blocks) {
+    if (tid == 0 && chunk == 0 && h == 0) set_error(p.err, KVARN_DEV_ERR_TOKEN_RANGE);
+    return;
+  }
+  if (chunk == p.n_chunks) {
+    tail_chunk<E>(p, b, h, len, smem_raw);
+    return;
+  }
+  const int n_closed = len / T;
+  const int first = chunk * p.chunk_tiles;
+  const int n_tiles = min(p.chunk_tiles, n_closed - first);
+  if (n_tiles <= 0) return;
+  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw);
+  const int G = p.G;
+
+  // per-warp barriers
+  if (lane == 0) {
+    for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
+    fence_mbar_init();
+  }
+  // rotated, scaled queries: qr[g][c] = scale * log2(e) * sum_k q[g][k] H[k][c]
+  {
+    const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
+    float* qraw = &sm.qr[0][0];  // temporarily holds the raw queries
+    for (int i = tid; i < 8 * D; i += 128) qraw[i] = (i < G * D) ? to_f(qb[i]) : 0.f;
+    __syncthreads();
+    float acc[8];
+#pragma unroll
+    for (int gg = 0; gg < 8; ++gg) acc[gg] = 0.f;
+    const int c = tid;
+    for (int k = 0; k < D; ++k) {
+      const float sgn = (__popc(k & c) & 1) ? -1.f : 1.f;
+#pragma unroll
+      for (int gg = 0; gg < 8; ++gg) acc[gg] = fmaf(sgn, qraw[gg * D + k], acc[gg]);
+    }
+    __syncthreads();
+    const float f = p.scale * LOG2E * INV_SQRT_D;
+#pragma unroll
+    for (int gg = 0; gg < 8; ++gg) sm.qr[gg][c] = acc[gg] * f;
+    __syncthreads();
+  }
+  float qreg[32];  // query g, channels 32j .. 32j+31
+#pragma unroll
+  for (int c = 0; c < 32; c += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(&sm.qr[g][32 * j + c]);
+    qreg[c] = v.x; qreg[c + 1] = v.y; qreg[c + 2] = v.z; qreg[c + 3] = v.w;
+  }
+
+  // tiles of this warp: first + warp, first + warp + 4, ...
+  const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
+  const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
+  auto issue = [&](int k) {  // lane 0: start the copy of this warp's k-th tile
+    const int tile = first + warp + k * DEC_WARPS;
+    const int32_t blk = tab[tile];
+    const int s = k % DEC_STAGES;
+    if (blk >= 0 && blk < p.num_blocks) {
+      mbar_expect_tx(&sm.bar[warp][s], HEAD_REC);
+      bulk_g2s(sm.stage[warp][s], p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC, HEAD_REC, &sm.bar[warp][s]);
+    } else {
+      set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.bar[warp][s])) : "memory");
+    }
+  };
+  __syncwarp();
+  if (lane == 0)
+    for (int k = 0; k < min(my_n, DEC_STAGES); ++k) issue(k);
+
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[16][2];
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
+
+  for (int k = 0; k < my_n; ++k) {
+    const int s = k % DEC_STAGES;
+    const int tile = first + warp + k * DEC_WARPS;
+    const int32_t blk = tab[tile];
+    const bool ok = mbar_wait_bounded(&sm.bar[warp][s], (k / DEC_STAGES) & 1, p.err);
+    if (ok && blk >= 0 && blk < p.num_blocks) {
+      const unsigned char* krec = sm.stage[warp][s];
+      const unsigned char* vrec = krec + K_REC;
+
+      // ---- query fold: qg = q' * gK (channels 32j..32j+31), S, per-query scale
+      uint32_t afr[8][4];
+      float S, qs_inv;
+      {
+        float qg[32];
+        const uint4 g0 = *reinterpret_cast<const uint4*>(krec + 32 * j);
+        const uint4 g1 = *reinterpret_cast<const uint4*>(krec + 32 * j + 16);
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float ssum = 0.f, amax = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float2 lo = e4m3x2_to_float2((uint16_t)(gw[w] & 0xFFFF));
+          const float2 hi = e4m3x2_to_float2((uint16_t)(gw[w] >> 16));
+          qg[4 * w] = qreg[4 * w] * lo.x; qg[4 * w + 1] = qreg[4 * w + 1] * lo.y;
+          qg[4 * w + 2] = qreg[4 * w + 2] * hi.x; qg[4 * w + 3] = qreg[4 * w + 3] * hi.y;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) { ssum += qg[4 * w + e]; amax = fmaxf(amax, fabsf(qg[4 * w + e])); }
+        }
+        S = quad_sum(ssum);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        // power-of-two scale putting max |qg| in [512, 1024): exact, keeps the low parts normal
+        int ex = 0;
+        if (amax > 0.f) frexpf(amax, &ex);
+        const float qs = ldexpf(1.f, 10 - ex);
+        qs_inv = ldexpf(1.f, ex - 10);
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          const int w = kb >> 1, sh = 2 * (kb & 1);
+          const int c0 = 8 * w + sh, c1 = c0 + 4;  // local channels of b0; b1 uses c0+1, c1+1
+          uint16_t h00, l00, h01, l01, h10, l10, h11, l11;
+          split_hl<__half>(qg[c0] * qs, h00, l00); split_hl<__half>(qg[c1] * qs, h01, l01);
+          split_hl<__half>(qg[c0 + 1] * qs, h10, l10); split_hl<__half>(qg[c1 + 1] * qs, h11, l11);
+          afr[kb][0] = pack2(h00, h01);
+          afr[kb][1] = pack2(l00, l01);
+          afr[kb][2] = pack2(h10, h11);
+          afr[kb][3] = pack2(l10, l11);
+        }
+      }
+
+      // ---- QK: n-block nb covers tokens 32*(n>>1) + off(nb) + 8*(n&1), n = 0..7
+      float sc[16][2];  // scores (log2 units) of tokens 32j + off(nb) (+8)
+      float tmax = -INFINITY;
+      {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(krec + 128 + 32 * j);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(krec + 128 + 32 * j + 16);
+        const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const __half* bz = reinterpret_cast<const __half*>(krec + 256) + 32 * j;
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb) {
+          const int off = nb < 8 ? nb : nb + 8;
+          const int tok = 32 * (g >> 1) + off + 8 * (g & 1);
+          const uint4 kw = *reinterpret_cast<const uint4*>(krec + 512 + tok * 64 + 16 * j);
+          const uint32_t kwa[4] = {kw.x, kw.y, kw.z, kw.w};
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) {
+            const uint32_t x = kwa[kb >> 1];
+            const int sh = 2 * (kb & 1);
+            mma_f16(c, afr[kb], nib2(x, sh), nib2(x, sh + 1));
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int r = off + 8 * e;  // local token index 0..31
+            const float a = e4m3_to_float((uint8_t)(aw[r >> 2] >> (8 * (r & 3))));
+            const float bzv = __half2float(bz[r]);
+            const float dot = (c[e] + c[2 + e]) * qs_inv;
+            sc[nb][e] = fmaf(a, dot, bzv * S);
+            tmax = fmaxf(tmax, sc[nb][e]);
+          }
+        }
+      }
+
+      // ---- online softmax (log2 domain)
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float m_new = fmaxf(m_run, tmax);
+      const float corr = exp2f(m_run - m_new);
+      m_run = m_new;
+
+      // ---- PV: A = p * aV (hi rows 0-7, lo rows 8-15), B = 2-bit V codes
+      uint32_t pfr[8][4];
+      float psum = 0.f, pb = 0.f;
+      {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(vrec + 128 + 32 * j);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(vrec + 128 + 32 * j + 16);
+        const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        const __half* bz = reinterpret_cast<const __half*>(vrec + 256) + 32 * j;
+        uint16_t ph[16][2], pl[16][2];
+#pragma unroll
+        for (int nb = 0; nb < 16; ++nb) {
+          const int off = nb < 8 ? nb : nb + 8;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int r = off + 8 * e;
+            const float pr = exp2f(sc[nb][e] - m_new);
+            psum += pr;
+            pb = fmaf(pr, __half2float(bz[r]), pb);
+            const float pa = pr * e4m3_to_float((uint8_t)(aw[r >> 2] >> (8 * (r & 3))));
+            split_hl<__half>(pa, ph[nb][e], pl[nb][e]);
+          }
+        }
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          pfr[kb][0] = pack2(ph[2 * kb][0], ph[2 * kb][1]);
+          pfr[kb][1] = pack2(pl[2 * kb][0], pl[2 * kb][1]);
+          pfr[kb][2] = pack2(ph[2 * kb + 1][0], ph[2 * kb + 1][1]);
+          pfr[kb][3] = pack2(pl[2 * kb + 1][0], pl[2 * kb + 1][1]);
+        }
+      }
+      psum = quad_sum(psum);
+      pb = quad_sum(pb);
+      l_run = l_run * corr + psum;
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb) {
+        const uint2 vw = *reinterpret_cast<const uint2*>(vrec + 512 + (8 * nb + g) * 32 + 8 * j);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          const int pr = 2 * kb;  // QK n-block pair (2kb) -> b0, (2kb+1) -> b1
+          const uint32_t x = (pr >> 3) ? vw.y : vw.x;
+          mma_f16(c, pfr[kb], crumb2(x, pr & 7), crumb2(x, (pr & 7) + 1));
+        }
+        const float2 gv = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vrec + 8 * nb + 2 * j));
+        acc[nb][0] = fmaf(acc[nb][0], corr, gv.x * (c[0] + c[2] + pb));
+        acc[nb][1] = fmaf(acc[nb][1], corr, gv.y * (c[1] + c[3] + pb));
+      }
+    }
+    __syncwarp();
+    if (k + DEC_STAGES < my_n && lane == 0) {
+      fence_proxy_async();
+      issue(k + DEC_STAGES);
+    }
+  }
+
+  // ---- merge the 4 warps and write this CTA's partial
+  __syncthreads();
+  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.stage);
+  if (j == 0) { mg.m[warp][g] = m_run; mg.l[warp][g] = l_run; }
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) {
+    mg.acc[warp][g][8 * nb + 2 * j] = acc[nb][0];
+    mg.acc[warp][g][8 * nb + 2 * j + 1] = acc[nb][1];
+  }
+  __syncthreads();
+  for (int gg = 0; gg < G; ++gg) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, mg.m[w][gg]);
+    float Lsum = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < DEC_WARPS; ++w) {
+        const float f = exp2f(mg.m[w][gg] - M);
+        Lsum += f * mg.l[w][gg];
+        A += f * mg.acc[w][gg][tid];
+      }
+    }
+    float* out = part_ptr(p, b, h, chunk, gg);
+    if (tid == 0) { out[0] = M; out[1] = Lsum; }
+    out[2 + tid] = A;
+  }
+}
+
+// Raw open tile of (b, h): len % 128 tokens in 16-bit, unrotated query.
+template <typename E>
+__device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem) {
+  const int n = len % T;
+  if (n == 0) return;
+  const int tid = threadIdx.x, G = p.G;
+  float* qs = reinterpret_cast<float*>(smem);  // [8][128]
+  float* pr = qs + 8 * D;                      // [8][128] scores, then probabilities
+  float* ml = pr + 8 * T;                      // [8][2]
+  const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
+  const float f = p.scale * LOG2E;
+  for (int i = tid; i < G * D; i += 128) qs[i] = to_f(qb[i]) * f;
+  __syncthreads();
+  const E* kt = static_cast<const E*>(p.tail) + (((int64_t)b * p.num_kv_heads + h) * 2 + 0) * (T * D);
+  const E* vt = kt + T * D;
+  if (tid < n) {
+    float s[8];
+#pragma unroll
+    for (int gg = 0; gg < 8; ++gg) s[gg] = 0.f;
+    for (int c = 0; c < D; ++c) {
+      const float kv = to_f(kt[tid * D + c]);
+#pragma unroll
+      for (int gg = 0; gg < 8; ++gg)
+        if (gg < G) s[gg] = fmaf(qs[gg * D + c], kv, s[gg]);
+    }
+    for (int gg = 0; gg < G; ++gg) pr[gg * T + tid] = s[gg];
+  }
+  __syncthreads();
+  if (tid < G) {
+    float m = -INFINITY, l = 0.f;
+    for (int t = 0; t < n; ++t) m = fmaxf(m, pr[tid * T + t]);
+    for (int t = 0; t < n; ++t) {
+      const float e = exp2f(pr[tid * T + t] - m);
+      pr[tid * T + t] = e;
+      l += e;
+    }
+    ml[2 * tid] = m;
+    ml[2 * tid + 1] = l;
+  }
+  __syncthreads();
+  float a[8];
+#pragma unroll
+  for (int gg = 0; gg < 8; ++gg) a[gg] = 0.f;
+  for (int t = 0; t < n; ++t) {
+    const float v = to_f(vt[t * D + tid]);
+#pragma unroll
+    for (int gg = 0; gg < 8; ++gg)
+      if (gg < G) a[gg] = fmaf(pr[gg * T + t], v, a[gg]);
+  }
+  for (int gg = 0; gg < G; ++gg) {
+    float* out = part_ptr(p, b, h, p.n_chunks, gg);
+    if (tid == 0) { out[0] = ml[2 * gg]; out[1] = ml[2 * gg + 1]; }
+    out[2 + tid] = a[gg];
+  }
+}
+
+// One warp per (sequence, query head): merge the split-K partials, apply
+// the inverse rotation to the packed-tile part, add the raw part, normalise.
+__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p, int rotate, int batch, float* __restrict__ out) {
+  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (wid >= batch * p.num_q_heads) return;
+  const int b = wid / p.num_q_heads, hq = wid % p.num_q_heads;
+  const int h = hq / p.G, g = hq % p.G;
+  const int len = p.seq_lens[b];
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (len > 0 && len <= T * p.max_blocks) {
+    const int n_tc = rotate ? ((len / T) + p.chunk_tiles - 1) / p.chunk_tiles
+                            : (((len + T - 1) / T) + p.chunk_tiles - 1) / p.chunk_tiles;
+    const bool has_tail = rotate && (len % T) != 0;
+    float M = -INFINITY;
+    for (int i = 0; i < n_tc; ++i) M = fmaxf(M, part_ptr(p, b, h, i, g)[0]);
+    if (has_tail) M = fmaxf(M, part_ptr(p, b, h, p.n_chunks, g)[0]);
+    float Lsum = 0.f;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = 0; i < n_tc; ++i) {
+      const float* pp = part_ptr(p, b, h, i, g);
+      const float f = (pp[0] == -INFINITY) ? 0.f : exp2f(pp[0] - M);
+      Lsum += f * pp[1];
+      const float4 a = *reinterpret_cast<const float4*>(pp + 2 + 4 * lane);
+      x[0] += f * a.x; x[1] += f * a.y; x[2] += f * a.z; x[3] += f * a.w;
+    }
+    if (rotate) {  // x = x H over the 128 channels held 4 per lane
+      float u = x[0], v = x[1];
+      x[0] = u + v; x[1] = u - v;
+      u = x[2]; v = x[3];
+      x[2] = u + v; x[3] = u - v;
+      u = x[0]; v = x[2];
+      x[0] = u + v; x[2] = u - v;
+      u = x[1]; v = x[3];
+      x[1] = u + v; x[3] = u - v;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float other = __shfl_xor_sync(0xffffffffu, x[e], m);
+          x[e] = upper ? (other - x[e]) : (x[e] + other);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] *= INV_SQRT_D;
+    }
+    if (has_tail) {
+      const float* pp = part_ptr(p, b, h, p.n_chunks, g);
+      const float f = exp2f(pp[0] - M);
+      Lsum += f * pp[1];
+      const float4 a = *reinterpret_cast<const float4*>(pp + 2 + 4 * lane);
+      x[0] += f * a.x; x[1] += f * a.y; x[2] += f * a.z; x[3] += f * a.w;
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    o = make_float4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
+  }
+  *reinterpret_cast<float4*>(out + ((int64_t)b * p.num_q_heads + hq) * D + 4 * lane) = o;
+}
+
+// ------------------------------------------------------------------ 16-bit comparison kernel
+// Pool block = [kv_head][K,V][128 tokens][128 channels] 16-bit.  Each tile is
+// loaded by TMA as four 64-channel x 128-token boxes with the 128-byte
+// swizzle; 8 warps each take 16 tokens of every tile.
+constexpr int F16_WARPS = 8;
+constexpr int F16_STAGES = 3;
+constexpr int F16_TILE = 2 * T * D * 2;  // K + V, 64 KB
+struct F16Smem {
+  alignas(1024) unsigned char stage[F16_STAGES][F16_TILE];
+  uint64_t bar[F16_STAGES];
+};
+struct F16Merge {
+  float m[F16_WARPS][8];
+  float l[F16_WARPS][8];
+  float acc[F16_WARPS][8][D];
+};
+static_assert(sizeof(F16Merge) <= sizeof(F16Smem::stage), "merge area must fit the stages");
+
+// Byte offset of 16-byte chunk `ch` (0..15) of row r in a swizzled K or V
+// matrix made of two 64-channel boxes of 128 rows x 128 B.
+__device__ __forceinline__ int f16_off(int r, int ch) {
+  return (ch >> 3) * (T * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(256, 1) decode_f16_kernel(const __grid_constant__ CUtensorMap tmap, DecodeParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_f16[];
+  // the 128-byte TMA swizzle needs 1024-byte aligned boxes: align explicitly
+  const uint32_t base = smem_u32(smem_f16);
+  F16Smem& sm = *reinterpret_cast<F16Smem*>(smem_f16 + (((base + 1023u) & ~1023u) - base));
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
+  const int len = p.seq_lens[b];
+  if (len < 0 || len > T * p.max_blocks) {
+    if (tid == 0 && chunk == 0 && h == 0) set_error(p.err, KVARN_DEV_ERR_TOKEN_RANGE);
+    return;
+  }
+  const int n_all = (len + T - 1) / T;
+  const int first = chunk * p.chunk_tiles;
+  const int n_tiles = min(p.chunk_tiles, n_all - first);
+  if (n_tiles <= 0) return;
+  const int G = p.G;
+  const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
+
+  if (tid == 0) {
+    for (int s = 0; s < F16_STAGES; ++s) mbar_init(&sm.bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  auto issue = [&](int k) {  // thread 0
+    const int s = k % F16_STAGES;
+    const int32_t blk = tab[first + k];
+    if (blk >= 0 && blk < p.num_blocks) {
+      mbar_expect_tx(&sm.bar[s], F16_TILE);
+      const int row0 = ((blk * p.num_kv_heads + h) * 2) * T;
+#pragma unroll
+      for (int part = 0; part < 4; ++part) {  // K lo, K hi, V lo, V hi
+        const int x = (part & 1) * 64, y = row0 + (part >> 1) * T;
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+                smem_u32(sm.stage[s] + part * (T * 128))),
+            "l"(&tmap), "r"(x), "r"(y), "r"(smem_u32(&sm.bar[s]))
+            : "memory");
+      }
+    } else {
+      set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.bar[s])) : "memory");
+    }
+  };
+  if (tid == 0)
+    for (int k = 0; k < min(n_tiles, F16_STAGES); ++k) issue(k);
+
+  // query fragments: rows 0-7 = queries (exact 16-bit), rows 8-15 zero
+  uint32_t qa[8][2];
+  {
+    const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c = 16 * kb + 2 * j + 8 * hh;
+        qa[kb][hh] = (g < G) ? *reinterpret_cast<const uint32_t*>(qb + g * D + c) : 0u;
+      }
+  }
+  const float sl2 = p.scale * LOG2E;
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[16][4];
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
+
+  for (int k = 0; k < n_tiles; ++k) {
+    const int s = k % F16_STAGES;
+    const int32_t blk = tab[first + k];
+    const bool ok = mbar_wait_bounded(&sm.bar[s], (k / F16_STAGES) & 1, p.err);
+    const int valid = min(T, len - (first + k) * T);
+    if (ok && blk >= 0 && blk < p.num_blocks && 16 * warp < valid) {
+      const unsigned char* kt = sm.stage[s];
+      const unsigned char* vt = kt + 2 * T * 128;
+      // QK for tokens 16w .. 16w+15 (two n-blocks)
+      float sc[2][4];
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {  // channel chunks 4kp .. 4kp+3 (k-blocks 2kp, 2kp+1)
+          uint32_t r[4];
+          const int row = 16 * warp + 8 * nb + (lane & 7);
+          ldmatrix_x4(r, kt + f16_off(row, 4 * kp + (lane >> 3)));
+          const uint32_t a0[4] = {qa[2 * kp][0], 0u, qa[2 * kp][1], 0u};
+          const uint32_t a1[4] = {qa[2 * kp + 1][0], 0u, qa[2 * kp + 1][1], 0u};
+          mma16816<E>(c, a0, r[0], r[1]);
+          mma16816<E>(c, a1, r[2], r[3]);
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = 16 * warp + 8 * nb + 2 * j + (e & 1);
+          sc[nb][e] = (tok < valid) ? c[e] * sl2 : -INFINITY;
+        }
+      }
+      float tmax = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+      const float m_new = fmaxf(m_run, tmax);
+      const float corr = exp2f(m_run - m_new);
+      m_run = m_new;
+      uint16_t ph[2][2], pl[2][2];
+      float psum = 0.f;
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pr = exp2f(sc[nb][e] - m_new);
+          psum += pr;
+          split_hl<E>(pr, ph[nb][e], pl[nb][e]);
+        }
+      psum = quad_sum(psum);
+      l_run = l_run * corr + psum;
+      const uint32_t pa[4] = {pack2(ph[0][0], ph[0][1]), pack2(pl[0][0], pl[0][1]), pack2(ph[1][0], ph[1][1]),
+                              pack2(pl[1][0], pl[1][1])};
+      // PV: tokens 16w .. 16w+15 (one k-block) x 128 channels
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {  // channel n-blocks 2np, 2np+1
+        uint32_t r[4];
+        const int row = 16 * warp + (lane & 7) + 8 * ((lane >> 3) & 1);
+        ldmatrix_x4_trans(r, vt + f16_off(row, 2 * np + (lane >> 4)));
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816<E>(c0, pa, r[0], r[1]);
+        mma16816<E>(c1, pa, r[2], r[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[2 * np][e] = fmaf(acc[2 * np][e], corr, c0[e]);
+          acc[2 * np + 1][e] = fmaf(acc[2 * np + 1][e], corr, c1[e]);
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && k + F16_STAGES < n_tiles) {
+      fence_proxy_async();
+      issue(k + F16_STAGES);
+    }
+  }
+
+  F16Merge& mg = *reinterpret_cast<F16Merge*>(sm.stage);
+  if (j == 0) { mg.m[warp][g] = m_run; mg.l[warp][g] = l_run; }
+#pragma unroll
+  for (int nb = 0; nb < 16; ++nb) {
+    mg.acc[warp][g][8 * nb + 2 * j] = acc[nb][0] + acc[nb][2];
+    mg.acc[warp][g][8 * nb + 2 * j + 1] = acc[nb][1] + acc[nb][3];
+  }
+  __syncthreads();
+  for (int i = tid; i < G * D; i += 256) {
+    const int gg = i / D, c = i % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < F16_WARPS; ++w) M = fmaxf(M, mg.m[w][gg]);
+    float Lsum = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < F16_WARPS; ++w) {
+        const float f = exp2f(mg.m[w][gg] - M);
+        Lsum += f * mg.l[w][gg];
+        A += f * mg.acc[w][gg][c];
+      }
+    }
+    float* o = part_ptr(p, b, h, chunk, gg);
+    if (c == 0) { o[0] = M; o[1] = Lsum; }
+    o[2 + c] = A;
+  }
+}
+
+// ------------------------------------------------------------------ launchers
+size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int chunk_tiles) {
+  const int n_chunks = (max_blocks + chunk_tiles - 1) / chunk_tiles;
+  return (size_t)batch * num_kv_heads * (n_chunks + 1) * G * PART * sizeof(float);
+}
+
+template <typename E>
+static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
+  const size_t smem = sizeof(DecSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 128, smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int warps = batch * p.num_q_heads;
+  combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, 1, batch, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
+  return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, batch, out, s)
+                                   : launch_decode_t<__half>(p, batch, out, s);
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+template <typename E>
+static cudaError_t launch_f16_t(DecodeParams p, const void* pool16, int batch, float* out, cudaStream_t s) {
+  auto encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.num_blocks * p.num_kv_heads * 2 * T};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)T};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(&tmap, std::is_same_v<E, __half> ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      2, const_cast<void*>(pool16), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const size_t smem = sizeof(F16Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(decode_f16_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_f16_kernel<E><<<dim3(p.n_chunks, p.num_kv_heads, batch), 256, smem, s>>>(tmap, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int warps = batch * p.num_q_heads;
+  combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, 0, batch, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,
+                              cudaStream_t s) {
+  return dtype == KVARN_DTYPE_BF16 ? launch_f16_t<__nv_bfloat16>(p, pool16, batch, out, s)
+                                   : launch_f16_t<__half>(p, pool16, batch, out, s);
+}
+
+}  // namespace kvarn

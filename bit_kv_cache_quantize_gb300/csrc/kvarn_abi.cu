@@ -1,0 +1,167 @@
+// kvarn_abi.cu -- the extern "C" entry points declared in include/kvarn.h:
+// host-side validation, launch configuration and status codes.  No
+// allocation, no global state, no exceptions across the boundary.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/kvarn.h"
+
+#include "params.h"
+
+namespace kvarn {
+constexpr int kHeadRec = 13312;
+constexpr int kChunkTiles = 16;  // packed tiles per split-K CTA
+constexpr int kF16ChunkTiles = 16;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by every entry point.
+static kvarn_status check_config(const kvarn_config* c) {
+  if (!c) return KVARN_ERR_INVALID;
+  if (c->num_kv_heads < 1 || c->num_q_heads < 1 || c->num_blocks < 0 || c->sinkhorn_iters < 0 ||
+      c->sinkhorn_iters > 64 || c->head_dim < 1 || c->tile_tokens < 1)
+    return KVARN_ERR_INVALID;
+  if (c->num_q_heads % c->num_kv_heads) return KVARN_ERR_INVALID;
+  if (c->dtype != KVARN_DTYPE_F16 && c->dtype != KVARN_DTYPE_BF16) return KVARN_ERR_INVALID;
+  if (c->head_dim != 128 || c->tile_tokens != 128 || c->k_bits != 4 || c->v_bits != 2) return KVARN_ERR_UNSUPPORTED;
+  if (c->num_q_heads / c->num_kv_heads > 8) return KVARN_ERR_UNSUPPORTED;
+  return KVARN_OK;
+}
+
+static kvarn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVARN_OK : KVARN_ERR_CUDA; }
+}  // namespace kvarn
+
+using namespace kvarn;
+
+extern "C" {
+
+size_t kvarn_block_bytes(const kvarn_config* cfg) {
+  if (check_config(cfg) != KVARN_OK) return 0;
+  return static_cast<size_t>(cfg->num_kv_heads) * kHeadRec;
+}
+
+size_t kvarn_tail_bytes(const kvarn_config* cfg, int32_t batch) {
+  if (check_config(cfg) != KVARN_OK || batch < 0) return 0;
+  return static_cast<size_t>(batch) * cfg->num_kv_heads * 2 * 128 * 128 * 2;
+}
+
+size_t kvarn_fp16_block_bytes(const kvarn_config* cfg) {
+  if (check_config(cfg) != KVARN_OK) return 0;
+  return static_cast<size_t>(cfg->num_kv_heads) * 2 * 128 * 128 * 2;
+}
+
+size_t kvarn_decode_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks) {
+  if (check_config(cfg) != KVARN_OK || batch < 0 || max_blocks < 1) return 0;
+  const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  const size_t a = decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles);
+  const size_t b = decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kF16ChunkTiles);
+  return a > b ? a : b;
+}
+
+kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const void* v, int64_t token_stride_elems,
+                                  int64_t n_tokens, const int64_t* tile_first_token, const int32_t* tile_dst_block,
+                                  int32_t n_tiles, void* block_pool, int32_t* dev_err, void* stream) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (n_tiles < 0 || n_tokens < 0) return KVARN_ERR_INVALID;
+  if (n_tiles == 0) return KVARN_OK;
+  if (!k || !v || !tile_first_token || !tile_dst_block || !block_pool) return KVARN_ERR_INVALID;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(block_pool)) return KVARN_ERR_INVALID;
+  if (token_stride_elems % 8 || token_stride_elems < static_cast<int64_t>(cfg->num_kv_heads) * 128)
+    return KVARN_ERR_INVALID;
+  if (static_cast<int64_t>(n_tiles) * cfg->num_kv_heads * 2 > 0x7fffffffLL) return KVARN_ERR_INVALID;
+  QuantizeParams p{k, v, token_stride_elems, n_tokens, tile_first_token, tile_dst_block,
+                   static_cast<unsigned char*>(block_pool), static_cast<int64_t>(kvarn_block_bytes(cfg)),
+                   cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters, dev_err};
+  return cuda_status(launch_quantize(p, cfg->dtype, n_tiles, static_cast<cudaStream_t>(stream)));
+}
+
+kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, const void* v_new, const int32_t* pos,
+                                 const int32_t* block_table, int32_t max_blocks, int32_t batch, void* tail_pool,
+                                 void* block_pool, int32_t* dev_err, void* stream) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || max_blocks < 1) return KVARN_ERR_INVALID;
+  if (batch == 0) return KVARN_OK;
+  if (batch > 0x7fffffff / 1 || cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
+  if (!k_new || !v_new || !pos || !block_table || !tail_pool || !block_pool) return KVARN_ERR_INVALID;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(tail_pool) || !aligned16(block_pool))
+    return KVARN_ERR_INVALID;
+  AppendParams p{k_new, v_new, pos, block_table, max_blocks, cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters,
+                 tail_pool, static_cast<unsigned char*>(block_pool), static_cast<int64_t>(kvarn_block_bytes(cfg)),
+                 dev_err};
+  return cuda_status(launch_append(p, cfg->dtype, batch, static_cast<cudaStream_t>(stream)));
+}
+
+static kvarn_status check_decode(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                 int32_t max_blocks, const int32_t* seq_lens, int32_t batch, const void* pool,
+                                 float* out, void* workspace, size_t workspace_bytes) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || max_blocks < 1 || batch > 65535) return KVARN_ERR_INVALID;
+  if (batch == 0) return KVARN_OK;
+  if (!q || !block_table || !seq_lens || !pool || !out || !workspace) return KVARN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(pool) || !aligned16(out) || !aligned16(workspace)) return KVARN_ERR_INVALID;
+  if (workspace_bytes < kvarn_decode_workspace_bytes(cfg, batch, max_blocks)) return KVARN_ERR_INVALID;
+  return KVARN_OK;
+}
+
+kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                    int32_t max_blocks, const int32_t* seq_lens, int32_t batch, const void* block_pool,
+                                    const void* tail_pool, float softmax_scale, float* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  kvarn_status st = check_decode(cfg, q, block_table, max_blocks, seq_lens, batch, block_pool, out, workspace,
+                                 workspace_bytes);
+  if (st != KVARN_OK || batch == 0) return st;
+  if (!tail_pool || !aligned16(tail_pool)) return KVARN_ERR_INVALID;
+  const int n_chunks = (max_blocks + kChunkTiles - 1) / kChunkTiles;
+  DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
+                 static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
+                 max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads,
+                 cfg->num_blocks, kChunkTiles, n_chunks};
+  return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
+}
+
+kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                         int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                         const void* fp16_pool, float softmax_scale, float* out, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  kvarn_status st = check_decode(cfg, q, block_table, max_blocks, seq_lens, batch, fp16_pool, out, workspace,
+                                 workspace_bytes);
+  if (st != KVARN_OK || batch == 0) return st;
+  if (cfg->num_blocks < 1) return KVARN_ERR_INVALID;
+  const int n_chunks = (max_blocks + kF16ChunkTiles - 1) / kF16ChunkTiles;
+  DecodeParams p{q, block_table, seq_lens, nullptr, nullptr, static_cast<float*>(workspace), dev_err, 0,
+                 softmax_scale, max_blocks, cfg->num_kv_heads, cfg->num_q_heads,
+                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks};
+  cudaError_t e = launch_decode_f16(p, fp16_pool, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return KVARN_ERR_INVALID;
+  if (e == cudaErrorNotSupported) return KVARN_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+kvarn_status kvarn_dequantize(const kvarn_config* cfg, const void* block_pool, const int32_t* blocks, int32_t n,
+                              float* out, int32_t* dev_err, void* stream) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (n < 0) return KVARN_ERR_INVALID;
+  if (n == 0) return KVARN_OK;
+  if (!block_pool || !blocks || !out || !aligned16(block_pool) || !aligned16(out)) return KVARN_ERR_INVALID;
+  if (cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
+  return cuda_status(launch_dequantize(static_cast<const unsigned char*>(block_pool),
+                                       static_cast<int64_t>(kvarn_block_bytes(cfg)), blocks, n, cfg->num_blocks,
+                                       cfg->num_kv_heads, out, dev_err, static_cast<cudaStream_t>(stream)));
+}
+
+const char* kvarn_status_string(kvarn_status s) {
+  switch (s) {
+    case KVARN_OK: return "ok";
+    case KVARN_ERR_INVALID: return "invalid argument";
+    case KVARN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVARN_ERR_CUDA: return "CUDA launch or runtime error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

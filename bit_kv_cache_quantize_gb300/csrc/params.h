@@ -1,0 +1,66 @@
+// params.h -- launch parameter blocks and launcher declarations shared by
+// the C-ABI layer (kvarn_abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace kvarn {
+struct QuantizeParams {
+  const void* k;
+  const void* v;
+  int64_t token_stride;
+  int64_t n_tokens;
+  const int64_t* tile_first_token;
+  const int32_t* tile_dst_block;
+  unsigned char* pool;
+  int64_t block_bytes;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  int32_t iters;
+  int32_t* err;
+};
+struct AppendParams {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* pos;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  int32_t num_kv_heads;
+  int32_t num_blocks;
+  int32_t iters;
+  void* tail;
+  unsigned char* pool;
+  int64_t block_bytes;
+  int32_t* err;
+};
+struct DecodeParams {
+  const void* q;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const unsigned char* pool;
+  const void* tail;
+  float* ws;
+  int32_t* err;
+  int64_t block_bytes;
+  float scale;
+  int32_t max_blocks;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t G;
+  int32_t num_blocks;
+  int32_t chunk_tiles;
+  int32_t n_chunks;
+};
+cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStream_t s);
+cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
+                              int num_blocks, int num_kv_heads, float* out, int32_t* err, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s);
+cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,
+                              cudaStream_t s);
+size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int chunk_tiles);
+
+}  // namespace kvarn

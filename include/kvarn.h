@@ -1,0 +1,203 @@
+/*
+ * kvarn.h -- C ABI of the KVarN KV-cache hot path on GB300 (sm_103a).
+ *
+ * The method (sources are web write-ups of KVarN; titles as published):
+ *  - "KVarN: 2-Bit KV-Cache That Beats FP16 Throughput, and Where the Catch
+ *    Lives", section "What KVarN does differently": each KV tile is rotated
+ *    by a Hadamard transform along the channel dimension, then its variance
+ *    is equalised by a Sinkhorn-like alternation of column and row
+ *    standard-deviation normalisation in log space.
+ *  - "Huawei's KVarN puts KV-cache quantization inside vLLM's backend",
+ *    section "What KVarN changes in vLLM's serving path": preset
+ *    kvarn_k4v2_g128 stores 4-bit keys and 2-bit values per 128-token tile
+ *    (one paged block) with dual FP8 scales and FP16 zero-points; section
+ *    "The four-stage pipeline": rotation, variance normalisation, asymmetric
+ *    round-to-nearest, and dequantisation at read time inside attention;
+ *    FAQ "Is the tile size configurable": the tile is fixed at 128 tokens.
+ *
+ * Conventions for every entry point:
+ *  - All pointers documented "device" are CUDA device pointers the caller
+ *    owns and keeps alive until the stream work completes.  The library
+ *    allocates nothing and keeps no global state.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).  Device pointers must be 16-byte
+ *    aligned; the library checks this on the host.
+ *  - Host-side validation fails synchronously with KVARN_ERR_INVALID (bad
+ *    argument) or KVARN_ERR_UNSUPPORTED (a configuration this build does not
+ *    implement) and launches nothing.  A failed launch returns
+ *    KVARN_ERR_CUDA.
+ *  - Faults found on the device (a block id outside [0, num_blocks), a
+ *    token index or length out of range) store the first error code into
+ *    *dev_err (a device int32 the caller zeroes) and the affected unit skips
+ *    its work.  Kernels never trap and never wait without a bound; a bounded
+ *    wait that expires reports KVARN_DEV_ERR_TIMEOUT.  No C++ exception
+ *    crosses this interface.
+ *
+ * Packed format (one record per tile x KV head, 16-byte aligned):
+ *   K record 8704 B: g[128] FP8 E4M3 per-channel scale | a[128] FP8 E4M3
+ *     per-token step | b[128] FP16 (little-endian) per-token zero-point |
+ *     codes[128 tokens][64 B], byte i of token t = code[t][2i] |
+ *     code[t][2i+1] << 4.
+ *   V record 4608 B: same 512-byte header | codes[128 channels][32 B],
+ *     byte j of channel c = sum_i code[4j+i][c] << 2i.
+ *   Block b of the pool = for each KV head h: [K record | V record], i.e.
+ *     num_kv_heads * 13312 bytes; head h of block b starts at
+ *     b * kvarn_block_bytes() + h * 13312.
+ *   Dequantised value (rotated domain): R[t][c] = g[c] * (a[t]*code + b[t]);
+ *   the cache value is R H with H the 128-point Sylvester Hadamard matrix
+ *   divided by sqrt(128).  4.25 bits/element for K, 2.25 for V.
+ */
+#ifndef KVARN_H
+#define KVARN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvarn_status {
+  KVARN_OK = 0,
+  KVARN_ERR_INVALID = 1,     /* bad pointer, size, alignment or stride */
+  KVARN_ERR_UNSUPPORTED = 2, /* valid request outside what this build implements */
+  KVARN_ERR_CUDA = 3         /* a kernel launch or CUDA runtime call failed */
+} kvarn_status;
+
+typedef enum kvarn_dtype {
+  KVARN_DTYPE_F16 = 0,
+  KVARN_DTYPE_BF16 = 1
+} kvarn_dtype;
+
+/* Codes stored into *dev_err by a kernel (first error wins). */
+#define KVARN_DEV_ERR_BLOCK_RANGE 1 /* a block id outside [0, num_blocks) */
+#define KVARN_DEV_ERR_TOKEN_RANGE 2 /* a token index, position or length out of range */
+#define KVARN_DEV_ERR_TIMEOUT 3     /* a bounded wait on an async copy expired */
+
+typedef struct kvarn_config {
+  int32_t head_dim;       /* channels per head; must be 128 */
+  int32_t tile_tokens;    /* tokens per tile = paged block size; must be 128 */
+  int32_t num_kv_heads;   /* KV heads of the layer, >= 1 */
+  int32_t num_q_heads;    /* query heads; a multiple of num_kv_heads with group size <= 8 */
+  int32_t num_blocks;     /* blocks in the packed block pool (device bounds check) */
+  int32_t k_bits;         /* key code width; must be 4 */
+  int32_t v_bits;         /* value code width; must be 2 */
+  int32_t sinkhorn_iters; /* normalisation iterations, 0..64 (the preset uses 8) */
+  int32_t dtype;          /* kvarn_dtype of K/V/query inputs and of the open-tile buffer */
+} kvarn_config;
+
+/* Bytes of one block of the packed pool: num_kv_heads * 13312.  0 if cfg is
+ * invalid. */
+size_t kvarn_block_bytes(const kvarn_config* cfg);
+
+/* Bytes of the open-tile (tail) buffer for `batch` sequences:
+ * batch * num_kv_heads * 2 * 128 * 128 * 2.  Layout [seq][kv_head][K=0,V=1]
+ * [token slot 0..127][channel], 16-bit elements of cfg->dtype; token p of a
+ * sequence lives in slot p % 128 until its tile closes.  0 if invalid. */
+size_t kvarn_tail_bytes(const kvarn_config* cfg, int32_t batch);
+
+/*
+ * Quantise whole 128-token tiles into the packed pool (write path: rotation,
+ * Sinkhorn-like normalisation, FP8/FP16 scales, asymmetric round-to-nearest,
+ * bit packing -- the first three stages of "The four-stage pipeline").
+ *
+ *  k, v              device, 16-bit (cfg->dtype).  Element (token r, head h,
+ *                    channel c) at k[r * token_stride_elems + h * 128 + c];
+ *                    e.g. a [seq][token][head][128] array flattened over
+ *                    (seq, token).  token_stride_elems: multiple of 8,
+ *                    >= num_kv_heads * 128.
+ *  n_tokens          number of token rows addressable from k and v (bound for
+ *                    the device check).
+ *  tile_first_token  device int64[n_tiles]: first token row of tile i.
+ *  tile_dst_block    device int32[n_tiles]: destination block of tile i; all
+ *                    num_kv_heads heads of the tile go into that block.
+ *  block_pool        device, num_blocks * kvarn_block_bytes() bytes.
+ *  dev_err           device int32 (see above); tiles whose first token or
+ *                    block is out of range are skipped.
+ * n_tiles == 0 is a no-op.  Records of different tiles must not alias.
+ */
+kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const void* v,
+                                  int64_t token_stride_elems, int64_t n_tokens,
+                                  const int64_t* tile_first_token, const int32_t* tile_dst_block,
+                                  int32_t n_tiles, void* block_pool, int32_t* dev_err, void* stream);
+
+/*
+ * Append one token per sequence to the open tile; when a tile fills (its
+ * 128th token arrives) quantise it into block_table[s][pos/128] (the write
+ * path "happens every decode step", "The four-stage pipeline").  The open
+ * tile stays raw 16-bit until it fills.
+ *
+ *  k_new, v_new  device, 16-bit [batch][num_kv_heads][128].
+ *  pos           device int32[batch]: position of the new token in its
+ *                sequence (0-based); must be >= 0 and pos/128 < max_blocks.
+ *  block_table   device int32[batch][max_blocks]: physical block of each
+ *                128-token tile of each sequence.
+ *  tail_pool     device, kvarn_tail_bytes(cfg, batch) bytes (layout above).
+ *  block_pool    device packed pool.
+ * Out-of-range positions or blocks set *dev_err and skip that sequence.
+ */
+kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, const void* v_new,
+                                 const int32_t* pos, const int32_t* block_table, int32_t max_blocks,
+                                 int32_t batch, void* tail_pool, void* block_pool, int32_t* dev_err,
+                                 void* stream);
+
+/* Workspace bytes kvarn_decode_attention needs for this batch and table
+ * width (split-K partial results).  0 if invalid. */
+size_t kvarn_decode_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks);
+
+/*
+ * Decode attention over the packed paged cache plus the raw open tile
+ * ("Dequantization at read time", "The four-stage pipeline"): for each
+ * sequence s and query head j (KV head j / (num_q_heads/num_kv_heads)),
+ *   out[s][j] = softmax(scale * q K^T) V
+ * over the seq_lens[s] tokens of s: tiles 0 .. seq_lens[s]/128 - 1 packed in
+ * block_table[s][.], then seq_lens[s] % 128 raw tokens in the open tile.
+ * Scales and the key rotation are folded into the query, the per-channel
+ * value scales into the accumulator, and one inverse rotation is applied to
+ * the output.
+ *
+ *  q           device, 16-bit (cfg->dtype) [batch][num_q_heads][128].
+ *  seq_lens    device int32[batch]; 0 gives a zero output row; must satisfy
+ *              seq_lens[s] <= 128 * max_blocks.
+ *  out         device float32 [batch][num_q_heads][128].
+ *  workspace   device, >= kvarn_decode_workspace_bytes(cfg, batch, max_blocks).
+ */
+kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                    int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                    const void* block_pool, const void* tail_pool, float softmax_scale,
+                                    float* out, void* workspace, size_t workspace_bytes,
+                                    int32_t* dev_err, void* stream);
+
+/*
+ * Dequantise packed blocks back to the unrotated domain (tests and tools).
+ *  blocks  device int32[n]: block ids.
+ *  out     device float32 [n][2 (K,V)][num_kv_heads][128 tokens][128].
+ */
+kvarn_status kvarn_dequantize(const kvarn_config* cfg, const void* block_pool, const int32_t* blocks,
+                              int32_t n, float* out, int32_t* dev_err, void* stream);
+
+/* Bytes of one block of the 16-bit comparison pool: num_kv_heads * 2 * 128 *
+ * 128 * 2, layout [kv_head][K=0,V=1][token][channel]. */
+size_t kvarn_fp16_block_bytes(const kvarn_config* cfg);
+
+/*
+ * Comparison point: the same decode attention over an unquantised 16-bit
+ * paged cache (cfg->dtype elements, pool of num_blocks blocks laid out as in
+ * kvarn_fp16_block_bytes).  seq_lens[s] tokens of sequence s live in
+ * block_table[s][0 .. ceil(seq_lens[s]/128) - 1]; slots past the length in
+ * the last block are ignored.  Arguments otherwise as kvarn_decode_attention.
+ */
+kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q,
+                                         const int32_t* block_table, int32_t max_blocks,
+                                         const int32_t* seq_lens, int32_t batch, const void* fp16_pool,
+                                         float softmax_scale, float* out, void* workspace,
+                                         size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/* Static description of a status code. */
+const char* kvarn_status_string(kvarn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVARN_H */

@@ -1,0 +1,102 @@
+"""Comparison of GPU-packed records with the oracle's, under the parity rule:
+
+* scales: every FP8 per-channel scale g, FP8 per-token step a and FP16
+  per-token zero-point b within one code of the oracle's (adjacent values);
+  the number of differing scales is reported;
+* codes: where g[c], a[t] and b[t] all equal the oracle's, every code is
+  bit-exact except where the oracle's fp64 pre-rounding value (Y - b)/a lies
+  within 1e-5 of a .5 boundary; there it may differ by one level, in at most
+  0.01% of the codes;
+* where a scale differs (both values are then valid quantisations), the GPU
+  code must still be the nearest level of its own scales: rint((Y - b)/a)
+  computed here in fp64 from the oracle's rotated tile, same tie rule.
+
+The GPU bytes are decoded here with numpy/torch, not with the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+T = D = 128
+
+
+def e4m3(codes: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def f16(bits: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def f16_order(bits: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns -> integers ordered like the values."""
+    b = bits.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def unpack(rec: np.ndarray, is_v: bool):
+    rec = np.ascontiguousarray(rec, dtype=np.uint8)
+    g8 = rec[:128].copy()
+    a8 = rec[128:256].copy()
+    b16 = rec[256:512].view(np.uint16).copy()
+    body = rec[512:]
+    if not is_v:
+        by = body.reshape(T, 64)
+        code = np.empty((T, D), np.uint8)
+        code[:, 0::2] = by & 15
+        code[:, 1::2] = by >> 4
+    else:
+        by = body.reshape(D, 32)                      # [channel][byte]
+        crumbs = np.stack([(by >> (2 * i)) & 3 for i in range(4)], axis=-1)  # [c][j][i] -> token 4j+i
+        code = crumbs.reshape(D, T).T.copy()
+    return g8, a8, b16, code
+
+
+class Stats:
+    def __init__(self):
+        self.tiles = self.codes = 0
+        self.g_flip = self.a_flip = self.b_flip = 0
+        self.tie_diff = self.valid_checked = 0
+
+    def __repr__(self):
+        return (f"tiles={self.tiles} codes={self.codes} g_flip={self.g_flip} a_flip={self.a_flip} "
+                f"b_flip={self.b_flip} tie_diff={self.tie_diff} checked_vs_own_scales={self.valid_checked}")
+
+
+def compare_record(gpu_rec: np.ndarray, tile, is_v: bool, st: Stats, where: str = ""):
+    """tile: oracle.Tile of the same input."""
+    L = 3 if is_v else 15
+    g8, a8, b16, code = unpack(gpu_rec, is_v)
+    st.tiles += 1
+    st.codes += code.size
+    assert code.max() <= L, where
+    dg = np.abs(g8.astype(int) - tile.g8.astype(int))
+    da = np.abs(a8.astype(int) - tile.a8.astype(int))
+    db = np.abs(f16_order(b16) - f16_order(tile.b16))
+    assert dg.max() <= 1 and da.max() <= 1 and db.max() <= 1, f"{where}: scale off by more than one code"
+    st.g_flip += int((dg > 0).sum()); st.a_flip += int((da > 0).sum()); st.b_flip += int((db > 0).sum())
+    same = (dg == 0)[None, :] & (da == 0)[:, None] & (db == 0)[:, None]
+    frac = tile.pre - np.floor(tile.pre)
+    near = np.abs(frac - 0.5) < 1e-5
+    mism = code != tile.code
+    bad = mism & same & ~near
+    assert not bad.any(), f"{where}: {int(bad.sum())} codes differ with identical scales (first {np.argwhere(bad)[:3]})"
+    tie = mism & same & near
+    assert (np.abs(code.astype(int) - tile.code.astype(int))[tie] <= 1).all(), where
+    st.tie_diff += int(tie.sum())
+    if not same.all():
+        g, a, b = e4m3(g8), e4m3(a8), f16(b16)
+        t = (tile.R / g[None, :] - b[:, None]) / a[:, None]
+        want = np.clip(np.rint(t), 0, L)
+        near2 = np.abs((t - np.floor(t)) - 0.5) < 1e-5
+        chk = ~same
+        badv = chk & (code != want) & ~(near2 & (np.abs(code - want) <= 1))
+        assert not badv.any(), f"{where}: {int(badv.sum())} codes are not the nearest level of their own scales"
+        st.valid_checked += int(chk.sum())
+
+
+def finish(st: Stats):
+    assert st.tie_diff <= 1e-4 * max(st.codes, 1), f"too many boundary flips: {st}"
+    return st

@@ -1,0 +1,85 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/kvarn.h declares, sizes its buffers as documented, and rejects bad
+arguments on the host without launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_kv_cache_quantize_gb300 import build as B
+from bit_kv_cache_quantize_gb300 import kvarn as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return K.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvarn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvarn_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(K.EXPORTS)
+
+
+def test_sizes(lib):
+    cfg = K.make_config(8, 64, 100, "f16")
+    assert K.kvarn_block_bytes(cfg) == 8 * 13312
+    assert K.kvarn_tail_bytes(cfg, 3) == 3 * 8 * 2 * 128 * 128 * 2
+    assert K.kvarn_fp16_block_bytes(cfg) == 8 * 65536
+    ws = K.kvarn_decode_workspace_bytes(cfg, 32, 128)
+    assert ws == 32 * 8 * (8 + 1) * 8 * 130 * 4
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, K.KVARN_ERR_UNSUPPORTED), ("tile_tokens", 64, K.KVARN_ERR_UNSUPPORTED),
+    ("k_bits", 2, K.KVARN_ERR_UNSUPPORTED), ("v_bits", 4, K.KVARN_ERR_UNSUPPORTED),
+    ("num_q_heads", 12, K.KVARN_ERR_INVALID), ("num_q_heads", 128, K.KVARN_ERR_UNSUPPORTED),
+    ("num_kv_heads", 0, K.KVARN_ERR_INVALID), ("dtype", 7, K.KVARN_ERR_INVALID),
+    ("sinkhorn_iters", -1, K.KVARN_ERR_INVALID), ("sinkhorn_iters", 65, K.KVARN_ERR_INVALID),
+])
+def test_config_validation(lib, field, value, status):
+    cfg = K.make_config(8, 64, 10)
+    setattr(cfg, field, value)
+    assert K.kvarn_block_bytes(cfg) == 0
+    st = K.kvarn_quantize_tiles(cfg, 16, 16, 1024, 128, 16, 16, 1, 16, 16, stream=0, check=False)
+    assert st == status
+
+
+def test_argument_validation_is_host_side(lib):
+    cfg = K.make_config(8, 64, 10)
+    # no tiles: nothing to do, even with null pointers
+    assert K.kvarn_quantize_tiles(cfg, None, None, 1024, 0, None, None, 0, None, None, stream=0, check=False) == 0
+    bad = [
+        dict(k=None), dict(k=17), dict(token_stride_elems=1020), dict(token_stride_elems=512), dict(block_pool=None),
+    ]
+    for b in bad:
+        args = dict(k=16, v=16, token_stride_elems=1024, n_tokens=128, tile_first_token=16, tile_dst_block=16,
+                    n_tiles=1, block_pool=16, dev_err=16)
+        args.update(b)
+        st = K.kvarn_quantize_tiles(cfg, args["k"], args["v"], args["token_stride_elems"], args["n_tokens"],
+                                    args["tile_first_token"], args["tile_dst_block"], args["n_tiles"],
+                                    args["block_pool"], args["dev_err"], stream=0, check=False)
+        assert st == K.KVARN_ERR_INVALID, b
+    ws = K.kvarn_decode_workspace_bytes(cfg, 2, 4)
+    assert K.kvarn_decode_attention(cfg, 16, 16, 4, 16, 2, 16, 16, 0.1, 16, 16, ws - 4, 16, stream=0,
+                                    check=False) == K.KVARN_ERR_INVALID
+    assert K.kvarn_decode_attention(cfg, 16, 16, 0, 16, 2, 16, 16, 0.1, 16, 16, ws, 16, stream=0,
+                                    check=False) == K.KVARN_ERR_INVALID
+    assert K.kvarn_append_tokens(cfg, 16, 16, 16, 16, 4, 0, 16, 16, 16, stream=0, check=False) == 0
+    assert K.kvarn_append_tokens(cfg, 8, 16, 16, 16, 4, 1, 16, 16, 16, stream=0, check=False) == K.KVARN_ERR_INVALID
+    assert K.kvarn_dequantize(cfg, 16, 16, -1, 16, 16, stream=0, check=False) == K.KVARN_ERR_INVALID
+    assert K.kvarn_status_string(K.KVARN_ERR_UNSUPPORTED) == "unsupported configuration"
+    with pytest.raises(K.KvarnError):
+        K.kvarn_dequantize(cfg, 16, 16, -1, 16, 16, stream=0)

@@ -1,0 +1,114 @@
+"""Decode-step path: append one token per sequence into the raw open tile,
+close and quantise tiles as they fill, attend after every append."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from bit_kv_cache_quantize_gb300 import inputs as I
+from bit_kv_cache_quantize_gb300 import kvarn as K
+from bit_kv_cache_quantize_gb300.cache import PagedCache
+
+import parity as PR
+from gpu_helpers import bits, device, oracle_attention_units, oracle_tiles
+from test_gpu_decode import load_oracle_records
+
+pytestmark = pytest.mark.gpu
+T = D = 128
+TOL = 1e-3
+
+
+def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
+    dev = device()
+    c = PagedCache(w, dev)
+    c.prefill()
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    check_seqs = list(range(w.batch)) if check_seqs is None else check_seqs
+    total = [n + steps for n in w.seq_lens]
+    ctx = {b: (I.kv_sequence(w, "k", b, total[b]), I.kv_sequence(w, "v", b, total[b])) for b in check_seqs}
+    # closed prefill tiles of the checked sequences: oracle records
+    pre_ctx = {b: (ctx[b][0][:w.seq_lens[b]], ctx[b][1][:w.seq_lens[b]]) for b in check_seqs}
+    recs = load_oracle_records(w, c, check_seqs, pre_ctx)
+    st = PR.Stats()
+    lens = torch.tensor(w.seq_lens, dtype=torch.int32)
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    worst = 0.0
+    for s in range(steps):
+        pos = lens.clone()
+        k_new = torch.stack([I.kv_values(w, "k", b, int(pos[b]), 1, dev)[0] for b in range(w.batch)])
+        v_new = torch.stack([I.kv_values(w, "v", b, int(pos[b]), 1, dev)[0] for b in range(w.batch)])
+        c.append(k_new, v_new, pos.to(dev))
+        lens = pos + 1
+        torch.cuda.synchronize()
+        assert c.check_error() == 0
+        # the raw slot holds the token bit for bit; tiles that filled are quantised
+        closing = [b for b in range(w.batch) if int(pos[b]) % T == T - 1]
+        for b in range(w.batch):
+            slot = int(pos[b]) % T
+            assert torch.equal(c.tail[b, :, 0, slot], k_new[b]) and torch.equal(c.tail[b, :, 1, slot], v_new[b])
+        jobs, keys = [], []
+        for b in closing:
+            t = int(pos[b]) // T
+            full_k = I.kv_values(w, "k", b, t * T, T)
+            full_v = I.kv_values(w, "v", b, t * T, T)
+            for h in range(w.num_kv_heads):
+                jobs += [(full_k[:, h], 0), (full_v[:, h], 1)]
+                keys += [(b, t, h, 0), (b, t, h, 1)]
+        tiles = oracle_tiles(jobs, w.dtype)
+        for (b, t, h, kv), tl in zip(keys, tiles):
+            blk = int(c.table[b, t])
+            PR.compare_record(c.record(blk, h, kv).cpu().numpy(), tl, bool(kv), st,
+                              where=f"step {s} seq {b} closed tile {t} head {h} kv {kv}")
+            if b in ctx:  # decode parity reads oracle records only
+                rec = O.pack_record(bool(kv), tl)
+                recs[(b, t, h, kv)] = rec
+                c.set_record(blk, h, kv, torch.from_numpy(rec).to(dev))
+        if s % attend_every and s != steps - 1:
+            continue
+        q = I.queries(w, step=s + 1)
+        c.decode(q.to(dev), out, lens=lens.to(dev))
+        torch.cuda.synchronize()
+        assert c.check_error() == 0
+        got = out.cpu().numpy().astype(np.float64)
+        units, ukeys = [], []
+        for b in check_seqs:
+            n = int(lens[b])
+            nf = n // T
+            k, v = ctx[b]
+            for h in range(w.num_kv_heads):
+                units.append(dict(q=O.decode16(bits(q[b, h * w.G:(h + 1) * w.G]), w.dtype),
+                                  krec=[recs[(b, t, h, 0)] for t in range(nf)],
+                                  vrec=[recs[(b, t, h, 1)] for t in range(nf)],
+                                  ktail=O.decode16(bits(k[nf * T:n, h]), w.dtype).reshape(-1, D),
+                                  vtail=O.decode16(bits(v[nf * T:n, h]), w.dtype).reshape(-1, D)))
+                ukeys.append((b, h))
+        for (b, h), o in zip(ukeys, oracle_attention_units(units, w.scale)):
+            worst = max(worst, np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max())
+    print(w.name, PR.finish(st), f"max |gpu - oracle| = {worst:.3e}")
+    assert worst <= TOL
+    return st
+
+
+def test_append_close_small():
+    w = I.Workload("append_small", 6, 16, 2, "f16", [125, 126, 127, 255, 300, 10], seed=41, decode_steps=4,
+                   max_tokens=310, block_perm=True)
+    st = run_steps(w, 4)
+    assert st.tiles == 4 * 2 * 2   # seqs 0..3 close one tile each
+
+
+def test_append_close_bf16():
+    w = I.Workload("append_bf16", 3, 8, 2, "bf16", [127, 383, 5], seed=43, decode_steps=2, max_tokens=400,
+                   v_dist="t4", k_outliers="random", block_perm=True)
+    run_steps(w, 2)
+
+
+@pytest.mark.slow
+def test_ragged_serving_full_size_sampled():
+    """256 sequences, lengths U[128, 32768], 64 decode steps; every closing
+    tile is checked, attention on 6 sampled sequences every 16 steps."""
+    w = I.ragged_32b()
+    lens = np.array(w.seq_lens)
+    closing = [b for b in range(w.batch) if (lens[b] % T) + 64 >= T][:4]
+    others = [b for b in range(w.batch) if b not in closing][:2]
+    run_steps(w, 64, check_seqs=closing + others, attend_every=16)

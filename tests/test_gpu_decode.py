@@ -1,0 +1,178 @@
+"""GPU read path (packed decode attention, 16-bit comparison kernel) against
+the CPU oracle.  The packed cache the GPU reads is made of ORACLE records
+(uploaded), so the expected outputs never depend on the GPU quantiser."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from bit_kv_cache_quantize_gb300 import inputs as I
+from bit_kv_cache_quantize_gb300 import kvarn as K
+from bit_kv_cache_quantize_gb300.cache import PagedCache
+
+from gpu_helpers import bits, device, oracle_attention_units, oracle_tiles
+
+pytestmark = pytest.mark.gpu
+T = D = 128
+TOL = 1e-3
+
+
+def load_oracle_records(w, c: PagedCache, seqs, ctx):
+    """Quantise the closed tiles of `seqs` with the oracle, upload the
+    records into the GPU pool and the raw remainder into the open tile.
+    Returns per (b, h) the oracle records."""
+    recs = {}
+    jobs, keys = [], []
+    for b in seqs:
+        k, v = ctx[b]
+        n_full = k.shape[0] // T
+        for t in range(n_full):
+            for h in range(w.num_kv_heads):
+                for kv, src in ((0, k), (1, v)):
+                    jobs.append((src[t * T:(t + 1) * T, h], kv))
+                    keys.append((b, t, h, kv))
+    tiles = oracle_tiles(jobs, w.dtype)
+    for (b, t, h, kv), tl in zip(keys, tiles):
+        rec = O.pack_record(bool(kv), tl)
+        recs[(b, t, h, kv)] = rec
+        c.set_record(int(c.table[b, t]), h, kv, torch.from_numpy(rec).to(c.device))
+    for b in seqs:
+        k, v = ctx[b]
+        n_full = k.shape[0] // T
+        r = k.shape[0] - n_full * T
+        if r:
+            c.tail[b, :, 0, :r] = k[n_full * T:].permute(1, 0, 2).to(c.device)
+            c.tail[b, :, 1, :r] = v[n_full * T:].permute(1, 0, 2).to(c.device)
+    return recs
+
+
+def oracle_outputs(w, seqs, ctx, recs, q, lens=None):
+    """Oracle attention per (b, h) over oracle records + raw tail."""
+    G = w.G
+    units, keys = [], []
+    for b in seqs:
+        k, v = ctx[b]
+        n = k.shape[0] if lens is None else lens[b]
+        n_full = n // T
+        for h in range(w.num_kv_heads):
+            units.append(dict(
+                q=O.decode16(bits(q[b, h * G:(h + 1) * G]), w.dtype),
+                krec=[recs[(b, t, h, 0)] for t in range(n_full)],
+                vrec=[recs[(b, t, h, 1)] for t in range(n_full)],
+                ktail=O.decode16(bits(k[n_full * T:n, h]), w.dtype).reshape(-1, D),
+                vtail=O.decode16(bits(v[n_full * T:n, h]), w.dtype).reshape(-1, D)))
+            keys.append((b, h))
+    outs = oracle_attention_units(units, w.scale)
+    return dict(zip(keys, outs))
+
+
+def run_decode_case(w, seqs=None, full_gpu_prefill=False):
+    dev = device()
+    seqs = list(range(w.batch)) if seqs is None else seqs
+    c = PagedCache(w, dev)
+    ctx = {b: (I.kv_sequence(w, "k", b, w.seq_lens[b]), I.kv_sequence(w, "v", b, w.seq_lens[b])) for b in seqs}
+    if full_gpu_prefill:
+        c.prefill()            # every sequence, GPU quantiser
+    recs = load_oracle_records(w, c, seqs, ctx)
+    q = I.queries(w)
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    c.decode(q.to(dev), out)
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    want = oracle_outputs(w, seqs, ctx, recs, q)
+    got = out.cpu().numpy().astype(np.float64)
+    worst = 0.0
+    for (b, h), o in want.items():
+        d = np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max()
+        worst = max(worst, d)
+    print(f"{w.name}: max |gpu - oracle| = {worst:.3e}")
+    assert worst <= TOL
+    return worst
+
+
+def test_single_tile():
+    run_decode_case(I.single_tile())
+
+
+def test_qwen3_4b_layer():
+    run_decode_case(I.qwen3_4b())
+
+
+def ragged_small():
+    return I.Workload("ragged_small", 7, 16, 2, "f16", [1, 127, 128, 129, 700, 2200, 0], seed=21, max_tokens=2400,
+                      block_perm=True)
+
+
+def test_ragged_tails_and_empty_sequence():
+    run_decode_case(ragged_small())
+
+
+def test_group_sizes_bf16():
+    for hq, hkv in ((2, 2), (4, 2), (6, 3)):
+        w = I.Workload(f"g{hq // hkv}", 3, hq, hkv, "bf16", [300, 128, 77], seed=30 + hq, max_tokens=300,
+                       v_dist="t4", k_outliers="random")
+        run_decode_case(w)
+
+
+@pytest.mark.slow
+def test_qwen3_32b_full_size_sampled():
+    """All 32 x 16384 tokens quantised by the GPU, decoded in the launch the
+    benchmark times; two sequences carry oracle records and are checked."""
+    run_decode_case(I.qwen3_32b(), seqs=[0, 17], full_gpu_prefill=True)
+
+
+def fp16_case(w, seqs=None):
+    dev = device()
+    seqs = list(range(w.batch)) if seqs is None else seqs
+    c = PagedCache(w, dev, fp16_pool=True)
+    ctx = {}
+    for b in range(w.batch):
+        k = I.kv_sequence(w, "k", b, w.seq_lens[b], dev)
+        v = I.kv_sequence(w, "v", b, w.seq_lens[b], dev)
+        c.quantize_sequence(b, k, v)
+        if b in seqs:
+            ctx[b] = (k.cpu(), v.cpu())
+    q = I.queries(w).to(dev)
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    c.decode_fp16(q, out)
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    got = out.cpu().numpy().astype(np.float64)
+    worst = 0.0
+    for b in seqs:
+        k, v = ctx[b]
+        for h in range(w.num_kv_heads):
+            want = O.attention(O.decode16(bits(q[b, h * w.G:(h + 1) * w.G]), w.dtype),
+                               O.decode16(bits(k[:, h]), w.dtype), O.decode16(bits(v[:, h]), w.dtype), w.scale)
+            worst = max(worst, np.abs(got[b, h * w.G:(h + 1) * w.G] - want).max())
+    print(f"fp16 {w.name}: max |gpu - oracle| = {worst:.3e}")
+    assert worst <= TOL
+
+
+def test_fp16_baseline_ragged():
+    fp16_case(ragged_small())
+
+
+def test_fp16_baseline_bf16_layer():
+    fp16_case(I.qwen3_4b(), seqs=[0, 5])
+
+
+def test_decode_device_errors():
+    dev = device()
+    w = ragged_small()
+    c = PagedCache(w, dev)
+    q = I.queries(w).to(dev)
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    bad = c.table.clone()
+    bad[4, 2] = c.num_blocks + 5
+    K.kvarn_decode_attention(c.cfg, q, bad, c.max_blocks, c.lens, w.batch, c.pool, c.tail, w.scale, out, c.ws,
+                             c.ws_bytes, c.err)
+    torch.cuda.synchronize()
+    assert c.check_error() == K.KVARN_DEV_ERR_BLOCK_RANGE
+    c.err.zero_()
+    lens = c.lens.clone()
+    lens[1] = T * c.max_blocks + 1
+    c.decode(q, out, lens=lens)
+    torch.cuda.synchronize()
+    assert c.check_error() == K.KVARN_DEV_ERR_TOKEN_RANGE
+    assert not out[1].any()
