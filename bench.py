@@ -1,0 +1,438 @@
+#!/usr/bin/env python
+"""Benchmark of the KVarN KV-cache hot path on GB300.
+
+Step = one decode step of the ragged serving mix (Qwen3-32B layer: 64 query
+heads, 8 KV heads, head_dim 128, fp16; 256 sequences with context lengths
+U[128, 32768], never a multiple of 128): append one token per sequence to
+the raw open tile (tiles that fill are quantised into their paged block on
+the spot), then decode attention of one query per sequence and head over the
+packed cache plus the open tile.  Every row of the hot path runs in every
+step.  Inputs (the prefilled cache, every step's new tokens and queries) are
+resident in HBM before the timed region; the packed cache (~3.5 GB) is far
+larger than L2.
+
+Also reported, as components: the 16K-context decode (32 x 16384 tokens) of
+the packed kernel beside the in-repo 16-bit paged decode kernel on the same
+shapes, and the write-path quantiser on 32 x 16384 x 8 heads of bf16.
+
+`--impl reference` times the CPU oracle (the plain fp64 restatement of the
+method) on the host cores on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn tokens/s & packed-KV HBM GB/s (% of 8 TB/s); quantized tiles/s"
+T = D = 128
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu, self.lines, self.proc = gpu, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        time.sleep(0.25)
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def decode_bytes(lens, w):
+    """Algorithmic bytes of one decode call: packed records of the closed
+    tiles, raw open-tile tokens, queries, outputs, block ids and lengths."""
+    H = w.num_kv_heads
+    closed = sum(n // T for n in lens)
+    tail = sum(n % T for n in lens)
+    return (closed * H * 13312 + tail * H * 2 * D * 2 + len(lens) * w.num_q_heads * D * (2 + 4)
+            + closed * 4 + len(lens) * 4)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world):
+    import torch
+    from bit_kv_cache_quantize_gb300 import build as B
+    from bit_kv_cache_quantize_gb300 import inputs as I
+    from bit_kv_cache_quantize_gb300 import kvarn as K
+    from bit_kv_cache_quantize_gb300.cache import PagedCache
+
+    B.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    hbm_peak, _, peak_src = measured_peaks()
+    steps, warm = args.steps, args.warmup
+    n_dec = max(64, steps + warm)
+    w = I.ragged_32b(steps=n_dec, seed=4 + 1000 * rank)
+    c = PagedCache(w, dev)
+    c.prefill()
+    torch.cuda.synchronize()
+    assert c.check_error() == 0, "device error during prefill"
+
+    # every step's inputs, resident before timing
+    B_, H, Hq = w.batch, w.num_kv_heads, w.num_q_heads
+    dt = I.torch_dtype(w.dtype)
+    base = torch.tensor(w.seq_lens, dtype=torch.int64)
+    pos_all = (base[None, :] + torch.arange(n_dec)[:, None]).to(torch.int32)          # [S, B]
+    kn = torch.empty(n_dec, B_, H, D, dtype=dt, device=dev)
+    vn = torch.empty_like(kn)
+    for b in range(B_):
+        kn[:, b] = I.kv_values(w, "k", b, w.seq_lens[b], n_dec, dev)
+        vn[:, b] = I.kv_values(w, "v", b, w.seq_lens[b], n_dec, dev)
+    qs = torch.stack([I.queries(w, step=s + 1, device=dev) for s in range(n_dec)])
+    pos_d = pos_all.to(dev)
+    lens_d = (pos_all + 1).to(dev)
+    out = torch.empty(B_, Hq, D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(s):
+        c.append(kn[s], vn[s], pos_d[s], stream)
+        c.decode(qs[s], out, lens=lens_d[s], stream=stream)
+
+    for s in range(warm):
+        step(s)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0.record(stream)
+        for i in range(steps):
+            s = warm + i
+            c.append(kn[s], vn[s], pos_d[s], stream)
+            evs[i][0].record(stream)
+            c.decode(qs[s], out, lens=lens_d[s], stream=stream)
+            evs[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    assert c.check_error() == 0, "device error during the timed steps"
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    dec_avg_s = sum(dec_ms) / len(dec_ms) / 1e3
+    dec_bytes = statistics.mean(decode_bytes([int(x) + 1 for x in pos_all[warm + i]], w) for i in range(steps))
+    achieved = dec_bytes / dec_avg_s / 1e9
+    tokens_per_s = B_ * steps * world / (ms / 1e3)
+
+    # e2e: the same steps through the public API with host buffers
+    e2e = run_e2e(c, w, kn, vn, qs, pos_all, dev, warm, steps)
+
+    res = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "ragged_32b_serving: 256 seqs, context U[128,32768] (never a multiple of 128), "
+                               "Qwen3-32B layer 64 q / 8 KV heads, head_dim 128, fp16 inputs, K4/V2 "
+                               "128-token tiles, 8 Sinkhorn iterations; step = append 1 token/seq "
+                               "(close+quantise full tiles) + decode attention",
+                   "batch": B_, "mean_context": statistics.mean(w.seq_lens),
+                   "decode_steps_appended": n_dec, "l2": "inputs larger than L2 (packed cache ~3.5 GB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "kvarn_decode_attention (split-K decode + combine)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_source": peak_src, "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+                     "avg_launch_us": dec_avg_s * 1e6},
+        "e2e": e2e,
+        "gpu_launches": steps * 3,
+        "bits_per_element": {"k": 4.25, "v": 2.25, "mean": 3.25, "vs_16bit": 16 / 3.25},
+    }
+    del c, kn, vn, qs
+    torch.cuda.empty_cache()
+    if not args.no_components and rank == 0:
+        res["components"] = components(dev, hbm_peak)
+    res["clocks"] = clk.summary()
+    return res
+
+
+def run_e2e(c, w, kn, vn, qs, pos_all, dev, warm, steps):
+    import torch
+    hk = kn.cpu().pin_memory(); hv = vn.cpu().pin_memory(); hq = qs.cpu().pin_memory()
+    hp = pos_all.pin_memory(); hl = (pos_all + 1).pin_memory()
+    hout = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32).pin_memory()
+    dk = torch.empty_like(kn[0]); dv = torch.empty_like(vn[0]); dq = torch.empty_like(qs[0])
+    dp = torch.empty(w.batch, dtype=torch.int32, device=dev); dl = torch.empty_like(dp)
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    h2d = dk.numel() * dk.element_size() * 2 + dq.numel() * dq.element_size() + dp.numel() * 8
+    d2h = out.numel() * 4
+
+    def step(s):
+        dk.copy_(hk[s], non_blocking=True); dv.copy_(hv[s], non_blocking=True)
+        dq.copy_(hq[s], non_blocking=True); dp.copy_(hp[s], non_blocking=True); dl.copy_(hl[s], non_blocking=True)
+        c.append(dk, dv, dp, stream)
+        c.decode(dq, out, lens=dl, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    # replay the same positions: the state a step writes is the state it reads
+    for s in range(warm):
+        step(s)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(steps):
+        step(warm + i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    return {"value": w.batch * steps / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps}
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+def components(dev, hbm_peak):
+    """16K decode (packed vs 16-bit kernel) and the prefill quantiser."""
+    import torch
+    from bit_kv_cache_quantize_gb300 import inputs as I
+    from bit_kv_cache_quantize_gb300 import kvarn as K
+    from bit_kv_cache_quantize_gb300.cache import PagedCache
+
+    out = {}
+    scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 2 x L2
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        ts = []
+        for _ in range(3):
+            fn()
+        for _ in range(reps):
+            flush_l2(scratch)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream); fn(); b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        return statistics.median(ts)
+
+    # --- 16K decode: packed KVarN vs 16-bit paged kernel, same table and shapes
+    w = I.qwen3_32b()
+    c = PagedCache(w, dev, fp16_pool=True)
+    c.prefill()
+    q = I.queries(w, device=dev)
+    o = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    t_pk = timed(lambda: c.decode(q, o), 50)
+    t_16 = timed(lambda: c.decode_fp16(q, o), 20)
+    b_pk = decode_bytes(w.seq_lens, w)
+    b_16 = sum(w.seq_lens) * w.num_kv_heads * 2 * D * 2 + w.batch * w.num_q_heads * D * 6
+    assert c.check_error() == 0
+    out["decode_16k"] = {
+        "workload": "qwen3_32b_decode_16k: 32 seqs x 16384 tokens, 64 q / 8 KV heads, fp16, permuted blocks",
+        "kvarn_us": t_pk * 1e6, "kvarn_tokens_per_s": w.batch / t_pk, "kvarn_GBps": b_pk / t_pk / 1e9,
+        "kvarn_frac_hbm": b_pk / t_pk / 1e9 / hbm_peak, "kvarn_bytes": b_pk,
+        "fp16_us": t_16 * 1e6, "fp16_tokens_per_s": w.batch / t_16, "fp16_GBps": b_16 / t_16 / 1e9,
+        "fp16_frac_hbm": b_16 / t_16 / 1e9 / hbm_peak, "fp16_bytes": b_16,
+        "speedup_vs_fp16": t_16 / t_pk,
+        "context_tokens_per_s": w.batch * w.seq_lens[0] / t_pk,
+    }
+    del c, q, o
+    torch.cuda.empty_cache()
+
+    # --- write path: quantise 32 x 16384 tokens x 8 heads of bf16 (65536 tile jobs)
+    w = I.prefill_32b()
+    c = PagedCache(w, dev)
+    Bn, n = w.batch, w.seq_lens[0]
+    k = torch.empty(Bn * n, w.num_kv_heads, D, dtype=I.torch_dtype(w.dtype), device=dev)
+    v = torch.empty_like(k)
+    for b in range(Bn):
+        k[b * n:(b + 1) * n] = I.kv_sequence(w, "k", b, n, dev)
+        v[b * n:(b + 1) * n] = I.kv_sequence(w, "v", b, n, dev)
+    n_tiles = Bn * n // T
+    first = torch.arange(n_tiles, dtype=torch.int64, device=dev) * T
+    dst = c.table[:, : n // T].reshape(-1).contiguous()
+    fn = lambda: K.kvarn_quantize_tiles(c.cfg, k, v, w.num_kv_heads * D, Bn * n, first, dst, n_tiles, c.pool,
+                                        c.err)
+    t_q = timed(fn, 10)
+    assert c.check_error() == 0
+    jobs = n_tiles * w.num_kv_heads * 2
+    byt = jobs * (T * D * 2) + n_tiles * w.num_kv_heads * 13312 + n_tiles * 12
+    out["quantizer"] = {
+        "workload": "prefill_32b_16k: 32 x 16384 tokens x 8 KV heads, bf16, K and V tiles (65536 tile jobs)",
+        "us": t_q * 1e6, "tiles_per_s": jobs / t_q, "GBps": byt / t_q / 1e9, "frac_hbm": byt / t_q / 1e9 / hbm_peak,
+        "bytes": byt,
+    }
+    return out
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_step_sample(n_seqs, seed=4, threads=None):
+    """Prepare a bounded sample of the serving step for the oracle: n_seqs
+    sequences of the ragged mix with their packed cache (oracle-quantised)."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from bit_kv_cache_quantize_gb300 import inputs as I
+
+    w = I.ragged_32b(seed=seed)
+    seqs = list(range(n_seqs))
+    units = []
+    for b in seqs:
+        n = w.seq_lens[b]
+        k = I.kv_sequence(w, "k", b, n + 1)
+        v = I.kv_sequence(w, "v", b, n + 1)
+        kb = k.view(torch.int16).numpy().view(np.uint16)
+        vb = v.view(torch.int16).numpy().view(np.uint16)
+        nf = (n + 1) // T
+        for h in range(w.num_kv_heads):
+            first = np.array([t * T * w.num_kv_heads * D + h * D for t in range(nf)], np.int64)
+            kr, _ = O.quantize_batch(kb, "f16", first, w.num_kv_heads * D, False, nthreads=threads)
+            vr, _ = O.quantize_batch(vb, "f16", first, w.num_kv_heads * D, True, nthreads=threads)
+            units.append(dict(q=None, krec=list(kr), vrec=list(vr),
+                              ktail=O.decode16(kb[nf * T:n + 1, h], "f16").reshape(-1, D),
+                              vtail=O.decode16(vb[nf * T:n + 1, h], "f16").reshape(-1, D), b=b, h=h))
+    q = I.queries(w, step=1)
+    for u in units:
+        u["q"] = O.decode16(q[u["b"], u["h"] * w.G:(u["h"] + 1) * w.G].contiguous().view(torch.int16).numpy()
+                            .view(np.uint16), "f16")
+    return w, units
+
+
+def oracle_step(w, units, threads):
+    import numpy as np
+    import oracle as O
+    G = w.G
+    qa = np.stack([u["q"] for u in units])
+    kt = np.zeros((len(units), T, D)); vt = np.zeros((len(units), T, D))
+    nt = np.zeros(len(units), np.int32)
+    for i, u in enumerate(units):
+        m = u["ktail"].shape[0]
+        kt[i, :m] = u["ktail"]; vt[i, :m] = u["vtail"]; nt[i] = m
+    return O.attention_batch(qa, [u["krec"] for u in units], [u["vrec"] for u in units], kt, vt, nt, w.scale,
+                             nthreads=threads)
+
+
+def cpu_baseline(n_seqs=4, reps=1):
+    threads = os.cpu_count() or 1
+    w, units = oracle_step_sample(n_seqs, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(w, units, threads)
+    dt = (time.perf_counter() - t0) / reps
+    ctx = sum(w.seq_lens[:n_seqs])
+    return {"value": n_seqs / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"decode step (attention over the packed cache + open tile, folded fp64 form) of "
+                      f"{n_seqs} sequences x 8 KV heads x 8 queries of the ragged serving mix "
+                      f"({ctx} context tokens); {dt:.2f} s per step on {threads} threads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    w, units = oracle_step_sample(args.ref_seqs, threads=threads)
+    for _ in range(args.warmup):
+        oracle_step(w, units, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, units, threads)
+    dt = time.perf_counter() - t0
+    v = args.ref_seqs * args.steps / dt
+    sample = (f"{args.ref_seqs} sequences x 8 KV heads x 8 queries of the ragged serving mix per step, "
+              f"CPU oracle (fp64 folded attention) on {threads} threads")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "ragged_32b_serving (bounded sample, see cpu_baseline.sample)"},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
+    ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seqs", type=int, default=4)
+    ap.add_argument("--ref-seqs", type=int, default=2)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1 and args.impl != "reference":
+        import torch
+        torch.distributed.init_process_group("nccl")
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_gpu(args, rank, world)
+        if rank == 0 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.cpu_seqs)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+    if world > 1 and args.impl != "reference":
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -29,7 +29,8 @@
 namespace kvarn {
 
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int PART = D + 2;  // floats per split-K partial: m, l, acc[128]
+constexpr int PART = D + 4;  // floats per split-K partial: m, l, 2 pad, acc[128] (16-byte aligned)
+constexpr int PACC = 4;      // offset of acc[] in a partial
 
 
 __device__ __forceinline__ float* part_ptr(const DecodeParams& p, int b, int h, int chunk, int g) {
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
     }
     float* out = part_ptr(p, b, h, chunk, gg);
     if (tid == 0) { out[0] = M; out[1] = Lsum; }
-    out[2 + tid] = A;
+    out[PACC + tid] = A;
   }
 }
 
@@ -377,7 +378,7 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
   for (int gg = 0; gg < G; ++gg) {
     float* out = part_ptr(p, b, h, p.n_chunks, gg);
     if (tid == 0) { out[0] = ml[2 * gg]; out[1] = ml[2 * gg + 1]; }
-    out[2 + tid] = a[gg];
+    out[PACC + tid] = a[gg];
   }
 }
 
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p, int rotate
       const float* pp = part_ptr(p, b, h, i, g);
       const float f = (pp[0] == -INFINITY) ? 0.f : exp2f(pp[0] - M);
       Lsum += f * pp[1];
-      const float4 a = *reinterpret_cast<const float4*>(pp + 2 + 4 * lane);
+      const float4 a = *reinterpret_cast<const float4*>(pp + PACC + 4 * lane);
       x[0] += f * a.x; x[1] += f * a.y; x[2] += f * a.z; x[3] += f * a.w;
     }
     if (rotate) {  // x = x H over the 128 channels held 4 per lane
@@ -431,7 +432,7 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p, int rotate
       const float* pp = part_ptr(p, b, h, p.n_chunks, g);
       const float f = exp2f(pp[0] - M);
       Lsum += f * pp[1];
-      const float4 a = *reinterpret_cast<const float4*>(pp + 2 + 4 * lane);
+      const float4 a = *reinterpret_cast<const float4*>(pp + PACC + 4 * lane);
       x[0] += f * a.x; x[1] += f * a.y; x[2] += f * a.z; x[3] += f * a.w;
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
@@ -626,7 +627,7 @@ __global__ void __launch_bounds__(256, 1) decode_f16_kernel(const __grid_constan
     }
     float* o = part_ptr(p, b, h, chunk, gg);
     if (c == 0) { o[0] = M; o[1] = Lsum; }
-    o[2 + c] = A;
+    o[PACC + c] = A;
   }
 }
 

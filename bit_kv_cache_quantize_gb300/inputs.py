@@ -4,10 +4,13 @@ This module is shared by the CUDA path's tests and benchmark and by the
 oracle side of the tests; it holds none of the method's arithmetic, only the
 random numbers and shapes of the workloads.  Every value is a pure function
 of (seed, stream, element index): a counter-based generator (SplitMix64
-finaliser applied to the counter), so any element can be regenerated on any
-device without generating the rest.  Uniforms are exact 53-bit fractions;
-normals come from Box-Muller in float64, are rounded to float32 and then to
-the 16-bit storage type (each step round-to-nearest-even).
+finaliser applied to the counter), so any element can be regenerated without
+generating the rest.  Uniforms are exact 23-bit fractions; normals come from
+Box-Muller in float32 and are rounded to the 16-bit storage type
+(round-to-nearest-even).  The integer part is bit-identical on every device;
+float32 log/cos may differ in the last bit between CPU and GPU, so a test
+generates its inputs once, on one device, and hands the same bytes to both
+sides.
 
 Workloads (distributions of the page "Huawei's KVarN puts KV-cache
 quantization inside vLLM's backend", section "Reported benchmarks and the
@@ -64,13 +67,13 @@ def hash64(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
 
 
 def uniform(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
-    """U(0,1) in float64, never 0 or 1."""
-    h = _shr(hash64(seed, stream, idx), 11)
-    return (h.to(torch.float64) + 0.5) * (2.0 ** -53)
+    """U(0,1) in float32 (exact 23-bit fractions plus half a step), never 0 or 1."""
+    h = _shr(hash64(seed, stream, idx), 41)
+    return (h.to(torch.float32) + 0.5) * (2.0 ** -23)
 
 
 def normal(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
-    """N(0,1) in float64 (Box-Muller on two counters per value)."""
+    """N(0,1) in float32 (Box-Muller on two counters per value)."""
     i2 = idx.to(torch.int64) * 2
     u1 = uniform(seed, stream, i2)
     u2 = uniform(seed, stream, i2 + 1)
@@ -88,9 +91,9 @@ def student_t4(seed: int, stream: int, idx: torch.Tensor) -> torch.Tensor:
     return z / torch.sqrt(chi2 / 4.0)
 
 
-def to16(x64: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
-    """float64 -> float32 -> 16-bit, each rounding to nearest even."""
-    return x64.to(torch.float32).to(dtype)
+def to16(x: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
+    """float32 -> 16-bit, rounding to nearest even."""
+    return x.to(torch.float32).to(dtype)
 
 
 def torch_dtype(name: str) -> torch.dtype:
@@ -169,8 +172,8 @@ S_K, S_V, S_Q, S_OUTL, S_PERM = 10, 11, 12, 13, 14
 
 
 def outlier_gain(w: Workload, device="cpu") -> torch.Tensor:
-    """[H_kv, D] float64 multiplier applied to the keys (unrotated index)."""
-    gain = torch.ones(w.num_kv_heads, D, dtype=torch.float64, device=device)
+    """[H_kv, D] float32 multiplier applied to the keys (unrotated index)."""
+    gain = torch.ones(w.num_kv_heads, D, dtype=torch.float32, device=device)
     if w.k_outliers == "fixed":
         gain[:, list(OUTLIER_CHANNELS)] = OUTLIER_GAIN
     else:

@@ -26,7 +26,9 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
     assert c.check_error() == 0
     check_seqs = list(range(w.batch)) if check_seqs is None else check_seqs
     total = [n + steps for n in w.seq_lens]
-    ctx = {b: (I.kv_sequence(w, "k", b, total[b]), I.kv_sequence(w, "v", b, total[b])) for b in check_seqs}
+    # inputs generated once on the device; the oracle reads the same bytes
+    ctx = {b: (I.kv_sequence(w, "k", b, total[b], dev).cpu(), I.kv_sequence(w, "v", b, total[b], dev).cpu())
+           for b in check_seqs}
     # closed prefill tiles of the checked sequences: oracle records
     pre_ctx = {b: (ctx[b][0][:w.seq_lens[b]], ctx[b][1][:w.seq_lens[b]]) for b in check_seqs}
     recs = load_oracle_records(w, c, check_seqs, pre_ctx)
@@ -50,8 +52,8 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
         jobs, keys = [], []
         for b in closing:
             t = int(pos[b]) // T
-            full_k = I.kv_values(w, "k", b, t * T, T)
-            full_v = I.kv_values(w, "v", b, t * T, T)
+            full_k = I.kv_values(w, "k", b, t * T, T, dev).cpu()
+            full_v = I.kv_values(w, "v", b, t * T, T, dev).cpu()
             for h in range(w.num_kv_heads):
                 jobs += [(full_k[:, h], 0), (full_v[:, h], 1)]
                 keys += [(b, t, h, 0), (b, t, h, 1)]
@@ -66,7 +68,7 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
                 c.set_record(blk, h, kv, torch.from_numpy(rec).to(dev))
         if s % attend_every and s != steps - 1:
             continue
-        q = I.queries(w, step=s + 1)
+        q = I.queries(w, step=s + 1, device=dev).cpu()
         c.decode(q.to(dev), out, lens=lens.to(dev))
         torch.cuda.synchronize()
         assert c.check_error() == 0

@@ -70,11 +70,13 @@ def run_decode_case(w, seqs=None, full_gpu_prefill=False):
     dev = device()
     seqs = list(range(w.batch)) if seqs is None else seqs
     c = PagedCache(w, dev)
-    ctx = {b: (I.kv_sequence(w, "k", b, w.seq_lens[b]), I.kv_sequence(w, "v", b, w.seq_lens[b])) for b in seqs}
+    # inputs generated once on the device; the oracle reads the same bytes
+    ctx = {b: (I.kv_sequence(w, "k", b, w.seq_lens[b], dev).cpu(), I.kv_sequence(w, "v", b, w.seq_lens[b], dev).cpu())
+           for b in seqs}
     if full_gpu_prefill:
         c.prefill()            # every sequence, GPU quantiser
     recs = load_oracle_records(w, c, seqs, ctx)
-    q = I.queries(w)
+    q = I.queries(w, device=dev).cpu()
     out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
     c.decode(q.to(dev), out)
     torch.cuda.synchronize()
