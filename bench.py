@@ -405,6 +405,44 @@ def run_reference(args, rank, world):
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case(name, launches):
+    """Small single-kernel workloads for ncu captures (each > L2, a few GB at
+    most): the 16K decode (436 MB packed), the 16-bit decode on the same
+    shapes (2.1 GB), or the quantiser on 4 of the 32 prefill sequences."""
+    import torch
+    from bit_kv_cache_quantize_gb300 import build as B
+    from bit_kv_cache_quantize_gb300 import inputs as I
+    from bit_kv_cache_quantize_gb300 import kvarn as K
+    from bit_kv_cache_quantize_gb300.cache import PagedCache
+    B.build()
+    dev = torch.device("cuda", 0)
+    if name in ("decode16k", "fp16"):
+        w = I.qwen3_32b()
+        c = PagedCache(w, dev, fp16_pool=(name == "fp16"))
+        c.prefill()
+        q = I.queries(w, device=dev)
+        o = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+        fn = (lambda: c.decode(q, o)) if name == "decode16k" else (lambda: c.decode_fp16(q, o))
+    else:
+        w = I.prefill_32b()
+        w.batch = 4
+        w.seq_lens = w.seq_lens[:4]
+        c = PagedCache(w, dev)
+        Bn, n = w.batch, w.seq_lens[0]
+        k = torch.cat([I.kv_sequence(w, "k", b, n, dev) for b in range(Bn)])
+        v = torch.cat([I.kv_sequence(w, "v", b, n, dev) for b in range(Bn)])
+        nt = Bn * n // T
+        first = torch.arange(nt, dtype=torch.int64, device=dev) * T
+        dst = c.table[:, : n // T].reshape(-1).contiguous()
+        fn = lambda: K.kvarn_quantize_tiles(c.cfg, k, v, w.num_kv_heads * D, Bn * n, first, dst, nt, c.pool, c.err)
+    torch.cuda.synchronize()
+    for _ in range(launches):
+        fn()
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    print(json.dumps({"profile_case": name, "launches": launches}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -413,9 +451,14 @@ def main():
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
     ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seqs", type=int, default=4)
-    ap.add_argument("--ref-seqs", type=int, default=2)
+    ap.add_argument("--cpu-seqs", type=int, default=16)
+    ap.add_argument("--ref-seqs", type=int, default=1)
+    ap.add_argument("--profile-case", choices=["decode16k", "fp16", "quantize"], default=None)
+    ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args.profile_case, args.profile_launches)
+        return
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     if world > 1 and args.impl != "reference":

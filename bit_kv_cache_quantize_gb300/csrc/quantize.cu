@@ -124,49 +124,50 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
   float v0 = 0.f, v1 = 0.f;  // log column factors of c0, c0+1 (replicated over q)
   float u0 = 0.f, u1 = 0.f;  // log row factors of t0, t1 (replicated over j)
   for (int it = 0; it < iters; ++it) {
-    // column step on copy 2: std over tokens of w = alpha_t * R[t][c]
+    // column step on copy 2: std over tokens of w = alpha_t * R[t][c], as
+    // shifted sums of d = alpha_t * R - K (K = token 0's value), two channels
+    // per packed f32x2 op
     {
-      float s1a = 0.f, s2a = 0.f, s1b = 0.f, s2b = 0.f;
-      float Ka = 0.f, Kb = 0.f;
       const float* al = sm.alpha + q * 36;
+      const float2 w0 = make_float2(al[0] * r2[0].x, al[0] * r2[0].y);
+      const float Ka = __shfl_sync(0xffffffffu, w0.x, lane & ~3);
+      const float Kb = __shfl_sync(0xffffffffu, w0.y, lane & ~3);
+      const float2 nK = make_float2(-Ka, -Kb);
+      float2 s1e = make_float2(0.f, 0.f), s2e = s1e, s1o = s1e, s2o = s1e;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = al[i];
-        const float wa = __fmul_rn(a, r2[i].x), wb = __fmul_rn(a, r2[i].y);
-        if (i == 0) {
-          Ka = __shfl_sync(0xffffffffu, wa, lane & ~3);
-          Kb = __shfl_sync(0xffffffffu, wb, lane & ~3);
-        }
-        const float da = wa - Ka, db = wb - Kb;
-        s1a += da; s2a = fmaf(da, da, s2a);
-        s1b += db; s2b = fmaf(db, db, s2b);
+      for (int i = 0; i < 32; i += 2) {
+        const float2 de = ffma2(make_float2(al[i], al[i]), r2[i], nK);
+        const float2 dd = ffma2(make_float2(al[i + 1], al[i + 1]), r2[i + 1], nK);
+        s1e = fadd2(s1e, de); s2e = ffma2(de, de, s2e);
+        s1o = fadd2(s1o, dd); s2o = ffma2(dd, dd, s2o);
       }
-      s1a = quad_sum(s1a); s2a = quad_sum(s2a); s1b = quad_sum(s1b); s2b = quad_sum(s2b);
+      s1e = fadd2(s1e, s1o); s2e = fadd2(s2e, s2o);
+      const float s1a = quad_sum(s1e.x), s2a = quad_sum(s2e.x), s1b = quad_sum(s1e.y), s2b = quad_sum(s2e.y);
       v0 = log_std_or_keep(s1a, s2a, Ka, v0);
       v1 = log_std_or_keep(s1b, s2b, Kb, v1);
       if (q == 0) { sm.beta[c0] = expf(-v0); sm.beta[c0 + 1] = expf(-v1); }
     }
     __syncthreads();
-    // row step on copy 1: std over channels of w = beta_c * R[t][c]
+    // row step on copy 1: std over channels of w = beta_c * R[t][c]; packed
+    // over the channel pair, the two lanes of a pair accumulate separately
     {
-      float s1a = 0.f, s2a = 0.f, s1b = 0.f, s2b = 0.f;
-      float Ka = 0.f, Kb = 0.f;
+      const float2 be0 = *reinterpret_cast<const float2*>(sm.beta + 2 * j);
+      const float Ka = __shfl_sync(0xffffffffu, be0.x * r1[0][0], lane & ~3);  // channel 0 of token t0
+      const float Kb = __shfl_sync(0xffffffffu, be0.x * r1[0][2], lane & ~3);  // channel 0 of token t1
+      const float2 nKa = make_float2(-Ka, -Ka), nKb = make_float2(-Kb, -Kb);
+      float2 s1a = make_float2(0.f, 0.f), s2a = s1a, s1b = s1a, s2b = s1a;
 #pragma unroll
       for (int nb = 0; nb < 16; ++nb) {
         const float2 be = *reinterpret_cast<const float2*>(sm.beta + 8 * nb + 2 * j);
-        const float w0 = __fmul_rn(be.x, r1[nb][0]), w1 = __fmul_rn(be.y, r1[nb][1]);
-        const float w2 = __fmul_rn(be.x, r1[nb][2]), w3 = __fmul_rn(be.y, r1[nb][3]);
-        if (nb == 0) {
-          Ka = __shfl_sync(0xffffffffu, w0, lane & ~3);  // channel 0 of token t0
-          Kb = __shfl_sync(0xffffffffu, w2, lane & ~3);  // channel 0 of token t1
-        }
-        const float d0 = w0 - Ka, d1 = w1 - Ka, d2 = w2 - Kb, d3 = w3 - Kb;
-        s1a += d0 + d1; s2a = fmaf(d0, d0, fmaf(d1, d1, s2a));
-        s1b += d2 + d3; s2b = fmaf(d2, d2, fmaf(d3, d3, s2b));
+        const float2 da = ffma2(be, make_float2(r1[nb][0], r1[nb][1]), nKa);
+        const float2 db = ffma2(be, make_float2(r1[nb][2], r1[nb][3]), nKb);
+        s1a = fadd2(s1a, da); s2a = ffma2(da, da, s2a);
+        s1b = fadd2(s1b, db); s2b = ffma2(db, db, s2b);
       }
-      s1a = quad_sum(s1a); s2a = quad_sum(s2a); s1b = quad_sum(s1b); s2b = quad_sum(s2b);
-      u0 = log_std_or_keep(s1a, s2a, Ka, u0);
-      u1 = log_std_or_keep(s1b, s2b, Kb, u1);
+      const float S1a = quad_sum(s1a.x + s1a.y), S2a = quad_sum(s2a.x + s2a.y);
+      const float S1b = quad_sum(s1b.x + s1b.y), S2b = quad_sum(s2b.x + s2b.y);
+      u0 = log_std_or_keep(S1a, S2a, Ka, u0);
+      u1 = log_std_or_keep(S1b, S2b, Kb, u1);
       if (j == 0) { sm.alpha[alpha_idx(t0)] = expf(-u0); sm.alpha[alpha_idx(t1)] = expf(-u1); }
     }
     __syncthreads();
