@@ -23,12 +23,15 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "params.h"
 
 namespace kvarn {
 
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr int kMaxDevices = 64;
 constexpr int PART = D + 4;  // floats per split-K partial: m, l, 2 pad, acc[128] (16-byte aligned)
 constexpr int PACC = 4;      // offset of acc[] in a partial
 
@@ -653,6 +656,44 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
   return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, batch, out, s)
                                    : launch_decode_t<__half>(p, batch, out, s);
+}
+
+// ---- fixed-scratch variant of the packed decode (no allocation anywhere)
+//
+// The split-K partials normally live in a caller-provided workspace.  Some
+// callers cannot hand one over: an inference engine whose memory manager has
+// already claimed the free device memory for its paged cache and forbids
+// ad-hoc allocations, or a latency-critical decode loop where cudaMalloc /
+// cudaFree would synchronise the device.  For them the partials go into this
+// file-scope device array instead.  Every device that loads the library holds
+// it until the process exits.  In host code `g_decode_scratch` only names a
+// host-side stand-in, so its device address is looked up per device.
+static __device__ __align__(256) unsigned char g_decode_scratch[KVARN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_decode_scratch on the current device, looked up once
+// per device (on the first call that runs with that device current).
+static cudaError_t scratch_address(float** out) {
+  static std::atomic<void*> addr[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev].store(p, std::memory_order_release);
+  }
+  *out = static_cast<float*>(p);
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* out, cudaStream_t s) {
+  float* ws = nullptr;
+  cudaError_t e = scratch_address(&ws);
+  if (e != cudaSuccess) return e;
+  p.ws = ws;
+  return launch_decode(p, dtype, batch, out, s);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {

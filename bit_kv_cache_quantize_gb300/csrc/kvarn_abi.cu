@@ -123,6 +123,26 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
+kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                            int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                            const void* block_pool, const void* tail_pool, float softmax_scale,
+                                            float* out, int32_t* dev_err, void* stream) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || max_blocks < 1 || batch > 65535) return KVARN_ERR_INVALID;
+  if (batch == 0) return KVARN_OK;
+  if (!q || !block_table || !seq_lens || !block_pool || !tail_pool || !out) return KVARN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(block_pool) || !aligned16(tail_pool) || !aligned16(out)) return KVARN_ERR_INVALID;
+  const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles) > KVARN_NOALLOC_SCRATCH_BYTES)
+    return KVARN_ERR_UNSUPPORTED;  // larger than the fixed scratch: use kvarn_decode_attention
+  const int n_chunks = (max_blocks + kChunkTiles - 1) / kChunkTiles;
+  DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool, nullptr, dev_err,
+                 static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale, max_blocks, cfg->num_kv_heads,
+                 cfg->num_q_heads, G, cfg->num_blocks, kChunkTiles, n_chunks};
+  return cuda_status(launch_decode_noalloc(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
+}
+
 kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q, const int32_t* block_table,
                                          int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
                                          const void* fp16_pool, float softmax_scale, float* out, void* workspace,

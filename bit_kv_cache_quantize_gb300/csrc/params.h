@@ -59,6 +59,7 @@ cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStrea
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
                               int num_blocks, int num_kv_heads, float* out, int32_t* err, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s);
+cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* out, cudaStream_t s);
 cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,
                               cudaStream_t s);
 size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int chunk_tiles);

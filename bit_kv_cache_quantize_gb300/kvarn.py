@@ -27,7 +27,9 @@ EXPORTS = (
     "kvarn_block_bytes", "kvarn_tail_bytes", "kvarn_quantize_tiles", "kvarn_append_tokens",
     "kvarn_decode_workspace_bytes", "kvarn_decode_attention", "kvarn_dequantize",
     "kvarn_fp16_block_bytes", "kvarn_fp16_decode_attention", "kvarn_status_string",
+    "kvarn_decode_attention_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class kvarn_config(ctypes.Structure):
@@ -70,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "kvarn_append_tokens": (i32, [C, P, P, P, P, i32, i32, P, P, P, P]),
             "kvarn_decode_attention": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, sz, P, P]),
             "kvarn_fp16_decode_attention": (i32, [C, P, P, i32, P, i32, P, f32, P, P, sz, P, P]),
+            "kvarn_decode_attention_noalloc": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, P]),
             "kvarn_dequantize": (i32, [C, P, P, i32, P, P, P]),
             "kvarn_status_string": (ctypes.c_char_p, [i32]),
         }
@@ -145,6 +148,17 @@ def kvarn_decode_attention(cfg, q, block_table, max_blocks, seq_lens, batch, blo
                                       int(batch), _p(block_pool), _p(tail_pool), float(softmax_scale), _p(out),
                                       _p(workspace), int(workspace_bytes), _p(dev_err), _s(stream))
     return _check(st, "kvarn_decode_attention", check)
+
+
+def kvarn_decode_attention_noalloc(cfg, q, block_table, max_blocks, seq_lens, batch, block_pool, tail_pool,
+                                   softmax_scale, out, dev_err, stream=None, check=True) -> int:
+    """Decode attention with the split-K partials in the library's fixed
+    16 MiB device scratch instead of a caller workspace, for callers that
+    cannot allocate device memory (see include/kvarn.h)."""
+    st = lib().kvarn_decode_attention_noalloc(ctypes.byref(cfg), _p(q), _p(block_table), int(max_blocks),
+                                              _p(seq_lens), int(batch), _p(block_pool), _p(tail_pool),
+                                              float(softmax_scale), _p(out), _p(dev_err), _s(stream))
+    return _check(st, "kvarn_decode_attention_noalloc", check)
 
 
 def kvarn_fp16_decode_attention(cfg, q, block_table, max_blocks, seq_lens, batch, fp16_pool, softmax_scale, out,

@@ -18,7 +18,8 @@
  * Conventions for every entry point:
  *  - All pointers documented "device" are CUDA device pointers the caller
  *    owns and keeps alive until the stream work completes.  The library
- *    allocates nothing and keeps no global state.
+ *    allocates nothing and keeps no global state other than the fixed
+ *    scratch array of kvarn_decode_attention_noalloc.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL is the legacy default stream).  Device pointers must be 16-byte
  *    aligned; the library checks this on the host.
@@ -167,6 +168,38 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
                                     const void* block_pool, const void* tail_pool, float softmax_scale,
                                     float* out, void* workspace, size_t workspace_bytes,
                                     int32_t* dev_err, void* stream);
+
+/* Size of the fixed device scratch used by kvarn_decode_attention_noalloc. */
+#define KVARN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * kvarn_decode_attention without a workspace argument, for callers that
+ * cannot allocate device memory: for example an inference engine whose
+ * memory manager has already reserved the free device memory for its paged
+ * cache and forbids ad-hoc allocations, or a latency-critical decode loop in
+ * which cudaMalloc/cudaFree would synchronise the device.  The pages describe
+ * nothing like it; it is this library's own addition.
+ *
+ * Arguments, layouts and results are those of kvarn_decode_attention (the
+ * caller still passes every input and the output).  The split-K partials go
+ * to a fixed device array of KVARN_NOALLOC_SCRATCH_BYTES (16 MiB) that the
+ * library defines at file scope; every GPU that loads the library holds it
+ * until the process exits.  Nothing is allocated: no cudaMalloc, no cudaFree.
+ *  - A request that needs more scratch than that (batch * num_kv_heads *
+ *    (ceil(max_blocks / 16) + 1) * group * 528 bytes) returns
+ *    KVARN_ERR_UNSUPPORTED and launches nothing; use kvarn_decode_attention.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    every partial a call reads was written earlier in that same call, so no
+ *    clearing is needed.  Calls that overlap on the GPU (two streams, two
+ *    host threads) race on the array and must be serialised by the caller.
+ */
+kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                            int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                            const void* block_pool, const void* tail_pool, float softmax_scale,
+                                            float* out, int32_t* dev_err, void* stream);
 
 /*
  * Dequantise packed blocks back to the unrotated domain (tests and tools).
