@@ -57,29 +57,43 @@ __device__ __forceinline__ float to_f(E x) {
   else return __bfloat162float(x);
 }
 
-// Shared memory of one packed-decode CTA: per warp two stages of one
-// (tile, head) record pair (K 8704 B + V 4608 B), the rotated queries, and
-// the cross-warp merge area (aliases the stages at the end).
-constexpr int DEC_WARPS = 4;
-constexpr int DEC_STAGES = 2;
+// Shared memory of one packed-decode CTA: per warp one K-record buffer and
+// one V-record buffer -- the next tile's K record streams in while this
+// tile's V record is in use and vice versa -- the rotated queries, and the
+// cross-warp merge area (aliases the record buffers at the end).
+constexpr int DEC_WARPS = 8;
+constexpr int QK_ILP = 2;   // independent MMA chains interleaved in QK
+constexpr int PV_ILP = 4;   // and in PV
 struct DecSmem {
-  alignas(128) unsigned char stage[DEC_WARPS][DEC_STAGES][HEAD_REC];
+  alignas(128) unsigned char kbuf[DEC_WARPS][K_REC];
+  alignas(128) unsigned char vbuf[DEC_WARPS][V_REC];
   alignas(16) float qr[8][D];
-  uint64_t bar[DEC_WARPS][DEC_STAGES];
+  uint64_t kbar[DEC_WARPS];
+  uint64_t vbar[DEC_WARPS];
 };
 struct DecMerge {
   float m[DEC_WARPS][8];
   float l[DEC_WARPS][8];
   float acc[DEC_WARPS][8][D];
 };
-static_assert(sizeof(DecMerge) <= sizeof(DecSmem::stage), "merge area must fit the stages");
+static_assert(sizeof(DecMerge) <= sizeof(DecSmem::kbuf) + sizeof(DecSmem::vbuf), "merge area must fit");
 
 template <typename E>
 __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
 
-// grid (n_chunks + 1, H_kv, B); chunk n_chunks handles the raw open tile.
+// Unpacking codes to exact fp16 operands.  A code field ORed into the
+// mantissa of 1024.0 (0x6400) and 1024 subtracted gives the code exactly.
+// Fields at mantissa bits 0-3 / 4-7 of each 16-bit half are taken without a
+// shift; a field at bit offset 4 (nibble) or 2k (crumb) comes out multiplied
+// by 16 or 4^k, and the matching entries of the other operand are divided by
+// the same power of two, which is exact.
+constexpr uint32_t MAGIC = 0x64006400u;
+__device__ __forceinline__ uint32_t field(uint32_t x, uint32_t mask) { return unbias((x & mask) | MAGIC); }
+
+// grid (n_chunks + 1, H_kv, B) x 256 threads; chunk n_chunks handles the
+// raw open tile.  Warp w of a chunk takes its tiles first + w, first + w + 8.
 template <typename E>
-__global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
@@ -98,58 +112,60 @@ __global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
   if (n_tiles <= 0) return;
   DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw);
   const int G = p.G;
+  const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
+  const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
 
-  // per-warp barriers
+  // start this warp's first tile before anything else
   if (lane == 0) {
-    for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&sm.bar[warp][s], 1);
+    mbar_init(&sm.kbar[warp], 1);
+    mbar_init(&sm.vbar[warp], 1);
     fence_mbar_init();
   }
-  // rotated, scaled queries: qr[g][c] = scale * log2(e) * sum_k q[g][k] H[k][c]
-  {
-    const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
-    float* qraw = &sm.qr[0][0];  // temporarily holds the raw queries
-    for (int i = tid; i < 8 * D; i += 128) qraw[i] = (i < G * D) ? to_f(qb[i]) : 0.f;
-    __syncthreads();
-    float acc[8];
-#pragma unroll
-    for (int gg = 0; gg < 8; ++gg) acc[gg] = 0.f;
-    const int c = tid;
-    for (int k = 0; k < D; ++k) {
-      const float sgn = (__popc(k & c) & 1) ? -1.f : 1.f;
-#pragma unroll
-      for (int gg = 0; gg < 8; ++gg) acc[gg] = fmaf(sgn, qraw[gg * D + k], acc[gg]);
-    }
-    __syncthreads();
-    const float f = p.scale * LOG2E * INV_SQRT_D;
-#pragma unroll
-    for (int gg = 0; gg < 8; ++gg) sm.qr[gg][c] = acc[gg] * f;
-    __syncthreads();
-  }
-  float qreg[32];  // query g, channels 32j .. 32j+31
-#pragma unroll
-  for (int c = 0; c < 32; c += 4) {
-    const float4 v = *reinterpret_cast<const float4*>(&sm.qr[g][32 * j + c]);
-    qreg[c] = v.x; qreg[c + 1] = v.y; qreg[c + 2] = v.z; qreg[c + 3] = v.w;
-  }
-
-  // tiles of this warp: first + warp, first + warp + 4, ...
-  const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
-  const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
-  auto issue = [&](int k) {  // lane 0: start the copy of this warp's k-th tile
-    const int tile = first + warp + k * DEC_WARPS;
-    const int32_t blk = tab[tile];
-    const int s = k % DEC_STAGES;
+  __syncwarp();
+  auto issue = [&](int k, bool is_v) {  // lane 0: copy the K or V record of this warp's k-th tile
+    const int32_t blk = tab[first + warp + k * DEC_WARPS];
+    uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     if (blk >= 0 && blk < p.num_blocks) {
-      mbar_expect_tx(&sm.bar[warp][s], HEAD_REC);
-      bulk_g2s(sm.stage[warp][s], p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC, HEAD_REC, &sm.bar[warp][s]);
+      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC + (is_v ? K_REC : 0);
+      mbar_expect_tx(bar, is_v ? V_REC : K_REC);
+      bulk_g2s(is_v ? sm.vbuf[warp] : sm.kbuf[warp], src, is_v ? V_REC : K_REC, bar);
     } else {
       set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.bar[warp][s])) : "memory");
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
     }
   };
-  __syncwarp();
-  if (lane == 0)
-    for (int k = 0; k < min(my_n, DEC_STAGES); ++k) issue(k);
+  if (lane == 0 && my_n > 0) { issue(0, false); issue(0, true); }
+
+  // rotated, scaled queries: warp w < G rotates query w with a 128-point
+  // butterfly over 4 channels per lane; qr = scale * log2(e) * (q H)
+  {
+    const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (warp < G) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = to_f(qb[warp * D + 4 * lane + e]);
+    }
+    float u = x[0], v = x[1];
+    x[0] = u + v; x[1] = u - v;
+    u = x[2]; v = x[3];
+    x[2] = u + v; x[3] = u - v;
+    u = x[0]; v = x[2];
+    x[0] = u + v; x[2] = u - v;
+    u = x[1]; v = x[3];
+    x[1] = u + v; x[3] = u - v;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+        x[e] = upper ? (o - x[e]) : (x[e] + o);
+      }
+    }
+    const float f = p.scale * LOG2E * INV_SQRT_D;
+    *reinterpret_cast<float4*>(&sm.qr[warp][4 * lane]) = make_float4(x[0] * f, x[1] * f, x[2] * f, x[3] * f);
+  }
+  __syncthreads();
 
   float m_run = -INFINITY, l_run = 0.f;
   float acc[16][2];
@@ -157,152 +173,183 @@ __global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
   for (int nb = 0; nb < 16; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
 
   for (int k = 0; k < my_n; ++k) {
-    const int s = k % DEC_STAGES;
-    const int tile = first + warp + k * DEC_WARPS;
-    const int32_t blk = tab[tile];
-    const bool ok = mbar_wait_bounded(&sm.bar[warp][s], (k / DEC_STAGES) & 1, p.err);
-    if (ok && blk >= 0 && blk < p.num_blocks) {
-      const unsigned char* krec = sm.stage[warp][s];
-      const unsigned char* vrec = krec + K_REC;
+    const int32_t blk = tab[first + warp + k * DEC_WARPS];
+    const bool valid = blk >= 0 && blk < p.num_blocks;
+    const unsigned char* krec = sm.kbuf[warp];
+    const unsigned char* vrec = sm.vbuf[warp];
+    // a wait that gives up ends this warp's loop (after waiting, bounded, for
+    // the V copy it still has in flight); the error word is already set
+    if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.kbar[warp], k & 1, p.err))) {
+      mbar_wait_bounded(&sm.vbar[warp], k & 1, p.err);
+      break;
+    }
+    const bool kok = valid;
 
-      // ---- query fold: qg = q' * gK (channels 32j..32j+31), S, per-query scale
-      uint32_t afr[8][4];
-      float S, qs_inv;
-      {
-        float qg[32];
-        const uint4 g0 = *reinterpret_cast<const uint4*>(krec + 32 * j);
-        const uint4 g1 = *reinterpret_cast<const uint4*>(krec + 32 * j + 16);
-        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        float ssum = 0.f, amax = 0.f;
+    // ---- query fold: qg = q' * gK over channels 32j..32j+31, scaled so max |qg| is in [512, 1024)
+    uint32_t afr[8][4];
+    float S = 0.f, qs_inv = 1.f;
+    float sc[16][2];
+    float tmax = -INFINITY;
+    if (kok) {
+      float qg[32];
+      const uint4 g0 = *reinterpret_cast<const uint4*>(krec + 32 * j);
+      const uint4 g1 = *reinterpret_cast<const uint4*>(krec + 32 * j + 16);
+      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float* q = &sm.qr[g][32 * j];
+      float amax = 0.f;
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-          const float2 lo = e4m3x2_to_float2((uint16_t)(gw[w] & 0xFFFF));
-          const float2 hi = e4m3x2_to_float2((uint16_t)(gw[w] >> 16));
-          qg[4 * w] = qreg[4 * w] * lo.x; qg[4 * w + 1] = qreg[4 * w + 1] * lo.y;
-          qg[4 * w + 2] = qreg[4 * w + 2] * hi.x; qg[4 * w + 3] = qreg[4 * w + 3] * hi.y;
+      for (int w = 0; w < 8; ++w) {
+        const float4 qv = *reinterpret_cast<const float4*>(q + 4 * w);
+        const float2 lo = e4m3x2_to_float2((uint16_t)(gw[w] & 0xFFFF));
+        const float2 hi = e4m3x2_to_float2((uint16_t)(gw[w] >> 16));
+        qg[4 * w] = qv.x * lo.x; qg[4 * w + 1] = qv.y * lo.y;
+        qg[4 * w + 2] = qv.z * hi.x; qg[4 * w + 3] = qv.w * hi.y;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) { ssum += qg[4 * w + e]; amax = fmaxf(amax, fabsf(qg[4 * w + e])); }
-        }
-        S = quad_sum(ssum);
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        // power-of-two scale putting max |qg| in [512, 1024): exact, keeps the low parts normal
-        int ex = 0;
-        if (amax > 0.f) frexpf(amax, &ex);
-        const float qs = ldexpf(1.f, 10 - ex);
-        qs_inv = ldexpf(1.f, ex - 10);
+        for (int e = 0; e < 4; ++e) { S += qg[4 * w + e]; amax = fmaxf(amax, fabsf(qg[4 * w + e])); }
+      }
+      S = quad_sum(S);
+      amax = quad_max(amax);
+      int ex = 0;
+      if (amax > 0.f) frexpf(amax, &ex);
+      const float qs = ldexpf(1.f, 10 - ex), qs16 = ldexpf(1.f, 6 - ex);
+      qs_inv = ldexpf(1.f, ex - 10);
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const int w = kb >> 1, sh = 2 * (kb & 1);
-          const int c0 = 8 * w + sh, c1 = c0 + 4;  // local channels of b0; b1 uses c0+1, c1+1
-          uint16_t h00, l00, h01, l01, h10, l10, h11, l11;
-          split_hl<__half>(qg[c0] * qs, h00, l00); split_hl<__half>(qg[c1] * qs, h01, l01);
-          split_hl<__half>(qg[c0 + 1] * qs, h10, l10); split_hl<__half>(qg[c1 + 1] * qs, h11, l11);
-          afr[kb][0] = pack2(h00, h01);
-          afr[kb][1] = pack2(l00, l01);
-          afr[kb][2] = pack2(h10, h11);
-          afr[kb][3] = pack2(l10, l11);
-        }
+      for (int kb = 0; kb < 8; ++kb) {
+        const int c0 = 8 * (kb >> 1) + 2 * (kb & 1);  // b0: channels c0, c0+4 (x1); b1: c0+1, c0+5 (x16)
+        uint16_t h00, l00, h01, l01, h10, l10, h11, l11;
+        split_hl<__half>(qg[c0] * qs, h00, l00);
+        split_hl<__half>(qg[c0 + 4] * qs, h01, l01);
+        split_hl<__half>(qg[c0 + 1] * qs16, h10, l10);
+        split_hl<__half>(qg[c0 + 5] * qs16, h11, l11);
+        afr[kb][0] = pack2(h00, h01);
+        afr[kb][1] = pack2(l00, l01);
+        afr[kb][2] = pack2(h10, h11);
+        afr[kb][3] = pack2(l10, l11);
       }
 
-      // ---- QK: n-block nb covers tokens 32*(n>>1) + off(nb) + 8*(n&1), n = 0..7
-      float sc[16][2];  // scores (log2 units) of tokens 32j + off(nb) (+8)
-      float tmax = -INFINITY;
-      {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(krec + 128 + 32 * j);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(krec + 128 + 32 * j + 16);
-        const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const __half* bz = reinterpret_cast<const __half*>(krec + 256) + 32 * j;
+      // ---- QK: n-block nb holds tokens off(nb), off(nb) + 8 of this lane's 32
+      // (off = nb for nb < 8, nb + 8 otherwise); B rows = K codes of token
+      // 32 (g >> 1) + off(nb) + 8 (g & 1), channels 32j .. 32j+31
+      const __half* bz = reinterpret_cast<const __half*>(krec + 256) + 32 * j;
+      const unsigned char* az = krec + 128 + 32 * j;
 #pragma unroll
-        for (int nb = 0; nb < 16; ++nb) {
+      for (int n4 = 0; n4 < 16; n4 += QK_ILP) {
+        uint32_t kw[QK_ILP][4];
+#pragma unroll
+        for (int i = 0; i < QK_ILP; ++i) {
+          const int nb = n4 + i;
           const int off = nb < 8 ? nb : nb + 8;
-          const int tok = 32 * (g >> 1) + off + 8 * (g & 1);
-          const uint4 kw = *reinterpret_cast<const uint4*>(krec + 512 + tok * 64 + 16 * j);
-          const uint32_t kwa[4] = {kw.x, kw.y, kw.z, kw.w};
-          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint4 v4 = *reinterpret_cast<const uint4*>(krec + 512 + (32 * (g >> 1) + off + 8 * (g & 1)) * 64 + 16 * j);
+          kw[i][0] = v4.x; kw[i][1] = v4.y; kw[i][2] = v4.z; kw[i][3] = v4.w;
+        }
+        float c[QK_ILP][4];
 #pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-            const uint32_t x = kwa[kb >> 1];
-            const int sh = 2 * (kb & 1);
-            mma_f16(c, afr[kb], nib2(x, sh), nib2(x, sh + 1));
-          }
+        for (int i = 0; i < QK_ILP; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int r = off + 8 * e;  // local token index 0..31
-            const float a = e4m3_to_float((uint8_t)(aw[r >> 2] >> (8 * (r & 3))));
-            const float bzv = __half2float(bz[r]);
-            const float dot = (c[e] + c[2 + e]) * qs_inv;
-            sc[nb][e] = fmaf(a, dot, bzv * S);
-            tmax = fmaxf(tmax, sc[nb][e]);
+        for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+          for (int i = 0; i < QK_ILP; ++i) {
+            const uint32_t x = (kb & 1) ? (kw[i][kb >> 1] >> 8) : kw[i][kb >> 1];
+            mma_f16(c[i], afr[kb], field(x, 0x000F000Fu), field(x, 0x00F000F0u));
           }
         }
-      }
-
-      // ---- online softmax (log2 domain)
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
-      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
-      const float m_new = fmaxf(m_run, tmax);
-      const float corr = exp2f(m_run - m_new);
-      m_run = m_new;
-
-      // ---- PV: A = p * aV (hi rows 0-7, lo rows 8-15), B = 2-bit V codes
-      uint32_t pfr[8][4];
-      float psum = 0.f, pb = 0.f;
-      {
-        const uint4 a0 = *reinterpret_cast<const uint4*>(vrec + 128 + 32 * j);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(vrec + 128 + 32 * j + 16);
-        const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const __half* bz = reinterpret_cast<const __half*>(vrec + 256) + 32 * j;
-        uint16_t ph[16][2], pl[16][2];
 #pragma unroll
-        for (int nb = 0; nb < 16; ++nb) {
+        for (int i = 0; i < QK_ILP; ++i) {
+          const int nb = n4 + i;
           const int off = nb < 8 ? nb : nb + 8;
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int r = off + 8 * e;
-            const float pr = exp2f(sc[nb][e] - m_new);
-            psum += pr;
-            pb = fmaf(pr, __half2float(bz[r]), pb);
-            const float pa = pr * e4m3_to_float((uint8_t)(aw[r >> 2] >> (8 * (r & 3))));
-            split_hl<__half>(pa, ph[nb][e], pl[nb][e]);
-          }
+          const float2 dot = fmul2(fadd2(make_float2(c[i][0], c[i][1]), make_float2(c[i][2], c[i][3])),
+                                   make_float2(qs_inv, qs_inv));
+          const float2 a = make_float2(e4m3_to_float(az[off]), e4m3_to_float(az[off + 8]));
+          const float2 bb = make_float2(__half2float(bz[off]), __half2float(bz[off + 8]));
+          const float2 s2 = ffma2(a, dot, fmul2(bb, make_float2(S, S)));
+          sc[nb][0] = s2.x; sc[nb][1] = s2.y;
+          tmax = fmaxf(tmax, fmaxf(s2.x, s2.y));
         }
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          pfr[kb][0] = pack2(ph[2 * kb][0], ph[2 * kb][1]);
-          pfr[kb][1] = pack2(pl[2 * kb][0], pl[2 * kb][1]);
-          pfr[kb][2] = pack2(ph[2 * kb + 1][0], ph[2 * kb + 1][1]);
-          pfr[kb][3] = pack2(pl[2 * kb + 1][0], pl[2 * kb + 1][1]);
-        }
-      }
-      psum = quad_sum(psum);
-      pb = quad_sum(pb);
-      l_run = l_run * corr + psum;
-#pragma unroll
-      for (int nb = 0; nb < 16; ++nb) {
-        const uint2 vw = *reinterpret_cast<const uint2*>(vrec + 512 + (8 * nb + g) * 32 + 8 * j);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const int pr = 2 * kb;  // QK n-block pair (2kb) -> b0, (2kb+1) -> b1
-          const uint32_t x = (pr >> 3) ? vw.y : vw.x;
-          mma_f16(c, pfr[kb], crumb2(x, pr & 7), crumb2(x, (pr & 7) + 1));
-        }
-        const float2 gv = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vrec + 8 * nb + 2 * j));
-        acc[nb][0] = fmaf(acc[nb][0], corr, gv.x * (c[0] + c[2] + pb));
-        acc[nb][1] = fmaf(acc[nb][1], corr, gv.y * (c[1] + c[3] + pb));
       }
     }
     __syncwarp();
-    if (k + DEC_STAGES < my_n && lane == 0) {
+    if (lane == 0 && k + 1 < my_n) {  // this K buffer is free: fetch the next tile's K
       fence_proxy_async();
-      issue(k + DEC_STAGES);
+      issue(k + 1, false);
+    }
+    if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.vbar[warp], k & 1, p.err))) {
+      if (k + 1 < my_n) mbar_wait_bounded(&sm.kbar[warp], (k + 1) & 1, p.err);
+      break;
+    }
+    const bool vok = kok;
+    if (vok) {
+      // ---- online softmax (log2 domain)
+      tmax = quad_max(tmax);
+      const float m_new = fmaxf(m_run, tmax);
+      const float corr = exp2f(m_run - m_new);
+      m_run = m_new;
+      // ---- P = p * aV * 64 / slot scale, hi rows 0-7 / lo rows 8-15
+      uint32_t pfr[8][4];
+      float2 psum = make_float2(0.f, 0.f), pb = psum;
+      const __half* bz = reinterpret_cast<const __half*>(vrec + 256) + 32 * j;
+      const unsigned char* az = vrec + 128 + 32 * j;
+#pragma unroll
+      for (int nb = 0; nb < 16; ++nb) {
+        const int off = nb < 8 ? nb : nb + 8;
+        const float2 pr = make_float2(exp2f(sc[nb][0] - m_new), exp2f(sc[nb][1] - m_new));
+        psum = fadd2(psum, pr);
+        pb = ffma2(pr, make_float2(__half2float(bz[off]), __half2float(bz[off + 8])), pb);
+        const float f = 64.f / (float)(1 << (2 * (nb & 3)));  // undo the slot scale of this pair
+        const float2 pa = fmul2(pr, make_float2(e4m3_to_float(az[off]) * f, e4m3_to_float(az[off + 8]) * f));
+        const __half2 hi = __floats2half2_rn(pa.x, pa.y);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(pa.x - hf.x, pa.y - hf.y);
+        const uint32_t hb = *reinterpret_cast<const uint32_t*>(&hi), lb = *reinterpret_cast<const uint32_t*>(&lo);
+        pfr[nb >> 1][(nb & 1) ? 2 : 0] = hb;
+        pfr[nb >> 1][(nb & 1) ? 3 : 1] = lb;
+      }
+      const float ps = quad_sum(psum.x + psum.y);
+      const float pbs = quad_sum(pb.x + pb.y);
+      l_run = l_run * corr + ps;
+      // ---- PV: B = 2-bit V codes of channel 8nb + g, tokens 32j .. 32j+31
+#pragma unroll
+      for (int n4 = 0; n4 < 16; n4 += PV_ILP) {
+        uint32_t vw[PV_ILP][2];
+#pragma unroll
+        for (int i = 0; i < PV_ILP; ++i) {
+          const uint2 v2 = *reinterpret_cast<const uint2*>(vrec + 512 + (8 * (n4 + i) + g) * 32 + 8 * j);
+          vw[i][0] = v2.x; vw[i][1] = v2.y;
+        }
+        float c[PV_ILP][4];
+#pragma unroll
+        for (int i = 0; i < PV_ILP; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          // pairs 2kb, 2kb+1 = crumb fields s, s+1 (s = 2kb & 7) of word kb >> 2
+          const int sh = (2 * kb) & 7;
+#pragma unroll
+          for (int i = 0; i < PV_ILP; ++i) {
+            const uint32_t x = (sh & 4) ? (vw[i][kb >> 2] >> 8) : vw[i][kb >> 2];
+            const uint32_t m0 = 0x00030003u << (2 * (sh & 3));
+            mma_f16(c[i], pfr[kb], field(x, m0), field(x, m0 << 2));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < PV_ILP; ++i) {
+          const int nb = n4 + i;
+          const float2 gv = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vrec + 8 * nb + 2 * j));
+          const float o0 = fmaf(c[i][0] + c[i][2], 1.f / 64.f, pbs);
+          const float o1 = fmaf(c[i][1] + c[i][3], 1.f / 64.f, pbs);
+          acc[nb][0] = fmaf(acc[nb][0], corr, gv.x * o0);
+          acc[nb][1] = fmaf(acc[nb][1], corr, gv.y * o1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && k + 1 < my_n) {  // this V buffer is free: fetch the next tile's V
+      fence_proxy_async();
+      issue(k + 1, true);
     }
   }
 
-  // ---- merge the 4 warps and write this CTA's partial
+  // ---- merge the warps and write this CTA's partial
   __syncthreads();
-  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.stage);
+  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.kbuf);
   if (j == 0) { mg.m[warp][g] = m_run; mg.l[warp][g] = l_run; }
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) {
@@ -310,7 +357,8 @@ __global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
     mg.acc[warp][g][8 * nb + 2 * j + 1] = acc[nb][1];
   }
   __syncthreads();
-  for (int gg = 0; gg < G; ++gg) {
+  for (int i = tid; i < G * D; i += 256) {
+    const int gg = i / D, c = i % D;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, mg.m[w][gg]);
@@ -320,12 +368,12 @@ __global__ void __launch_bounds__(128) decode_packed_kernel(DecodeParams p) {
       for (int w = 0; w < DEC_WARPS; ++w) {
         const float f = exp2f(mg.m[w][gg] - M);
         Lsum += f * mg.l[w][gg];
-        A += f * mg.acc[w][gg][tid];
+        A += f * mg.acc[w][gg][c];
       }
     }
-    float* out = part_ptr(p, b, h, chunk, gg);
-    if (tid == 0) { out[0] = M; out[1] = Lsum; }
-    out[PACC + tid] = A;
+    float* o = part_ptr(p, b, h, chunk, gg);
+    if (c == 0) { o[0] = M; o[1] = Lsum; }
+    o[PACC + c] = A;
   }
 }
 
@@ -340,7 +388,7 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
   float* ml = pr + 8 * T;                      // [8][2]
   const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
   const float f = p.scale * LOG2E;
-  for (int i = tid; i < G * D; i += 128) qs[i] = to_f(qb[i]) * f;
+  for (int i = tid; i < G * D; i += blockDim.x) qs[i] = to_f(qb[i]) * f;
   __syncthreads();
   const E* kt = static_cast<const E*>(p.tail) + (((int64_t)b * p.num_kv_heads + h) * 2 + 0) * (T * D);
   const E* vt = kt + T * D;
@@ -369,6 +417,7 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
     ml[2 * tid + 1] = l;
   }
   __syncthreads();
+  if (tid >= D) return;
   float a[8];
 #pragma unroll
   for (int gg = 0; gg < 8; ++gg) a[gg] = 0.f;
@@ -537,7 +586,9 @@ __global__ void __launch_bounds__(256, 1) decode_f16_kernel(const __grid_constan
   for (int k = 0; k < n_tiles; ++k) {
     const int s = k % F16_STAGES;
     const int32_t blk = tab[first + k];
-    const bool ok = mbar_wait_bounded(&sm.bar[s], (k / F16_STAGES) & 1, p.err);
+    // a wait that gives up (error word set) ends the loop for the whole CTA
+    if (__syncthreads_or(!mbar_wait_bounded(&sm.bar[s], (k / F16_STAGES) & 1, p.err))) break;
+    const bool ok = true;
     const int valid = min(T, len - (first + k) * T);
     if (ok && blk >= 0 && blk < p.num_blocks && 16 * warp < valid) {
       const unsigned char* kt = sm.stage[s];
@@ -645,7 +696,7 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
   const size_t smem = sizeof(DecSmem);
   cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 128, smem, s>>>(p);
+  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;

@@ -24,276 +24,360 @@
 
 namespace kvarn {
 
-// Shared memory of one quantiser CTA (dynamic, ~78 KB).
+// Shared memory of one quantiser CTA (~66 KB).  One area is reused: first
+// the 16-bit tile (128 x 272 B), then per-warp transposition slabs (8 x 8 KB),
+// then the packed record, the column partial sums and per-token scale pairs.
 struct QSmem {
-  alignas(128) unsigned char big[65536];   // X staging (128 x 272 B), then R fp32 (swizzled)
-  alignas(16) unsigned char rec[512 + 128 * 68];  // header | codes (K rows padded to 68 B)
-  float alpha[4 * 36];                     // row factors exp(-u), padded per 32 tokens
-  float beta[128];                         // column factors exp(-v)
-  float inv_g[128];
-  float inv_a[128];
-  float bval[128];
-  float red[8];
+  alignas(128) unsigned char xs[65536];
+  float beta[D];                            // column factors exp(-v) of the last column step
+  float inv_g[D];
+  float vred[8];
 };
-
 constexpr int X_ROW = 272;                 // staging row stride: 256 B + 16 B pad
+constexpr int OFF_PART = 9216;             // float2 [8 warps][128]: column (mean, M2) over 16 tokens
+constexpr int OFF_TOK = 17408;             // float2 [128]: (zero-point, 1/step) per token
+static_assert(OFF_TOK + 128 * 8 <= 65536 && T * 272 <= 65536, "staging reuse overflows");
 
-__device__ __forceinline__ int alpha_idx(int t) { return (t >> 5) * 36 + (t & 31); }
-
-// Byte offset of the float2 holding R[t][2*c2 .. 2*c2+1] (XOR swizzle keeps
-// both the token-major writes and the channel-major reads conflict-free).
-__device__ __forceinline__ int r_off(int t, int c2) {
-  return t * 512 + ((c2 ^ (((t ^ (t >> 5)) & 3) << 2)) << 3);
+// New log factor ln(std) from a population variance and mean over 128
+// values; keeps `old` when the std is at most 1e-6 of the rms (a constant or
+// all-zero row/column).
+__device__ __forceinline__ float log_std_or_keep(float var, float mean, float old) {
+  var = fmaxf(var, 0.0f);
+  return (var > 1e-12f * (var + mean * mean)) ? logf(sqrtf(var)) : old;
 }
 
-// New log factor from shifted sums over n = 128 values: s1 = sum(w - K),
-// s2 = sum((w - K)^2).  Keeps `old` when the std is at most 1e-6 of the rms
-// (constant or all-zero row/column).
-__device__ __forceinline__ float log_std_or_keep(float s1, float s2, float K, float old) {
-  const float inv_n = 1.0f / 128.0f;
-  float md = s1 * inv_n;
-  float var = fmaxf(s2 * inv_n - md * md, 0.0f);
-  float mw = K + md;
-  float ms = var + mw * mw;
-  return (var > 1e-12f * ms) ? logf(sqrtf(var)) : old;
+// Sum of 16 values (8 tokens x 2 quantities, index 2i + m) across the 16 lanes
+// of a half-warp: recursive halving over lane bits 3, 2, 1, then a butterfly
+// over bit 0.  Lane ends with the two totals of token ti = (lane & 15) >> 1.
+// Selects keep every register index static.
+template <typename Op>
+__device__ __forceinline__ void halve16(float (&t)[8][2], int lane, Op op, float& r0, float& r1) {
+  const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+  float a[4][2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const float keep = b3 ? t[q + 4][m] : t[q][m];
+      const float send = b3 ? t[q][m] : t[q + 4][m];
+      a[q][m] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+  float c[2][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const float keep = b2 ? a[q + 2][m] : a[q][m];
+      const float send = b2 ? a[q][m] : a[q + 2][m];
+      c[q][m] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+  float d[2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const float keep = b1 ? c[1][m] : c[0][m];
+    const float send = b1 ? c[0][m] : c[1][m];
+    d[m] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+  r0 = op(d[0], __shfl_xor_sync(0xffffffffu, d[0], 1));
+  r1 = op(d[1], __shfl_xor_sync(0xffffffffu, d[1], 1));
 }
+
+// The 8 per-token values v[0..7] (identical in every lane of the half-warp)
+// reduced the same way: value of token ti.
+__device__ __forceinline__ float pick8(const float (&v)[8], int lane) {
+  const int ti = (lane & 15) >> 1;
+  float r = v[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) r = (ti == i) ? v[i] : r;
+  return r;
+}
+
+struct AddOp { __device__ float operator()(float a, float b) const { return a + b; } };
+struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
+struct MaxOp { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
 
 // Quantise one tile.  src: token rows of 128 16-bit channels, consecutive
 // rows row_stride elements apart (16-byte aligned).  dst: the record in the
-// pool.  All 256 threads of the CTA must call this.
+// pool.  All 256 threads of the CTA must call this.  After the rotation every
+// thread holds one 8-token x 8-channel block of R: tokens 16w + 8(l >> 4) +
+// 0..7, channels 8(l & 15) + 0..7 (warp w, lane l).
 template <typename E, bool IS_V>
 __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride, unsigned char* __restrict__ dst,
                                   int iters, QSmem& sm) {
   constexpr int L = IS_V ? 3 : 15;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, j = lane & 3;  // copy 1: token g (+8) of the warp's 16, channel pair j of each 8
-  const int p = g, q = j;                 // copy 2: channel pair p of the warp's 16, tokens 32q..32q+31
+  const int g = lane >> 2, j = lane & 3;          // MMA fragment coordinates
+  const int tbl = lane >> 4, cb = lane & 15;       // 8x8 block coordinates
+  const int tok0 = 16 * warp + 8 * tbl;            // first token of this thread's block
 
   // ---- 1. stage X (16-bit) into shared memory
   for (int i = tid; i < T * 16; i += 256) {
-    int row = i >> 4, ch16 = i & 15;
-    cp_async16(sm.big + row * X_ROW + ch16 * 16, src + row * row_stride + ch16 * 8);
+    const int row = i >> 4, ch16 = i & 15;
+    cp_async16(sm.xs + row * X_ROW + ch16 * 16, src + row * row_stride + ch16 * 8);
   }
-  for (int i = tid; i < T; i += 256) sm.alpha[alpha_idx(i)] = 1.0f;
   cp_async_wait_all();
   __syncthreads();
-
   uint32_t afr[8][4];
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
-    ldmatrix_x4(afr[ks], sm.big + (16 * warp + (lane & 15)) * X_ROW + (16 * ks + (lane >> 4) * 8) * 2);
-  __syncthreads();  // the staging area is reused for R below
+    ldmatrix_x4(afr[ks], sm.xs + (16 * warp + (lane & 15)) * X_ROW + (16 * ks + (lane >> 4) * 8) * 2);
+  __syncthreads();  // the staging area is reused below
 
   // ---- 2. R = X H on the tensor cores; H[k][n] = (-1)^popcount(k & n)
   // For k = 16ks + kk, n = 8nb + g:  popcount(k & n) = popcount(kk & g)
   // + (kk >> 3) * (nb & 1) + popcount(ks & (nb >> 1)), so every B fragment is
   // +-F with F the lane's base sign pair.
-  const uint32_t one = Bits16<E>::one;
-  const uint32_t F = ((__popc((2 * j) & g) & 1) ? (one | 0x8000u) : one) |
-                     (((__popc((2 * j + 1) & g) & 1) ? (one | 0x8000u) : one) << 16);
-  const uint32_t NF = F ^ 0x80008000u;
-  float r1[16][4];  // copy 1: R[16w+g][8nb+2j+{0,1}] and R[16w+g+8][...]
+  float2 r[8][4];  // r[i][p] = R[tok0 + i][8cb + 2p .. 2p+1]
+  {
+    const uint32_t one = Bits16<E>::one;
+    const uint32_t F = ((__popc((2 * j) & g) & 1) ? (one | 0x8000u) : one) |
+                       (((__popc((2 * j + 1) & g) & 1) ? (one | 0x8000u) : one) << 16);
+    const uint32_t NF = F ^ 0x80008000u;
+    float acc[16][4];
 #pragma unroll
-  for (int nb = 0; nb < 16; ++nb) {
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int nb = 0; nb < 16; ++nb) {
+      acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int P = __builtin_popcount(ks & (nb >> 1)) & 1;
-      const uint32_t b0 = P ? NF : F;
-      const uint32_t b1 = (P ^ (nb & 1)) ? NF : F;
-      mma16816<E>(c, afr[ks], b0, b1);
+      for (int ks = 0; ks < 8; ++ks) {
+        const int P = __builtin_popcount(ks & (nb >> 1)) & 1;
+        mma16816<E>(acc[nb], afr[ks], P ? NF : F, (P ^ (nb & 1)) ? NF : F);
+      }
     }
+    // transpose the warp's 16 x 128 slab into 8x8 blocks through 8 KB of
+    // shared memory (XOR-swizzled columns keep both sides conflict-light)
+    float* slab = reinterpret_cast<float*>(sm.xs) + warp * 2048;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) r1[nb][e] = c[e] * INV_SQRT_D;
+    for (int nb = 0; nb < 16; ++nb) {
+      const int col = (8 * nb + 2 * j) ^ (8 * (g & 3));
+      *reinterpret_cast<float2*>(slab + g * 128 + col) = make_float2(acc[nb][0] * INV_SQRT_D, acc[nb][1] * INV_SQRT_D);
+      *reinterpret_cast<float2*>(slab + (g + 8) * 128 + col) =
+          make_float2(acc[nb][2] * INV_SQRT_D, acc[nb][3] * INV_SQRT_D);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float4 v = *reinterpret_cast<const float4*>(slab + (8 * tbl + i) * 128 + ((8 * cb + 4 * hh) ^ (8 * (i & 3))));
+        r[i][2 * hh] = make_float2(v.x, v.y);
+        r[i][2 * hh + 1] = make_float2(v.z, v.w);
+      }
   }
-
-  // ---- transpose through shared memory into copy 2 (channel-major)
-  const int t0 = 16 * warp + g, t1 = t0 + 8;
-#pragma unroll
-  for (int nb = 0; nb < 16; ++nb) {
-    *reinterpret_cast<float2*>(sm.big + r_off(t0, 4 * nb + j)) = make_float2(r1[nb][0], r1[nb][1]);
-    *reinterpret_cast<float2*>(sm.big + r_off(t1, 4 * nb + j)) = make_float2(r1[nb][2], r1[nb][3]);
-  }
-  __syncthreads();
-  const int c0 = 16 * warp + 2 * p;  // copy-2 channels c0, c0 + 1
-  float2 r2[32];                     // R[32q + i][c0 .. c0+1]
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r2[i] = *reinterpret_cast<const float2*>(sm.big + r_off(32 * q + i, 8 * warp + p));
+  float2* part = reinterpret_cast<float2*>(sm.xs + OFF_PART);
+  float2* tokv = reinterpret_cast<float2*>(sm.xs + OFF_TOK);
+  __syncthreads();  // slabs done: the staging area now holds partials and the record
 
   // ---- 3. Sinkhorn-like iterations
-  float v0 = 0.f, v1 = 0.f;  // log column factors of c0, c0+1 (replicated over q)
-  float u0 = 0.f, u1 = 0.f;  // log row factors of t0, t1 (replicated over j)
+  // column step: per thread, shifted sums over its 8 tokens of w = alpha_t
+  // R[t][c] with shift = w at its first token (exact zero for a constant
+  // column), turned into (mean, M2) and merged across threads pairwise
+  // (M2 = M2a + M2b + d^2 na nb / (na + nb), d = difference of the means);
+  // row step: shifted sums over channels of w = beta_c R[t][c], shift = the
+  // row's channel-0 value, the same in every lane of the half-warp.
+  float al[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) al[i] = 1.f;
+  float v_c = 0.f;   // log factor of channel tid (tid < 128)
+  float u_t = 0.f;   // log factor of token tok0 + ((lane & 15) >> 1)
   for (int it = 0; it < iters; ++it) {
-    // column step on copy 2: std over tokens of w = alpha_t * R[t][c], as
-    // shifted sums of d = alpha_t * R - K (K = token 0's value), two channels
-    // per packed f32x2 op
     {
-      const float* al = sm.alpha + q * 36;
-      const float2 w0 = make_float2(al[0] * r2[0].x, al[0] * r2[0].y);
-      const float Ka = __shfl_sync(0xffffffffu, w0.x, lane & ~3);
-      const float Kb = __shfl_sync(0xffffffffu, w0.y, lane & ~3);
-      const float2 nK = make_float2(-Ka, -Kb);
-      float2 s1e = make_float2(0.f, 0.f), s2e = s1e, s1o = s1e, s2o = s1e;
+      const float2 a0 = make_float2(al[0], al[0]);
+      float2 nK[4], s1[4], s2[4];
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 de = ffma2(make_float2(al[i], al[i]), r2[i], nK);
-        const float2 dd = ffma2(make_float2(al[i + 1], al[i + 1]), r2[i + 1], nK);
-        s1e = fadd2(s1e, de); s2e = ffma2(de, de, s2e);
-        s1o = fadd2(s1o, dd); s2o = ffma2(dd, dd, s2o);
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 K = fmul2(a0, r[0][pp]);
+        nK[pp] = make_float2(-K.x, -K.y);
+        s1[pp] = s2[pp] = make_float2(0.f, 0.f);
       }
-      s1e = fadd2(s1e, s1o); s2e = fadd2(s2e, s2o);
-      const float s1a = quad_sum(s1e.x), s2a = quad_sum(s2e.x), s1b = quad_sum(s1e.y), s2b = quad_sum(s2e.y);
-      v0 = log_std_or_keep(s1a, s2a, Ka, v0);
-      v1 = log_std_or_keep(s1b, s2b, Kb, v1);
-      if (q == 0) { sm.beta[c0] = expf(-v0); sm.beta[c0 + 1] = expf(-v1); }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 a2 = make_float2(al[i], al[i]);
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          const float2 d = ffma2(a2, r[i][pp], nK[pp]);
+          s1[pp] = fadd2(s1[pp], d);
+          s2[pp] = ffma2(d, d, s2[pp]);
+        }
+      }
+      float2 mean[4], M2[4];   // over this thread's 8 tokens
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        mean[pp] = ffma2(s1[pp], make_float2(0.125f, 0.125f), make_float2(-nK[pp].x, -nK[pp].y));
+        M2[pp] = ffma2(fmul2(s1[pp], make_float2(-0.125f, -0.125f)), s1[pp], s2[pp]);
+      }
+      // lane pair (tbl 0, tbl 1) shares channels: tbl 0 keeps pairs 0-1, tbl 1 keeps 2-3
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const float2 km = tbl ? mean[q + 2] : mean[q], kM = tbl ? M2[q + 2] : M2[q];
+        const float2 om = tbl ? mean[q] : mean[q + 2], oM = tbl ? M2[q] : M2[q + 2];
+        const float2 pm = make_float2(__shfl_xor_sync(0xffffffffu, om.x, 16), __shfl_xor_sync(0xffffffffu, om.y, 16));
+        const float2 pM = make_float2(__shfl_xor_sync(0xffffffffu, oM.x, 16), __shfl_xor_sync(0xffffffffu, oM.y, 16));
+        const float2 dl = make_float2(km.x - pm.x, km.y - pm.y);
+        const float2 m16 = fmul2(fadd2(km, pm), make_float2(0.5f, 0.5f));
+        const float2 M16 = ffma2(fmul2(dl, make_float2(4.f, 4.f)), dl, fadd2(kM, pM));
+        const int c = 8 * cb + 4 * tbl + 2 * q;
+        part[warp * D + c] = make_float2(m16.x, M16.x);
+        part[warp * D + c + 1] = make_float2(m16.y, M16.y);
+      }
     }
     __syncthreads();
-    // row step on copy 1: std over channels of w = beta_c * R[t][c]; packed
-    // over the channel pair, the two lanes of a pair accumulate separately
-    {
-      const float2 be0 = *reinterpret_cast<const float2*>(sm.beta + 2 * j);
-      const float Ka = __shfl_sync(0xffffffffu, be0.x * r1[0][0], lane & ~3);  // channel 0 of token t0
-      const float Kb = __shfl_sync(0xffffffffu, be0.x * r1[0][2], lane & ~3);  // channel 0 of token t1
-      const float2 nKa = make_float2(-Ka, -Ka), nKb = make_float2(-Kb, -Kb);
-      float2 s1a = make_float2(0.f, 0.f), s2a = s1a, s1b = s1a, s2b = s1a;
+    if (tid < D) {
+      float mw[8], msum = 0.f, M2 = 0.f;
 #pragma unroll
-      for (int nb = 0; nb < 16; ++nb) {
-        const float2 be = *reinterpret_cast<const float2*>(sm.beta + 8 * nb + 2 * j);
-        const float2 da = ffma2(be, make_float2(r1[nb][0], r1[nb][1]), nKa);
-        const float2 db = ffma2(be, make_float2(r1[nb][2], r1[nb][3]), nKb);
-        s1a = fadd2(s1a, da); s2a = ffma2(da, da, s2a);
-        s1b = fadd2(s1b, db); s2b = ffma2(db, db, s2b);
+      for (int w = 0; w < 8; ++w) {
+        const float2 v = part[w * D + tid];
+        mw[w] = v.x; msum += v.x; M2 += v.y;
       }
-      const float S1a = quad_sum(s1a.x + s1a.y), S2a = quad_sum(s2a.x + s2a.y);
-      const float S1b = quad_sum(s1b.x + s1b.y), S2b = quad_sum(s2b.x + s2b.y);
-      u0 = log_std_or_keep(S1a, S2a, Ka, u0);
-      u1 = log_std_or_keep(S1b, S2b, Kb, u1);
-      if (j == 0) { sm.alpha[alpha_idx(t0)] = expf(-u0); sm.alpha[alpha_idx(t1)] = expf(-u1); }
+      const float mean = msum * 0.125f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) M2 = fmaf(16.f * (mw[w] - mean), mw[w] - mean, M2);
+      v_c = log_std_or_keep(M2 * (1.0f / 128.0f), mean, v_c);
+      sm.beta[tid] = expf(-v_c);
     }
     __syncthreads();
+    // row step
+    {
+      const float4 b0 = *reinterpret_cast<const float4*>(sm.beta + 8 * cb);
+      const float4 b1 = *reinterpret_cast<const float4*>(sm.beta + 8 * cb + 4);
+      const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                            make_float2(b1.z, b1.w)};
+      float Kt[8], t[8][2];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        Kt[i] = __shfl_sync(0xffffffffu, bp[0].x * r[i][0].x, lane & 16);  // channel 0 of token i
+        const float2 nK = make_float2(-Kt[i], -Kt[i]);
+        float2 s1 = make_float2(0.f, 0.f), s2 = s1;
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+          const float2 d = ffma2(bp[pp], r[i][pp], nK);
+          s1 = fadd2(s1, d);
+          s2 = ffma2(d, d, s2);
+        }
+        t[i][0] = s1.x + s1.y;
+        t[i][1] = s2.x + s2.y;
+      }
+      float S1, S2;
+      halve16(t, lane, AddOp(), S1, S2);
+      const float md = S1 * (1.0f / 128.0f);
+      u_t = log_std_or_keep(S2 * (1.0f / 128.0f) - md * md, pick8(Kt, lane) + md, u_t);
+      const float a_mine = expf(-u_t);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) al[i] = __shfl_sync(0xffffffffu, a_mine, (lane & 16) | (2 * i));
+    }
   }
 
   // ---- 4. gauge and per-channel FP8 scales
+  unsigned char* rec = sm.xs;
   {
-    float s = (q == 0) ? (v0 + v1) : 0.f;
+    float s = (tid < D) ? v_c : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) sm.red[warp] = s;
+    if (lane == 0) sm.vred[warp] = s;
   }
   __syncthreads();
-  {
+  if (tid < D) {
     float mean = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) mean += sm.red[w];
+    for (int w = 0; w < 8; ++w) mean += sm.vred[w];
     mean *= (1.0f / 128.0f);
-    if (q == 0) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = e ? v1 : v0;
-        uint8_t gc = float_to_e4m3_rn(expf(v - mean));
-        if (gc == 0) gc = 0x01;
-        sm.rec[c0 + e] = gc;
-        sm.inv_g[c0 + e] = __frcp_rn(e4m3_to_float(gc));
-      }
-    }
+    uint8_t gc = float_to_e4m3_rn(expf(v_c - mean));
+    if (gc == 0) gc = 0x01;
+    rec[tid] = gc;
+    sm.inv_g[tid] = __frcp_rn(e4m3_to_float(gc));
   }
   __syncthreads();
 
-  // ---- 5. per-token zero-point and step (copy 1)
-  float ig[16][2];
-#pragma unroll
-  for (int nb = 0; nb < 16; ++nb) {
-    const float2 v = *reinterpret_cast<const float2*>(sm.inv_g + 8 * nb + 2 * j);
-    ig[nb][0] = v.x; ig[nb][1] = v.y;
-  }
-  float ba, bb, ia, ib;  // zero-point and 1/step of t0, t1
+  // ---- 5. per-token zero-point and step
+  float2 ig[4];
   {
-    float mn0 = INFINITY, mx0 = -INFINITY, mn1 = INFINITY, mx1 = -INFINITY;
+    const float4 g0 = *reinterpret_cast<const float4*>(sm.inv_g + 8 * cb);
+    const float4 g1 = *reinterpret_cast<const float4*>(sm.inv_g + 8 * cb + 4);
+    ig[0] = make_float2(g0.x, g0.y); ig[1] = make_float2(g0.z, g0.w);
+    ig[2] = make_float2(g1.x, g1.y); ig[3] = make_float2(g1.z, g1.w);
+  }
 #pragma unroll
-    for (int nb = 0; nb < 16; ++nb) {
-      const float y0 = __fmul_rn(r1[nb][0], ig[nb][0]), y1 = __fmul_rn(r1[nb][1], ig[nb][1]);
-      const float y2 = __fmul_rn(r1[nb][2], ig[nb][0]), y3 = __fmul_rn(r1[nb][3], ig[nb][1]);
-      mn0 = fminf(mn0, fminf(y0, y1)); mx0 = fmaxf(mx0, fmaxf(y0, y1));
-      mn1 = fminf(mn1, fminf(y2, y3)); mx1 = fmaxf(mx1, fmaxf(y2, y3));
-    }
-    mn0 = quad_min(mn0); mx0 = quad_max(mx0); mn1 = quad_min(mn1); mx1 = quad_max(mx1);
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float mn = e ? mn1 : mn0, mx = e ? mx1 : mx0;
-      __half bh = (mn <= -65504.f) ? __float2half_rn(-65504.f) : __float2half_rd(mn);
-      const float bv = __half2float(bh);
-      const float step = __fdiv_ru(__fsub_ru(mx, bv), (float)L);
-      uint8_t ac = float_to_e4m3_ru(step);
-      if (ac == 0) ac = 0x01;
-      const float inv_a = __frcp_rn(e4m3_to_float(ac));
-      if (e) { bb = bv; ib = inv_a; } else { ba = bv; ia = inv_a; }
-      if (j == 0) {
-        const int t = e ? t1 : t0;
-        sm.rec[128 + t] = ac;
-        *reinterpret_cast<__half*>(sm.rec + 256 + 2 * t) = bh;
-        sm.inv_a[t] = inv_a;
-        sm.bval[t] = bv;
+    for (int pp = 0; pp < 4; ++pp) r[i][pp] = fmul2(r[i][pp], ig[pp]);   // r now holds Y = R / g
+  {
+    float mn[8][2], mx[8][2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float a = fminf(r[i][0].x, r[i][0].y), bmax = fmaxf(r[i][0].x, r[i][0].y);
+#pragma unroll
+      for (int pp = 1; pp < 4; ++pp) {
+        a = fminf(a, fminf(r[i][pp].x, r[i][pp].y));
+        bmax = fmaxf(bmax, fmaxf(r[i][pp].x, r[i][pp].y));
       }
+      mn[i][0] = a; mn[i][1] = a;
+      mx[i][0] = bmax; mx[i][1] = bmax;
+    }
+    float ymin, ymax, dummy;
+    halve16(mn, lane, MinOp(), ymin, dummy);
+    halve16(mx, lane, MaxOp(), ymax, dummy);
+    const __half bh = (ymin <= -65504.f) ? __float2half_rn(-65504.f) : __float2half_rd(ymin);
+    const float bv = __half2float(bh);
+    const float step = __fdiv_ru(__fsub_ru(ymax, bv), (float)L);
+    uint8_t ac = float_to_e4m3_ru(step);
+    if (ac == 0) ac = 0x01;
+    const float inv_a = __frcp_rn(e4m3_to_float(ac));
+    if ((lane & 1) == 0) {
+      const int tk = tok0 + ((lane & 15) >> 1);
+      rec[128 + tk] = ac;
+      *reinterpret_cast<__half*>(rec + 256 + 2 * tk) = bh;
+      tokv[tk] = make_float2(bv, inv_a);
     }
   }
+  __syncthreads();
 
   // ---- 6. codes and packing
   if constexpr (!IS_V) {
-    // token-major nibbles: byte 4nb+j of token t holds channels 8nb+2j, +1
 #pragma unroll
-    for (int nb = 0; nb < 16; ++nb) {
+    for (int i = 0; i < 8; ++i) {
+      const float2 ta = tokv[tok0 + i];
+      uint32_t word = 0;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float bv = e ? bb : ba, inv_a = e ? ib : ia;
-        int k0 = __float2int_rn(__fmul_rn(__fsub_rn(__fmul_rn(r1[nb][2 * e], ig[nb][0]), bv), inv_a));
-        int k1 = __float2int_rn(__fmul_rn(__fsub_rn(__fmul_rn(r1[nb][2 * e + 1], ig[nb][1]), bv), inv_a));
+      for (int pp = 0; pp < 4; ++pp) {
+        int k0 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].x, ta.x), ta.y));
+        int k1 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].y, ta.x), ta.y));
         k0 = min(max(k0, 0), L);
         k1 = min(max(k1, 0), L);
-        const int t = e ? t1 : t0;
-        sm.rec[512 + t * 68 + 4 * nb + j] = static_cast<unsigned char>(k0 | (k1 << 4));
+        word |= (uint32_t)(k0 | (k1 << 4)) << (8 * pp);
       }
-    }
-    __syncthreads();
-    // header (32 x 16 B) then 128 rows x 4 x 16 B of codes
-    for (int i = tid; i < 32 + T * 4; i += 256) {
-      uint4 v;
-      if (i < 32) {
-        v = *reinterpret_cast<const uint4*>(sm.rec + 16 * i);
-      } else {
-        const int k = i - 32, t = k >> 2, part = k & 3;
-        const uint32_t* s = reinterpret_cast<const uint32_t*>(sm.rec + 512 + t * 68 + 16 * part);
-        v = make_uint4(s[0], s[1], s[2], s[3]);
-      }
-      *reinterpret_cast<uint4*>(dst + 16 * i) = v;
+      *reinterpret_cast<uint32_t*>(rec + 512 + (tok0 + i) * 64 + 4 * cb) = word;
     }
   } else {
-    __syncthreads();  // inv_a / bval of every token are needed by copy 2
-    const float ga = sm.inv_g[c0], gb = sm.inv_g[c0 + 1];
-    uint64_t pa = 0, pb = 0;  // channel-major 2-bit codes of tokens 32q .. 32q+31
+    uint32_t half[8];  // channel 8cb + k: 2-bit codes of tokens tok0 .. tok0+7
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int t = 32 * q + i;
-      const float bv = sm.bval[t], inv_a = sm.inv_a[t];
-      int ka = __float2int_rn(__fmul_rn(__fsub_rn(__fmul_rn(r2[i].x, ga), bv), inv_a));
-      int kb = __float2int_rn(__fmul_rn(__fsub_rn(__fmul_rn(r2[i].y, gb), bv), inv_a));
-      ka = min(max(ka, 0), L);
-      kb = min(max(kb, 0), L);
-      pa |= static_cast<uint64_t>(ka) << (2 * i);
-      pb |= static_cast<uint64_t>(kb) << (2 * i);
+    for (int k = 0; k < 8; ++k) half[k] = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 ta = tokv[tok0 + i];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        int k0 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].x, ta.x), ta.y));
+        int k1 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].y, ta.x), ta.y));
+        k0 = min(max(k0, 0), L);
+        k1 = min(max(k1, 0), L);
+        half[2 * pp] |= (uint32_t)k0 << (2 * i);
+        half[2 * pp + 1] |= (uint32_t)k1 << (2 * i);
+      }
     }
-    *reinterpret_cast<uint64_t*>(sm.rec + 512 + c0 * 32 + 8 * q) = pa;
-    *reinterpret_cast<uint64_t*>(sm.rec + 512 + (c0 + 1) * 32 + 8 * q) = pb;
-    __syncthreads();
-    for (int i = tid; i < V_REC / 16; i += 256)
-      *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(sm.rec + 16 * i);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<uint16_t*>(rec + 512 + (8 * cb + k) * 32 + (tok0 >> 2)) = (uint16_t)half[k];
   }
+  __syncthreads();
+  const int bytes = IS_V ? V_REC : K_REC;
+  for (int i = tid; i < bytes / 16; i += 256)
+    *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(rec + 16 * i);
 }
 
 // ------------------------------------------------------------------ kernels
 
 // One CTA per (tile, head, K|V): blockIdx.x = (tile * H + head) * 2 + kv.
 template <typename E>
-__global__ void __launch_bounds__(256, 1) quantize_tiles_kernel(QuantizeParams prm) {
+__global__ void __launch_bounds__(256, 2) quantize_tiles_kernel(QuantizeParams prm) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   QSmem& sm = *reinterpret_cast<QSmem*>(smem_raw);
   const int job = blockIdx.x;
@@ -320,7 +404,7 @@ __global__ void __launch_bounds__(256, 1) quantize_tiles_kernel(QuantizeParams p
 // One CTA per (sequence, head, K|V): copy the new token into the open tile;
 // the CTA whose token fills the tile quantises it into the sequence's block.
 template <typename E>
-__global__ void __launch_bounds__(256, 1) append_tokens_kernel(AppendParams prm) {
+__global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   QSmem& sm = *reinterpret_cast<QSmem*>(smem_raw);
   const int b = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
