@@ -62,12 +62,24 @@ __device__ __forceinline__ float to_f(E x) {
 // tile's V record is in use and vice versa -- the rotated queries, and the
 // cross-warp merge area (aliases the record buffers at the end).
 constexpr int DEC_WARPS = 8;
-constexpr int QK_ILP = 2;   // independent MMA chains interleaved in QK
-constexpr int PV_ILP = 4;   // and in PV
+#ifndef KVARN_QK_ILP
+#define KVARN_QK_ILP 1
+#endif
+#ifndef KVARN_PV_ILP
+#define KVARN_PV_ILP 4
+#endif
+constexpr int QK_ILP = KVARN_QK_ILP;  // independent MMA chains interleaved in QK
+constexpr int PV_ILP = KVARN_PV_ILP;  // and in PV
+constexpr int QR_STRIDE = D + 4;  // padded query rows: lanes g, g+1 hit different banks
+// The K codes (128 tokens x 64 B) arrive by a 2-D TMA load of 64 rows of
+// 128 B (two tokens per row) with the 128-byte swizzle: 16-byte chunk c of
+// row r lands at chunk c ^ (r & 7).  Tokens t and t + 8, which lanes g and
+// g + 1 read together, then sit in different banks.
 struct DecSmem {
-  alignas(128) unsigned char kbuf[DEC_WARPS][K_REC];
+  alignas(1024) unsigned char kcodes[DEC_WARPS][T * D / 2];
+  alignas(128) unsigned char khdr[DEC_WARPS][512];
   alignas(128) unsigned char vbuf[DEC_WARPS][V_REC];
-  alignas(16) float qr[8][D];
+  alignas(16) float qr[8][QR_STRIDE];
   uint64_t kbar[DEC_WARPS];
   uint64_t vbar[DEC_WARPS];
 };
@@ -76,7 +88,14 @@ struct DecMerge {
   float l[DEC_WARPS][8];
   float acc[DEC_WARPS][8][D];
 };
-static_assert(sizeof(DecMerge) <= sizeof(DecSmem::kbuf) + sizeof(DecSmem::vbuf), "merge area must fit");
+static_assert(sizeof(DecMerge) <= sizeof(DecSmem::kcodes), "merge area must fit");
+
+// Byte offset, inside a warp's swizzled K-code buffer, of the 16 bytes of
+// token t's codes for channels 32j .. 32j+31.
+__device__ __forceinline__ int kcode_off(int t, int j) {
+  const int row = t >> 1, chunk = ((t & 1) << 2) | j;
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
 
 template <typename E>
 __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
@@ -93,7 +112,7 @@ __device__ __forceinline__ uint32_t field(uint32_t x, uint32_t mask) { return un
 // grid (n_chunks + 1, H_kv, B) x 256 threads; chunk n_chunks handles the
 // raw open tile.  Warp w of a chunk takes its tiles first + w, first + w + 8.
 template <typename E>
-__global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_constant__ CUtensorMap kmap, DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
@@ -110,7 +129,8 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   const int first = chunk * p.chunk_tiles;
   const int n_tiles = min(p.chunk_tiles, n_closed - first);
   if (n_tiles <= 0) return;
-  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw);
+  const uint32_t sbase = smem_u32(smem_raw);
+  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw + (((sbase + 1023u) & ~1023u) - sbase));
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
   const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
@@ -126,9 +146,15 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     if (blk >= 0 && blk < p.num_blocks) {
-      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC + (is_v ? K_REC : 0);
-      mbar_expect_tx(bar, is_v ? V_REC : K_REC);
-      bulk_g2s(is_v ? sm.vbuf[warp] : sm.kbuf[warp], src, is_v ? V_REC : K_REC, bar);
+      const int64_t rec = blk * p.block_bytes + (int64_t)h * HEAD_REC;
+      if (is_v) {
+        mbar_expect_tx(bar, V_REC);
+        bulk_g2s(sm.vbuf[warp], p.pool + rec + K_REC, V_REC, bar);
+      } else {
+        mbar_expect_tx(bar, K_REC);
+        bulk_g2s(sm.khdr[warp], p.pool + rec, 512, bar);
+        tma_load_2d(sm.kcodes[warp], &kmap, 0, (int)((rec + 512) >> 7), bar);
+      }
     } else {
       set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
@@ -175,7 +201,8 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   for (int k = 0; k < my_n; ++k) {
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     const bool valid = blk >= 0 && blk < p.num_blocks;
-    const unsigned char* krec = sm.kbuf[warp];
+    const unsigned char* krec = sm.khdr[warp];
+    const unsigned char* kcodes = sm.kcodes[warp];
     const unsigned char* vrec = sm.vbuf[warp];
     // a wait that gives up ends this warp's loop (after waiting, bounded, for
     // the V copy it still has in flight); the error word is already set
@@ -239,7 +266,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
         for (int i = 0; i < QK_ILP; ++i) {
           const int nb = n4 + i;
           const int off = nb < 8 ? nb : nb + 8;
-          const uint4 v4 = *reinterpret_cast<const uint4*>(krec + 512 + (32 * (g >> 1) + off + 8 * (g & 1)) * 64 + 16 * j);
+          const uint4 v4 = *reinterpret_cast<const uint4*>(kcodes + kcode_off(32 * (g >> 1) + off + 8 * (g & 1), j));
           kw[i][0] = v4.x; kw[i][1] = v4.y; kw[i][2] = v4.z; kw[i][3] = v4.w;
         }
         float c[QK_ILP][4];
@@ -349,7 +376,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
 
   // ---- merge the warps and write this CTA's partial
   __syncthreads();
-  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.kbuf);
+  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.kcodes);
   if (j == 0) { mg.m[warp][g] = m_run; mg.l[warp][g] = l_run; }
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) {
@@ -691,12 +718,32 @@ size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int c
   return (size_t)batch * num_kv_heads * (n_chunks + 1) * G * PART * sizeof(float);
 }
 
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
+
+// 2-D view of the packed pool as rows of 128 bytes, read in boxes of 64 rows
+// (one tile's K codes) with the 128-byte swizzle.
+static cudaError_t pool_tensor_map(const DecodeParams& p, CUtensorMap* m) {
+  auto encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_bytes / 128};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<unsigned char*>(p.pool), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <typename E>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
-  const size_t smem = sizeof(DecSmem);
-  cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  CUtensorMap kmap;
+  cudaError_t e = pool_tensor_map(p, &kmap);
   if (e != cudaSuccess) return e;
-  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
+  const size_t smem = sizeof(DecSmem) + 1024;
+  e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(kmap, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
