@@ -31,6 +31,7 @@
 namespace kvarn {
 
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr uint32_t MAGIC = 0x64006400u;  // 1024.0 in both fp16 halves
 constexpr int kMaxDevices = 64;
 constexpr int PART = D + 4;  // floats per split-K partial: m, l, 2 pad, acc[128] (16-byte aligned)
 constexpr int PACC = 4;      // offset of acc[] in a partial
@@ -40,6 +41,9 @@ __device__ __forceinline__ float* part_ptr(const DecodeParams& p, int b, int h, 
   return p.ws + ((((int64_t)b * p.num_kv_heads + h) * (p.n_chunks + 1) + chunk) * p.G + g) * PART;
 }
 
+
+__device__ __forceinline__ __half2 u2h2(uint32_t x) { return *reinterpret_cast<__half2*>(&x); }
+__device__ __forceinline__ uint32_t h22u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
 // Two fp16 codes (1024 + c) in a half2 -> exact (c0, c1).
 __device__ __forceinline__ uint32_t unbias(uint32_t x) {
@@ -106,7 +110,6 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
 // shift; a field at bit offset 4 (nibble) or 2k (crumb) comes out multiplied
 // by 16 or 4^k, and the matching entries of the other operand are divided by
 // the same power of two, which is exact.
-constexpr uint32_t MAGIC = 0x64006400u;
 __device__ __forceinline__ uint32_t field(uint32_t x, uint32_t mask) { return unbias((x & mask) | MAGIC); }
 
 // grid (n_chunks + 1, H_kv, B) x 256 threads; chunk n_chunks handles the
@@ -402,6 +405,378 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
     if (c == 0) { o[0] = M; o[1] = Lsum; }
     o[PACC + c] = A;
   }
+}
+
+// ------------------------------------------------------------------ tcgen05 decode
+// One CTA of 128 threads per (sequence, KV head, chunk of tiles).  Per tile:
+//   QK: thread t unpacks token t's 4-bit K codes (scaled by its step a_t,
+//       exactly, in the same fp16 FMA that removes the 1024 bias) into tensor
+//       memory lane t; the MMA  D1[t][n] = sum_c A_K[t][c] B_q[c][n]  with
+//       B_q = qg hi | lo (n = 0..7 | 8..15) from shared memory gives a_t <qg, code_t>.
+//       A second MMA against an all-ones A gives S = sum_c qg_c for every row.
+//   PV: thread c unpacks channel c's 2-bit V codes into lane c; the MMA
+//       D2[c][n] = sum_t A_V[c][t] B_P[t][n]  with B_P = p_t aV_t (hi | lo) gives
+//       the packed part of the output; an all-ones MMA over B_Pb = p_t bV_t
+//       gives sum_t p_t bV_t.
+// The only CTA-wide reduction per tile is the running maximum of the scores.
+constexpr int TCW = 4;                    // warps per CTA
+constexpr uint32_t TC_COLS = 128;         // tensor-memory columns per CTA
+constexpr uint32_t TC_A = 0;              // A operand: 64 columns = 128 fp16
+constexpr uint32_t TC_D1 = 64, TC_DS = 80, TC_D2 = 96, TC_DPB = 112;
+constexpr uint32_t TC_IDESC = umma_idesc_f16(128, 16, 1);
+
+struct TcSmem {
+  alignas(128) unsigned char rec[2][HEAD_REC];  // two stages of one (tile, head) K+V record pair
+  alignas(128) unsigned char bq[4096];          // B: qg hi|lo, MN-major, K = 128 channels (permuted), N = 16
+  alignas(128) unsigned char bp[4096];          // B: p aV 64 / 4^(t & 3) hi|lo, K = 128 tokens (permuted)
+  alignas(128) unsigned char bpb[4096];         // B: p bV hi|lo, K = 128 tokens
+  alignas(128) unsigned char ones[128];         // one 8 x 8 core matrix of fp16 1.0
+  alignas(16) float qr[8][D];                   // rotated, scaled queries
+  alignas(16) float red[TCW][8];
+  uint64_t rbar[2];
+  uint64_t mbar;
+  uint32_t tmem;
+};
+
+// Byte offset of element (n, k) in an MN-major B operand (K x 16, no
+// swizzle): 8 x 8 core matrices, K-groups 256 B apart, N-groups 128 B apart.
+__device__ __forceinline__ int bmn_off(int k) { return (k >> 3) * 256 + (k & 7) * 16; }
+
+template <typename E>
+__device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
+
+template <typename E>
+__global__ void __launch_bounds__(TCW * 32) decode_tc_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) unsigned char smem_tc[];
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int len = p.seq_lens[b];
+  if (len < 0 || len > T * p.max_blocks) {
+    if (tid == 0 && chunk == 0 && h == 0) set_error(p.err, KVARN_DEV_ERR_TOKEN_RANGE);
+    return;
+  }
+  if (chunk == p.n_chunks) {
+    tail_chunk<E>(p, b, h, len, smem_tc);
+    return;
+  }
+  const int first = chunk * p.chunk_tiles;
+  const int n_tiles = min(p.chunk_tiles, len / T - first);
+  if (n_tiles <= 0) return;
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_tc);
+  const int G = p.G;
+  const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
+
+  if (warp == 0) tmem_alloc(&sm.tmem, TC_COLS);
+  if (tid == 0) {
+    mbar_init(&sm.rbar[0], 1);
+    mbar_init(&sm.rbar[1], 1);
+    mbar_init(&sm.mbar, 1);
+    fence_mbar_init();
+  }
+  if (tid < 64) reinterpret_cast<uint32_t*>(sm.ones)[tid & 31] = 0x3C003C00u;
+  auto issue = [&](int k) {  // thread 0: copy tile k's K+V record pair
+    const int s = k & 1;
+    const int32_t blk = tab[first + k];
+    if (blk >= 0 && blk < p.num_blocks) {
+      mbar_expect_tx(&sm.rbar[s], HEAD_REC);
+      bulk_g2s(sm.rec[s], p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC, HEAD_REC, &sm.rbar[s]);
+    } else {
+      set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.rbar[s])) : "memory");
+    }
+  };
+  __syncthreads();
+  if (tid == 0) {
+    issue(0);
+    if (n_tiles > 1) issue(1);
+  }
+
+  // rotated queries: warp w rotates queries w and w + 4 (128-point butterfly,
+  // 4 channels per lane); then one power-of-two scale for the CTA puts
+  // max |q'| in [0.5, 1) so the fp16 hi/lo parts of q' g stay normal
+  {
+    const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
+    float amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int qq = warp + 4 * r;
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (qq < G) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = to_f(qb[qq * D + 4 * lane + e]);
+      }
+      float u = x[0], v = x[1];
+      x[0] = u + v; x[1] = u - v;
+      u = x[2]; v = x[3];
+      x[2] = u + v; x[3] = u - v;
+      u = x[0]; v = x[2];
+      x[0] = u + v; x[2] = u - v;
+      u = x[1]; v = x[3];
+      x[1] = u + v; x[3] = u - v;
+#pragma unroll
+      for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+          x[e] = upper ? (o - x[e]) : (x[e] + o);
+        }
+      }
+      const float f = p.scale * LOG2E * INV_SQRT_D;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) { x[e] *= f; amax = fmaxf(amax, fabsf(x[e])); }
+      *reinterpret_cast<float4*>(&sm.qr[qq][4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) sm.red[warp][0] = amax;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);  // this thread's lane
+  float qscale, qscale_inv;
+  {
+    float amax = fmaxf(fmaxf(sm.red[0][0], sm.red[1][0]), fmaxf(sm.red[2][0], sm.red[3][0]));
+    int ex = 0;
+    if (amax > 0.f) frexpf(amax, &ex);
+    qscale = ldexpf(1.f, -ex);
+    qscale_inv = ldexpf(1.f, ex);
+  }
+  // this thread's channel c = tid: its queries (scaled) and its place in B_q
+  float qc[8];
+#pragma unroll
+  for (int qq = 0; qq < 8; ++qq) qc[qq] = sm.qr[qq][tid] * qscale;
+  const int c = tid, t = tid;
+  const int kq = 8 * (c >> 3) + 2 * (c & 3) + ((c & 7) >> 2);   // K slot of channel c
+  const int kp = 16 * (t >> 4) + 2 * (t & 7) + ((t >> 3) & 1);  // K slot of token t
+  const float pscale = 64.f / (float)(1 << (2 * (t & 3)));       // undo the 4^k field scale of token t
+  const uint64_t ones_desc = umma_desc(smem_u32(sm.ones), 0, 0);
+  const uint32_t bq_s = smem_u32(sm.bq), bp_s = smem_u32(sm.bp), bpb_s = smem_u32(sm.bpb);
+
+  float m_run[8], l_run[8], acc[8];
+#pragma unroll
+  for (int qq = 0; qq < 8; ++qq) { m_run[qq] = -INFINITY; l_run[qq] = 0.f; acc[qq] = 0.f; }
+  uint32_t mphase = 0;
+  bool dead = false;
+
+  for (int k = 0; k < n_tiles && !dead; ++k) {
+    const int s = k & 1;
+    const int32_t blk = tab[first + k];
+    const bool valid = blk >= 0 && blk < p.num_blocks;
+    if (__syncthreads_or(!mbar_wait_bounded(&sm.rbar[s], (k >> 1) & 1, p.err))) { dead = true; break; }
+    const unsigned char* krec = sm.rec[s];
+    const unsigned char* vrec = krec + K_REC;
+
+    // ---- QK operands: B_q (thread c) and A_K = a_t * codes of token t
+    {
+      const float g = e4m3_to_float(krec[c]);
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int qq = 0; qq < 8; qq += 2) {
+        uint16_t h0, l0, h1, l1;
+        split_hl<__half>(qc[qq] * g, h0, l0);
+        split_hl<__half>(qc[qq + 1] * g, h1, l1);
+        hw[qq >> 1] = pack2(h0, h1);
+        lw[qq >> 1] = pack2(l0, l1);
+      }
+      *reinterpret_cast<uint4*>(sm.bq + bmn_off(kq)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sm.bq + bmn_off(kq) + 128) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    {
+      const float a = e4m3_to_float(krec[128 + t]);
+      const __half2 A1 = __float2half2_rn(a), A16 = __float2half2_rn(a * 0.0625f);
+      const __half2 N1 = __float2half2_rn(-1024.f * a), N16 = __float2half2_rn(-64.f * a);
+      uint32_t f[64];
+      const unsigned char* row = krec + 512 + t * 64;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(row + 16 * q4);
+        const uint32_t wv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int w = 4 * q4 + e;
+          const uint32_t x = wv[e], x8 = x >> 8;
+          __half2 y0 = __hfma2(u2h2((x & 0x000F000Fu) | MAGIC), A1, N1);
+          __half2 y1 = __hfma2(u2h2((x & 0x00F000F0u) | MAGIC), A16, N16);
+          __half2 y2 = __hfma2(u2h2((x8 & 0x000F000Fu) | MAGIC), A1, N1);
+          __half2 y3 = __hfma2(u2h2((x8 & 0x00F000F0u) | MAGIC), A16, N16);
+          f[4 * w] = h22u(y0); f[4 * w + 1] = h22u(y1); f[4 * w + 2] = h22u(y2); f[4 * w + 3] = h22u(y3);
+        }
+      }
+      tmem_st64(lane_base + TC_A, f);
+    }
+    tmem_wait_st();
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t bd = umma_desc(bq_s + 512 * kk, 256, 128);
+        umma_ts(tmem + TC_D1, tmem + TC_A + 8 * kk, bd, TC_IDESC, kk);
+        umma_ss(tmem + TC_DS, ones_desc, bd, TC_IDESC, kk);
+      }
+      umma_commit(&sm.mbar);
+    }
+    // ---- meanwhile: V codes of channel c (fields scaled by 4^(s & 3))
+    uint32_t fv[64];
+    {
+      const unsigned char* row = vrec + 512 + c * 32;
+      const __half2 M = u2h2(MAGIC);
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const uint4 v4 = *reinterpret_cast<const uint4*>(row + 16 * q2);
+        const uint32_t wv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ww = 4 * q2 + e;
+          const uint32_t x = wv[e], x8 = x >> 8;
+#pragma unroll
+          for (int sh = 0; sh < 4; ++sh) {
+            const uint32_t m = 0x00030003u << (2 * sh);
+            fv[8 * ww + sh] = h22u(__hsub2(u2h2((x & m) | MAGIC), M));
+            fv[8 * ww + 4 + sh] = h22u(__hsub2(u2h2((x8 & m) | MAGIC), M));
+          }
+        }
+      }
+    }
+    const float bK = __half2float(*reinterpret_cast<const __half*>(krec + 256 + 2 * t));
+    const float aV = e4m3_to_float(vrec[128 + t]);
+    const float bV = __half2float(*reinterpret_cast<const __half*>(vrec + 256 + 2 * t));
+    const float gV = e4m3_to_float(vrec[c]);
+    if (__syncthreads_or(!mbar_wait_bounded(&sm.mbar, mphase, p.err))) { dead = true; break; }
+    mphase ^= 1;
+    tc_fence_after();
+    // ---- scores of token t
+    float sc[8];
+    {
+      float d1[16], ds[16];
+      tmem_ld16(lane_base + TC_D1, d1);
+      tmem_ld16(lane_base + TC_DS, ds);
+      tmem_wait_ld();
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) sc[qq] = qscale_inv * fmaf(bK, ds[qq] + ds[8 + qq], d1[qq] + d1[8 + qq]);
+    }
+    tmem_st64(lane_base + TC_A, fv);  // QK is done with the A columns
+    // ---- tile maximum of each query: reduce-scatter in the warp, then across warps
+    {
+      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+      float r4[4], r2[2], r1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float keep = b4 ? sc[i + 4] : sc[i], send = b4 ? sc[i] : sc[i + 4];
+        r4[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float keep = b3 ? r4[i + 2] : r4[i], send = b3 ? r4[i] : r4[i + 2];
+        r2[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+      }
+      {
+        const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
+        r1 = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+      }
+      r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, 2));
+      r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, 1));
+      if ((lane & 3) == 0) sm.red[warp][(b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0)] = r1;
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    float corr[8];
+    {
+      const float4 r00 = *reinterpret_cast<const float4*>(&sm.red[0][0]), r01 = *reinterpret_cast<const float4*>(&sm.red[0][4]);
+      const float4 r10 = *reinterpret_cast<const float4*>(&sm.red[1][0]), r11 = *reinterpret_cast<const float4*>(&sm.red[1][4]);
+      const float4 r20 = *reinterpret_cast<const float4*>(&sm.red[2][0]), r21 = *reinterpret_cast<const float4*>(&sm.red[2][4]);
+      const float4 r30 = *reinterpret_cast<const float4*>(&sm.red[3][0]), r31 = *reinterpret_cast<const float4*>(&sm.red[3][4]);
+      const float tm[8] = {fmaxf(fmaxf(r00.x, r10.x), fmaxf(r20.x, r30.x)), fmaxf(fmaxf(r00.y, r10.y), fmaxf(r20.y, r30.y)),
+                           fmaxf(fmaxf(r00.z, r10.z), fmaxf(r20.z, r30.z)), fmaxf(fmaxf(r00.w, r10.w), fmaxf(r20.w, r30.w)),
+                           fmaxf(fmaxf(r01.x, r11.x), fmaxf(r21.x, r31.x)), fmaxf(fmaxf(r01.y, r11.y), fmaxf(r21.y, r31.y)),
+                           fmaxf(fmaxf(r01.z, r11.z), fmaxf(r21.z, r31.z)), fmaxf(fmaxf(r01.w, r11.w), fmaxf(r21.w, r31.w))};
+      uint32_t pw[4], plw[4], bw[4], blw[4];
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq) {
+        const float mn = valid ? fmaxf(m_run[qq], tm[qq]) : m_run[qq];
+        corr[qq] = (m_run[qq] == -INFINITY) ? 0.f : exp2f(m_run[qq] - mn);
+        m_run[qq] = mn;
+        const float pr = valid ? exp2f(sc[qq] - mn) : 0.f;
+        l_run[qq] = fmaf(l_run[qq], corr[qq], pr);
+        uint16_t ph, pl, bh, bl;
+        split_hl<__half>(pr * aV * pscale, ph, pl);
+        split_hl<__half>(pr * bV, bh, bl);
+        if (qq & 1) {
+          pw[qq >> 1] |= (uint32_t)ph << 16; plw[qq >> 1] |= (uint32_t)pl << 16;
+          bw[qq >> 1] |= (uint32_t)bh << 16; blw[qq >> 1] |= (uint32_t)bl << 16;
+        } else {
+          pw[qq >> 1] = ph; plw[qq >> 1] = pl; bw[qq >> 1] = bh; blw[qq >> 1] = bl;
+        }
+      }
+      *reinterpret_cast<uint4*>(sm.bp + bmn_off(kp)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+      *reinterpret_cast<uint4*>(sm.bp + bmn_off(kp) + 128) = make_uint4(plw[0], plw[1], plw[2], plw[3]);
+      *reinterpret_cast<uint4*>(sm.bpb + bmn_off(t)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+      *reinterpret_cast<uint4*>(sm.bpb + bmn_off(t) + 128) = make_uint4(blw[0], blw[1], blw[2], blw[3]);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        umma_ts(tmem + TC_D2, tmem + TC_A + 8 * kk, umma_desc(bp_s + 512 * kk, 256, 128), TC_IDESC, kk);
+        umma_ss(tmem + TC_DPB, ones_desc, umma_desc(bpb_s + 512 * kk, 256, 128), TC_IDESC, kk);
+      }
+      umma_commit(&sm.mbar);
+      if (k + 2 < n_tiles) {  // every thread is done reading this stage
+        fence_proxy_async();
+        issue(k + 2);
+      }
+    }
+    if (__syncthreads_or(!mbar_wait_bounded(&sm.mbar, mphase, p.err))) { dead = true; break; }
+    mphase ^= 1;
+    tc_fence_after();
+    {
+      float d2[16], dpb[16];
+      tmem_ld16(lane_base + TC_D2, d2);
+      tmem_ld16(lane_base + TC_DPB, dpb);
+      tmem_wait_ld();
+#pragma unroll
+      for (int qq = 0; qq < 8; ++qq)
+        acc[qq] = fmaf(acc[qq], corr[qq], valid ? gV * fmaf(d2[qq] + d2[8 + qq], 1.f / 64.f, dpb[qq] + dpb[8 + qq]) : 0.f);
+    }
+    tc_fence_before();
+  }
+
+  // ---- partial of this CTA: m (uniform), l = sum over threads, acc per channel
+#pragma unroll
+  for (int qq = 0; qq < 8; ++qq) {
+    float v = l_run[qq];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    l_run[qq] = v;
+  }
+  __syncthreads();
+  if (lane == 0) {
+#pragma unroll
+    for (int qq = 0; qq < 8; ++qq) sm.red[warp][qq] = l_run[qq];
+  }
+  __syncthreads();
+  for (int qq = 0; qq < G; ++qq) {
+    float* o = part_ptr(p, b, h, chunk, qq);
+    if (tid == 0) {
+      o[0] = dead ? -INFINITY : m_run[qq];
+      o[1] = dead ? 0.f : sm.red[0][qq] + sm.red[1][qq] + sm.red[2][qq] + sm.red[3][qq];
+    }
+    o[PACC + c] = dead ? 0.f : acc[qq];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, TC_COLS);
 }
 
 // Raw open tile of (b, h): len % 128 tokens in 16-bit, unrotated query.
@@ -751,9 +1126,27 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
   return cudaGetLastError();
 }
 
+template <typename E>
+static cudaError_t launch_decode_tc_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
+  const size_t smem = sizeof(TcSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), TCW * 32, smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int warps = batch * p.num_q_heads;
+  combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, 1, batch, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
+#ifdef KVARN_DECODE_TC
+  return dtype == KVARN_DTYPE_BF16 ? launch_decode_tc_t<__nv_bfloat16>(p, batch, out, s)
+                                   : launch_decode_tc_t<__half>(p, batch, out, s);
+#else
   return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, batch, out, s)
                                    : launch_decode_t<__half>(p, batch, out, s);
+#endif
 }
 
 // ---- fixed-scratch variant of the packed decode (no allocation anywhere)

@@ -36,14 +36,16 @@ struct QSmem {
 constexpr int X_ROW = 272;                 // staging row stride: 256 B + 16 B pad
 constexpr int OFF_PART = 9216;             // float2 [8 warps][128]: column (mean, M2) over 16 tokens
 constexpr int OFF_TOK = 17408;             // float2 [128]: (zero-point, 1/step) per token
-static_assert(OFF_TOK + 128 * 8 <= 65536 && T * 272 <= 65536, "staging reuse overflows");
+constexpr int OFF_ROW = 18432;             // per half-warp row-step slot: 8 x 36 partials, 8 shifts, 8 factors
+constexpr int ROW_SLOT = 304;              // floats per slot
+static_assert(OFF_ROW + 16 * ROW_SLOT * 4 <= 65536 && T * 272 <= 65536, "staging reuse overflows");
 
 // New log factor ln(std) from a population variance and mean over 128
 // values; keeps `old` when the std is at most 1e-6 of the rms (a constant or
 // all-zero row/column).
 __device__ __forceinline__ float log_std_or_keep(float var, float mean, float old) {
   var = fmaxf(var, 0.0f);
-  return (var > 1e-12f * (var + mean * mean)) ? logf(sqrtf(var)) : old;
+  return (var > 1e-12f * (var + mean * mean)) ? 0.5f * __logf(var) : old;
 }
 
 // Sum of 16 values (8 tokens x 2 quantities, index 2i + m) across the 16 lanes
@@ -232,19 +234,33 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
 #pragma unroll
       for (int w = 0; w < 8; ++w) M2 = fmaf(16.f * (mw[w] - mean), mw[w] - mean, M2);
       v_c = log_std_or_keep(M2 * (1.0f / 128.0f), mean, v_c);
-      sm.beta[tid] = expf(-v_c);
+      sm.beta[tid] = __expf(-v_c);
     }
     __syncthreads();
-    // row step
+    // row step: the half-warp holding tokens tok0 .. tok0+7 reduces through
+    // its own shared-memory slot: row shifts, 16 partial pairs per lane, then
+    // each token's owner lanes (cb = 2i, 2i+1) sum the 16 partials of token i
     {
+      float* rs = reinterpret_cast<float*>(sm.xs + OFF_ROW) + (2 * warp + tbl) * ROW_SLOT;
       const float4 b0 = *reinterpret_cast<const float4*>(sm.beta + 8 * cb);
       const float4 b1 = *reinterpret_cast<const float4*>(sm.beta + 8 * cb + 4);
       const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
                             make_float2(b1.z, b1.w)};
-      float Kt[8], t[8][2];
+      if (cb == 0) {  // channel 0 of each token: the shift of its row
+        *reinterpret_cast<float4*>(rs + 288) =
+            make_float4(bp[0].x * r[0][0].x, bp[0].x * r[1][0].x, bp[0].x * r[2][0].x, bp[0].x * r[3][0].x);
+        *reinterpret_cast<float4*>(rs + 292) =
+            make_float4(bp[0].x * r[4][0].x, bp[0].x * r[5][0].x, bp[0].x * r[6][0].x, bp[0].x * r[7][0].x);
+      }
+      __syncwarp();
+      float Kt[8];
+      {
+        const float4 k0 = *reinterpret_cast<const float4*>(rs + 288), k1 = *reinterpret_cast<const float4*>(rs + 292);
+        Kt[0] = k0.x; Kt[1] = k0.y; Kt[2] = k0.z; Kt[3] = k0.w; Kt[4] = k1.x; Kt[5] = k1.y; Kt[6] = k1.z; Kt[7] = k1.w;
+      }
+      float t2[16];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        Kt[i] = __shfl_sync(0xffffffffu, bp[0].x * r[i][0].x, lane & 16);  // channel 0 of token i
         const float2 nK = make_float2(-Kt[i], -Kt[i]);
         float2 s1 = make_float2(0.f, 0.f), s2 = s1;
 #pragma unroll
@@ -253,16 +269,29 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
           s1 = fadd2(s1, d);
           s2 = ffma2(d, d, s2);
         }
-        t[i][0] = s1.x + s1.y;
-        t[i][1] = s2.x + s2.y;
+        t2[2 * i] = s1.x + s1.y;
+        t2[2 * i + 1] = s2.x + s2.y;
       }
-      float S1, S2;
-      halve16(t, lane, AddOp(), S1, S2);
-      const float md = S1 * (1.0f / 128.0f);
-      u_t = log_std_or_keep(S2 * (1.0f / 128.0f) - md * md, pick8(Kt, lane) + md, u_t);
-      const float a_mine = expf(-u_t);
+      // partial pairs: slot layout [token i (stride 36)][lane cb] float2: the owner's 16 reads are
+      // contiguous and the 8 owners hit different banks
 #pragma unroll
-      for (int i = 0; i < 8; ++i) al[i] = __shfl_sync(0xffffffffu, a_mine, (lane & 16) | (2 * i));
+      for (int i = 0; i < 8; ++i) *reinterpret_cast<float2*>(rs + 36 * i + 2 * cb) = make_float2(t2[2 * i], t2[2 * i + 1]);
+      __syncwarp();
+      const int ti = cb >> 1;
+      float2 S = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 v = *reinterpret_cast<const float4*>(rs + 36 * ti + 4 * q4);
+        S = fadd2(S, make_float2(v.x + v.z, v.y + v.w));
+      }
+      const float md = S.x * (1.0f / 128.0f);
+      u_t = log_std_or_keep(S.y * (1.0f / 128.0f) - md * md, rs[288 + ti] + md, u_t);
+      __syncwarp();
+      if ((cb & 1) == 0) rs[296 + ti] = __expf(-u_t);
+      __syncwarp();
+      const float4 a0 = *reinterpret_cast<const float4*>(rs + 296), a1 = *reinterpret_cast<const float4*>(rs + 300);
+      al[0] = a0.x; al[1] = a0.y; al[2] = a0.z; al[3] = a0.w; al[4] = a1.x; al[5] = a1.y; al[6] = a1.z; al[7] = a1.w;
+      __syncwarp();
     }
   }
 
@@ -330,19 +359,23 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
   }
   __syncthreads();
 
-  // ---- 6. codes and packing
+  // ---- 6. codes and packing: code = rne((Y - b) * (1/a)) clamped to [0, L];
+  // the rounding adds 1.5 * 2^23, which leaves the integer in the low bits
+  constexpr float RNE_MAGIC = 12582912.0f;
+  const float2 MAG2 = make_float2(RNE_MAGIC, RNE_MAGIC);
   if constexpr (!IS_V) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float2 ta = tokv[tok0 + i];
+      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
       uint32_t word = 0;
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
-        int k0 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].x, ta.x), ta.y));
-        int k1 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].y, ta.x), ta.y));
-        k0 = min(max(k0, 0), L);
-        k1 = min(max(k1, 0), L);
-        word |= (uint32_t)(k0 | (k1 << 4)) << (8 * pp);
+        float2 q2 = fmul2(fadd2(r[i][pp], nb), ia);
+        q2.x = fminf(fmaxf(q2.x, 0.f), (float)L);
+        q2.y = fminf(fmaxf(q2.y, 0.f), (float)L);
+        q2 = fadd2(q2, MAG2);
+        word |= ((__float_as_uint(q2.x) & 0xFu) | ((__float_as_uint(q2.y) & 0xFu) << 4)) << (8 * pp);
       }
       *reinterpret_cast<uint32_t*>(rec + 512 + (tok0 + i) * 64 + 4 * cb) = word;
     }
@@ -353,14 +386,15 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float2 ta = tokv[tok0 + i];
+      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
-        int k0 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].x, ta.x), ta.y));
-        int k1 = __float2int_rn(__fmul_rn(__fsub_rn(r[i][pp].y, ta.x), ta.y));
-        k0 = min(max(k0, 0), L);
-        k1 = min(max(k1, 0), L);
-        half[2 * pp] |= (uint32_t)k0 << (2 * i);
-        half[2 * pp + 1] |= (uint32_t)k1 << (2 * i);
+        float2 q2 = fmul2(fadd2(r[i][pp], nb), ia);
+        q2.x = fminf(fmaxf(q2.x, 0.f), (float)L);
+        q2.y = fminf(fmaxf(q2.y, 0.f), (float)L);
+        q2 = fadd2(q2, MAG2);
+        half[2 * pp] |= (__float_as_uint(q2.x) & 3u) << (2 * i);
+        half[2 * pp + 1] |= (__float_as_uint(q2.y) & 3u) << (2 * i);
       }
     }
 #pragma unroll
