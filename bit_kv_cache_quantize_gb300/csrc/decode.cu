@@ -51,8 +51,6 @@ __device__ __forceinline__ uint32_t unbias(uint32_t x) {
   h = __hsub2(h, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
   return *reinterpret_cast<uint32_t*>(&h);
 }
-__device__ __forceinline__ uint32_t nib2(uint32_t w, int s) { return unbias(((w >> (4 * s)) & 0x000F000Fu) | 0x64006400u); }
-__device__ __forceinline__ uint32_t crumb2(uint32_t w, int s) { return unbias(((w >> (2 * s)) & 0x00030003u) | 0x64006400u); }
 
 
 template <typename E>
@@ -63,27 +61,19 @@ __device__ __forceinline__ float to_f(E x) {
 
 // Shared memory of one packed-decode CTA: per warp one K-record buffer and
 // one V-record buffer -- the next tile's K record streams in while this
-// tile's V record is in use and vice versa -- the rotated queries, and the
-// cross-warp merge area (aliases the record buffers at the end).
+// tile's V record is in use and vice versa -- the query operand fragments,
+// and the cross-warp merge area (aliases the K buffers at the end).
 constexpr int DEC_WARPS = 8;
-#ifndef KVARN_QK_ILP
-#define KVARN_QK_ILP 1
-#endif
 #ifndef KVARN_PV_ILP
 #define KVARN_PV_ILP 4
 #endif
-constexpr int QK_ILP = KVARN_QK_ILP;  // independent MMA chains interleaved in QK
-constexpr int PV_ILP = KVARN_PV_ILP;  // and in PV
-constexpr int QR_STRIDE = D + 4;  // padded query rows: lanes g, g+1 hit different banks
-// The K codes (128 tokens x 64 B) arrive by a 2-D TMA load of 64 rows of
-// 128 B (two tokens per row) with the 128-byte swizzle: 16-byte chunk c of
-// row r lands at chunk c ^ (r & 7).  Tokens t and t + 8, which lanes g and
-// g + 1 read together, then sit in different banks.
+constexpr int PV_ILP = KVARN_PV_ILP;  // independent MMA chains interleaved in PV
 struct DecSmem {
-  alignas(1024) unsigned char kcodes[DEC_WARPS][T * D / 2];
-  alignas(128) unsigned char khdr[DEC_WARPS][512];
-  alignas(128) unsigned char vbuf[DEC_WARPS][V_REC];
-  alignas(16) float qr[8][QR_STRIDE];
+  alignas(128) unsigned char krec[DEC_WARPS][K_REC];
+  alignas(128) unsigned char vrec[DEC_WARPS][V_REC];
+  alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order (hi, lo, hi/16, lo/16)
+  alignas(16) float qr[8][D];   // rotated, scaled queries (set-up only)
+  float qsi[8];                 // per query: inverse of its power-of-two operand scale
   uint64_t kbar[DEC_WARPS];
   uint64_t vbar[DEC_WARPS];
 };
@@ -92,30 +82,49 @@ struct DecMerge {
   float l[DEC_WARPS][8];
   float acc[DEC_WARPS][8][D];
 };
-static_assert(sizeof(DecMerge) <= sizeof(DecSmem::kcodes), "merge area must fit");
-
-// Byte offset, inside a warp's swizzled K-code buffer, of the 16 bytes of
-// token t's codes for channels 32j .. 32j+31.
-__device__ __forceinline__ int kcode_off(int t, int j) {
-  const int row = t >> 1, chunk = ((t & 1) << 2) | j;
-  return row * 128 + ((chunk ^ (row & 7)) << 4);
-}
+static_assert(sizeof(DecMerge) <= sizeof(DecSmem::krec), "merge area must fit");
+static_assert(K_REC % 128 == 0 && V_REC % 128 == 0, "record buffers stay 128-byte aligned");
 
 template <typename E>
 __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
 
 // Unpacking codes to exact fp16 operands.  A code field ORed into the
 // mantissa of 1024.0 (0x6400) and 1024 subtracted gives the code exactly.
-// Fields at mantissa bits 0-3 / 4-7 of each 16-bit half are taken without a
-// shift; a field at bit offset 4 (nibble) or 2k (crumb) comes out multiplied
-// by 16 or 4^k, and the matching entries of the other operand are divided by
-// the same power of two, which is exact.
-__device__ __forceinline__ uint32_t field(uint32_t x, uint32_t mask) { return unbias((x & mask) | MAGIC); }
+// A field at mantissa bits 4s .. 4s+3 (nibble) or 2s .. 2s+1 (crumb) comes
+// out multiplied by 16^s or 4^s; the matching entries of the other operand
+// carry the inverse power of two, which is exact.
+// (x & mask) | MAGIC as one explicit three-input logic op (the C expression
+// compiles to two), then the exact fp16 subtraction of 1024.
+__device__ __forceinline__ uint32_t field(uint32_t x, uint32_t mask) {
+  uint32_t y;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(y) : "r"(x), "r"(mask), "r"(MAGIC));
+  return unbias(y);
+}
+
+// Two E4M3 bytes (low byte first) -> fp16 pair, exact.
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xFFFFu), __NV_E4M3);
+  return __half2(h);
+}
 
 // grid (n_chunks + 1, H_kv, B) x 256 threads; chunk n_chunks handles the
 // raw open tile.  Warp w of a chunk takes its tiles first + w, first + w + 8.
+//
+// Per tile and warp, with lane = 4 g + j:
+//   QK (m16n8k16, M = 8 queries hi | lo, N = 8 tokens, K = 16 channels):
+//     A = qg = q * gK as an exact fp16 high part plus low part, formed per
+//     tile from the fp16 query pairs with HMUL2/HFMA2; B = 4-bit codes of
+//     token 32 (g >> 1) + 2 nb + (g & 1), channels 32 j .. 32 j + 31 in the
+//     order (c0, c0+4 | c0+1, c0+5), c0 = 32 j + 8 (kb >> 1) + 2 (kb & 1).
+//     Lane (g, j) receives the scores of query g for tokens 32 j + 2 nb, +1.
+//   S = sum_c qg_c from eight more MMAs against constant B = 1 | 16.
+//   PV: A = p aV 64 / 4^(nb & 3) (hi | lo) of the same tokens, which k-block
+//     kb = nb >> 1 takes as k = 2j, 2j+1 (nb even) and 2j+8, 2j+9 (nb odd);
+//     B = 2-bit codes of channel 8 nbp + g, whose 32-bit words keep even
+//     tokens in the low half and odd tokens in the high half, so each B
+//     register is one masked field of one word.
 template <typename E>
-__global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_constant__ CUtensorMap kmap, DecodeParams p) {
+__global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
@@ -133,7 +142,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
   const int n_tiles = min(p.chunk_tiles, n_closed - first);
   if (n_tiles <= 0) return;
   const uint32_t sbase = smem_u32(smem_raw);
-  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw + (((sbase + 1023u) & ~1023u) - sbase));
+  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
   const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
@@ -149,15 +158,10 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     if (blk >= 0 && blk < p.num_blocks) {
-      const int64_t rec = blk * p.block_bytes + (int64_t)h * HEAD_REC;
-      if (is_v) {
-        mbar_expect_tx(bar, V_REC);
-        bulk_g2s(sm.vbuf[warp], p.pool + rec + K_REC, V_REC, bar);
-      } else {
-        mbar_expect_tx(bar, K_REC);
-        bulk_g2s(sm.khdr[warp], p.pool + rec, 512, bar);
-        tma_load_2d(sm.kcodes[warp], &kmap, 0, (int)((rec + 512) >> 7), bar);
-      }
+      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC + (is_v ? K_REC : 0);
+      const uint32_t bytes = is_v ? V_REC : K_REC;
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(is_v ? sm.vrec[warp] : sm.krec[warp], src, bytes, bar);
     } else {
       set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
@@ -166,7 +170,9 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
   if (lane == 0 && my_n > 0) { issue(0, false); issue(0, true); }
 
   // rotated, scaled queries: warp w < G rotates query w with a 128-point
-  // butterfly over 4 channels per lane; qr = scale * log2(e) * (q H)
+  // butterfly over 4 channels per lane; qr = qs * scale * log2(e) * (q H),
+  // qs a power of two putting max |qr| in [64, 128), so |qr gK| <= 128 * 448
+  // stays inside fp16
   {
     const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
     float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -192,107 +198,103 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
       }
     }
     const float f = p.scale * LOG2E * INV_SQRT_D;
-    *reinterpret_cast<float4*>(&sm.qr[warp][4 * lane]) = make_float4(x[0] * f, x[1] * f, x[2] * f, x[3] * f);
+    float amax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[e] *= f;
+      amax = fmaxf(amax, fabsf(x[e]));
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    int ex = 0;
+    if (amax > 0.f) frexpf(amax, &ex);
+    const float qs = ldexpf(1.f, 7 - ex);
+    *reinterpret_cast<float4*>(&sm.qr[warp][4 * lane]) = make_float4(x[0] * qs, x[1] * qs, x[2] * qs, x[3] * qs);
+    if (lane == 0) sm.qsi[warp] = ldexpf(1.f, ex - 7);
+  }
+  __syncthreads();
+  {  // thread (kb = warp, lane) forms the fp16 high/low query pairs of its A-fragment slot
+    const int kb = warp, c0 = 32 * j + 8 * (kb >> 1) + 2 * (kb & 1);
+    const float* q = sm.qr[g];
+    const float v0 = q[c0], v1 = q[c0 + 4], v2 = q[c0 + 1] * (1.f / 16.f), v3 = q[c0 + 5] * (1.f / 16.f);
+    const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
+    const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+    const __half2 l01 = __floats2half2_rn(v0 - f01.x, v1 - f01.y), l23 = __floats2half2_rn(v2 - f23.x, v3 - f23.y);
+    sm.qf[kb][lane] = make_uint4(h22u(h01), h22u(l01), h22u(h23), h22u(l23));
   }
   __syncthreads();
 
+  const float qsi = sm.qsi[g];
   float m_run = -INFINITY, l_run = 0.f;
-  float acc[16][2];
+  float2 acc[16];  // query g, channels 8 nbp + 2j, +1
 #pragma unroll
-  for (int nb = 0; nb < 16; ++nb) acc[nb][0] = acc[nb][1] = 0.f;
+  for (int nb = 0; nb < 16; ++nb) acc[nb] = make_float2(0.f, 0.f);
 
   for (int k = 0; k < my_n; ++k) {
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     const bool valid = blk >= 0 && blk < p.num_blocks;
-    const unsigned char* krec = sm.khdr[warp];
-    const unsigned char* kcodes = sm.kcodes[warp];
-    const unsigned char* vrec = sm.vbuf[warp];
+    const unsigned char* kr = sm.krec[warp];
+    const unsigned char* vr = sm.vrec[warp];
     // a wait that gives up ends this warp's loop (after waiting, bounded, for
     // the V copy it still has in flight); the error word is already set
     if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.kbar[warp], k & 1, p.err))) {
       mbar_wait_bounded(&sm.vbar[warp], k & 1, p.err);
       break;
     }
-    const bool kok = valid;
 
-    // ---- query fold: qg = q' * gK over channels 32j..32j+31, scaled so max |qg| is in [512, 1024)
-    uint32_t afr[8][4];
-    float S = 0.f, qs_inv = 1.f;
-    float sc[16][2];
+    float2 sc[16];  // scores x qs of query g, tokens 32j + 2nb, +1
     float tmax = -INFINITY;
-    if (kok) {
-      float qg[32];
-      const uint4 g0 = *reinterpret_cast<const uint4*>(krec + 32 * j);
-      const uint4 g1 = *reinterpret_cast<const uint4*>(krec + 32 * j + 16);
-      const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      const float* q = &sm.qr[g][32 * j];
-      float amax = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const float4 qv = *reinterpret_cast<const float4*>(q + 4 * w);
-        const float2 lo = e4m3x2_to_float2((uint16_t)(gw[w] & 0xFFFF));
-        const float2 hi = e4m3x2_to_float2((uint16_t)(gw[w] >> 16));
-        qg[4 * w] = qv.x * lo.x; qg[4 * w + 1] = qv.y * lo.y;
-        qg[4 * w + 2] = qv.z * hi.x; qg[4 * w + 3] = qv.w * hi.y;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) { S += qg[4 * w + e]; amax = fmaxf(amax, fabsf(qg[4 * w + e])); }
-      }
-      S = quad_sum(S);
-      amax = quad_max(amax);
-      int ex = 0;
-      if (amax > 0.f) frexpf(amax, &ex);
-      const float qs = ldexpf(1.f, 10 - ex), qs16 = ldexpf(1.f, 6 - ex);
-      qs_inv = ldexpf(1.f, ex - 10);
-#pragma unroll
-      for (int kb = 0; kb < 8; ++kb) {
-        const int c0 = 8 * (kb >> 1) + 2 * (kb & 1);  // b0: channels c0, c0+4 (x1); b1: c0+1, c0+5 (x16)
-        uint16_t h00, l00, h01, l01, h10, l10, h11, l11;
-        split_hl<__half>(qg[c0] * qs, h00, l00);
-        split_hl<__half>(qg[c0 + 4] * qs, h01, l01);
-        split_hl<__half>(qg[c0 + 1] * qs16, h10, l10);
-        split_hl<__half>(qg[c0 + 5] * qs16, h11, l11);
-        afr[kb][0] = pack2(h00, h01);
-        afr[kb][1] = pack2(l00, l01);
-        afr[kb][2] = pack2(h10, h11);
-        afr[kb][3] = pack2(l10, l11);
-      }
-
-      // ---- QK: n-block nb holds tokens off(nb), off(nb) + 8 of this lane's 32
-      // (off = nb for nb < 8, nb + 8 otherwise); B rows = K codes of token
-      // 32 (g >> 1) + off(nb) + 8 (g & 1), channels 32j .. 32j+31
-      const __half* bz = reinterpret_cast<const __half*>(krec + 256) + 32 * j;
-      const unsigned char* az = krec + 128 + 32 * j;
-#pragma unroll
-      for (int n4 = 0; n4 < 16; n4 += QK_ILP) {
-        uint32_t kw[QK_ILP][4];
-#pragma unroll
-        for (int i = 0; i < QK_ILP; ++i) {
-          const int nb = n4 + i;
-          const int off = nb < 8 ? nb : nb + 8;
-          const uint4 v4 = *reinterpret_cast<const uint4*>(kcodes + kcode_off(32 * (g >> 1) + off + 8 * (g & 1), j));
-          kw[i][0] = v4.x; kw[i][1] = v4.y; kw[i][2] = v4.z; kw[i][3] = v4.w;
-        }
-        float c[QK_ILP][4];
-#pragma unroll
-        for (int i = 0; i < QK_ILP; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+    if (valid) {
+      // ---- A operand: qg = q gK, high part RN(q_hi gK), low part q_lo gK + (q_hi gK - high)
+      uint32_t afr[8][4];
+      {
+        const uint4 gA = *reinterpret_cast<const uint4*>(kr + 32 * j);
+        const uint4 gB = *reinterpret_cast<const uint4*>(kr + 32 * j + 16);
+        const uint32_t gw[8] = {gA.x, gA.y, gA.z, gA.w, gB.x, gB.y, gB.z, gB.w};  // channels 32j + 4i .. +3
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
-#pragma unroll
-          for (int i = 0; i < QK_ILP; ++i) {
-            const uint32_t x = (kb & 1) ? (kw[i][kb >> 1] >> 8) : kw[i][kb >> 1];
-            mma_f16(c[i], afr[kb], field(x, 0x000F000Fu), field(x, 0x00F000F0u));
-          }
+          const uint32_t lo = gw[2 * (kb >> 1)], hi = gw[2 * (kb >> 1) + 1];
+          const uint32_t pr = __byte_perm(lo, hi, (kb & 1) ? 0x7362 : 0x5140);
+          const __half2 g01 = e4m3x2_to_half2(pr), g23 = e4m3x2_to_half2(pr >> 16);
+          const uint4 qv = sm.qf[kb][lane];
+          const __half2 h01 = __hmul2_rn(u2h2(qv.x), g01);
+          const __half2 l01 = __hfma2(u2h2(qv.y), g01, __hfma2(u2h2(qv.x), g01, __hneg2(h01)));
+          const __half2 h23 = __hmul2_rn(u2h2(qv.z), g23);
+          const __half2 l23 = __hfma2(u2h2(qv.w), g23, __hfma2(u2h2(qv.z), g23, __hneg2(h23)));
+          afr[kb][0] = h22u(h01); afr[kb][1] = h22u(l01);
+          afr[kb][2] = h22u(h23); afr[kb][3] = h22u(l23);
         }
+      }
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < QK_ILP; ++i) {
-          const int nb = n4 + i;
-          const int off = nb < 8 ? nb : nb + 8;
-          const float2 dot = fmul2(fadd2(make_float2(c[i][0], c[i][1]), make_float2(c[i][2], c[i][3])),
-                                   make_float2(qs_inv, qs_inv));
-          const float2 a = make_float2(e4m3_to_float(az[off]), e4m3_to_float(az[off + 8]));
-          const float2 bb = make_float2(__half2float(bz[off]), __half2float(bz[off + 8]));
-          const float2 s2 = ffma2(a, dot, fmul2(bb, make_float2(S, S)));
-          sc[nb][0] = s2.x; sc[nb][1] = s2.y;
+      for (int kb = 0; kb < 8; ++kb) mma_f16(sacc, afr[kb], 0x3C003C00u, 0x4C004C00u);  // B = 1 | 16
+      const float S = sacc[0] + sacc[2];
+      const float2 S2 = make_float2(S, S);
+
+      // ---- QK: scores x qs = aK <qg, code> + bK S
+      const unsigned char* kc = kr + 512 + (32 * (g >> 1) + (g & 1)) * 64 + 16 * j;
+      const unsigned char* ka = kr + 128 + 32 * j;
+      const unsigned char* kz = kr + 256 + 64 * j;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint2 a8 = *reinterpret_cast<const uint2*>(ka + 8 * q4);
+        const uint4 b8 = *reinterpret_cast<const uint4*>(kz + 16 * q4);
+        const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nb = 4 * q4 + i;
+          const uint4 v4 = *reinterpret_cast<const uint4*>(kc + nb * 128);
+          const uint32_t kw[4] = {v4.x, v4.y, v4.z, v4.w};
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) {
+            const uint32_t x = (kb & 1) ? (kw[kb >> 1] >> 8) : kw[kb >> 1];
+            mma_f16(c, afr[kb], field(x, 0x000F000Fu), field(x, 0x00F000F0u));
+          }
+          const float2 a2 = __half22float2(e4m3x2_to_half2(((i & 2) ? a8.y : a8.x) >> (16 * (i & 1))));
+          const float2 b2 = __half22float2(u2h2(bw[i]));
+          const float2 s2 = ffma2(a2, fadd2(make_float2(c[0], c[1]), make_float2(c[2], c[3])), fmul2(b2, S2));
+          sc[nb] = s2;
           tmax = fmaxf(tmax, fmaxf(s2.x, s2.y));
         }
       }
@@ -306,67 +308,69 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
       if (k + 1 < my_n) mbar_wait_bounded(&sm.kbar[warp], (k + 1) & 1, p.err);
       break;
     }
-    const bool vok = kok;
-    if (vok) {
+    if (valid) {
       // ---- online softmax (log2 domain)
       tmax = quad_max(tmax);
-      const float m_new = fmaxf(m_run, tmax);
-      const float corr = exp2f(m_run - m_new);
+      const float m_new = fmaxf(m_run, tmax * qsi);
+      const float corr = ex2_ftz(m_run - m_new);
+      const float nm = -m_new;
       m_run = m_new;
-      // ---- P = p * aV * 64 / slot scale, hi rows 0-7 / lo rows 8-15
+      // ---- P = p aV 64 / 4^(nb & 3), hi rows 0-7 / lo rows 8-15
       uint32_t pfr[8][4];
       float2 psum = make_float2(0.f, 0.f), pb = psum;
-      const __half* bz = reinterpret_cast<const __half*>(vrec + 256) + 32 * j;
-      const unsigned char* az = vrec + 128 + 32 * j;
+      const unsigned char* va = vr + 128 + 32 * j;
+      const unsigned char* vz = vr + 256 + 64 * j;
 #pragma unroll
-      for (int nb = 0; nb < 16; ++nb) {
-        const int off = nb < 8 ? nb : nb + 8;
-        const float2 pr = make_float2(exp2f(sc[nb][0] - m_new), exp2f(sc[nb][1] - m_new));
-        psum = fadd2(psum, pr);
-        pb = ffma2(pr, make_float2(__half2float(bz[off]), __half2float(bz[off + 8])), pb);
-        const float f = 64.f / (float)(1 << (2 * (nb & 3)));  // undo the slot scale of this pair
-        const float2 pa = fmul2(pr, make_float2(e4m3_to_float(az[off]) * f, e4m3_to_float(az[off + 8]) * f));
-        const __half2 hi = __floats2half2_rn(pa.x, pa.y);
-        const float2 hf = __half22float2(hi);
-        const __half2 lo = __floats2half2_rn(pa.x - hf.x, pa.y - hf.y);
-        const uint32_t hb = *reinterpret_cast<const uint32_t*>(&hi), lb = *reinterpret_cast<const uint32_t*>(&lo);
-        pfr[nb >> 1][(nb & 1) ? 2 : 0] = hb;
-        pfr[nb >> 1][(nb & 1) ? 3 : 1] = lb;
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint2 a8 = *reinterpret_cast<const uint2*>(va + 8 * q4);
+        const uint4 b8 = *reinterpret_cast<const uint4*>(vz + 16 * q4);
+        const uint32_t bw[4] = {b8.x, b8.y, b8.z, b8.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int nb = 4 * q4 + i;
+          const float2 pr = make_float2(ex2_ftz(fmaf(sc[nb].x, qsi, nm)), ex2_ftz(fmaf(sc[nb].y, qsi, nm)));
+          psum = fadd2(psum, pr);
+          pb = ffma2(pr, __half22float2(u2h2(bw[i])), pb);
+          const __half2 f2 = __float2half2_rn(64.f / (float)(1 << (2 * (nb & 3))));
+          const __half2 av = __hmul2(e4m3x2_to_half2(((i & 2) ? a8.y : a8.x) >> (16 * (i & 1))), f2);  // exact
+          const float2 pa = fmul2(pr, __half22float2(av));
+          const __half2 hi = __float22half2_rn(pa);
+          const float2 lo = fadd2(pa, fmul2(__half22float2(hi), make_float2(-1.f, -1.f)));
+          pfr[nb >> 1][(nb & 1) ? 2 : 0] = h22u(hi);
+          pfr[nb >> 1][(nb & 1) ? 3 : 1] = h22u(__float22half2_rn(lo));
+        }
       }
-      const float ps = quad_sum(psum.x + psum.y);
+      l_run = l_run * corr + quad_sum(psum.x + psum.y);
       const float pbs = quad_sum(pb.x + pb.y);
-      l_run = l_run * corr + ps;
-      // ---- PV: B = 2-bit V codes of channel 8nb + g, tokens 32j .. 32j+31
+      const float2 corr2 = make_float2(corr, corr), pbs2 = make_float2(pbs, pbs);
+      const float2 inv64 = make_float2(1.f / 64.f, 1.f / 64.f);
+      // ---- PV: B = 2-bit codes of channel 8 nbp + g, tokens 32j .. 32j+31
+      const unsigned char* vc = vr + 512 + g * 32 + 8 * j;
 #pragma unroll
       for (int n4 = 0; n4 < 16; n4 += PV_ILP) {
-        uint32_t vw[PV_ILP][2];
+        uint2 vw[PV_ILP];
 #pragma unroll
-        for (int i = 0; i < PV_ILP; ++i) {
-          const uint2 v2 = *reinterpret_cast<const uint2*>(vrec + 512 + (8 * (n4 + i) + g) * 32 + 8 * j);
-          vw[i][0] = v2.x; vw[i][1] = v2.y;
-        }
+        for (int i = 0; i < PV_ILP; ++i) vw[i] = *reinterpret_cast<const uint2*>(vc + (n4 + i) * 256);
         float c[PV_ILP][4];
 #pragma unroll
         for (int i = 0; i < PV_ILP; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
-          // pairs 2kb, 2kb+1 = crumb fields s, s+1 (s = 2kb & 7) of word kb >> 2
-          const int sh = (2 * kb) & 7;
+          // tokens 32j + 4kb + {0,1} | {2,3}: fields at bits 4 (kb & 1) | +2 of word kb >> 2, shifted by 8 when kb & 2
+          const uint32_t m0 = 0x00030003u << (4 * (kb & 1));
 #pragma unroll
           for (int i = 0; i < PV_ILP; ++i) {
-            const uint32_t x = (sh & 4) ? (vw[i][kb >> 2] >> 8) : vw[i][kb >> 2];
-            const uint32_t m0 = 0x00030003u << (2 * (sh & 3));
+            const uint32_t w = (kb & 4) ? vw[i].y : vw[i].x;
+            const uint32_t x = (kb & 2) ? (w >> 8) : w;
             mma_f16(c[i], pfr[kb], field(x, m0), field(x, m0 << 2));
           }
         }
 #pragma unroll
         for (int i = 0; i < PV_ILP; ++i) {
-          const int nb = n4 + i;
-          const float2 gv = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vrec + 8 * nb + 2 * j));
-          const float o0 = fmaf(c[i][0] + c[i][2], 1.f / 64.f, pbs);
-          const float o1 = fmaf(c[i][1] + c[i][3], 1.f / 64.f, pbs);
-          acc[nb][0] = fmaf(acc[nb][0], corr, gv.x * o0);
-          acc[nb][1] = fmaf(acc[nb][1], corr, gv.y * o1);
+          const int nbp = n4 + i;
+          const float2 gv = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vr + 8 * nbp + 2 * j));
+          const float2 o = ffma2(fadd2(make_float2(c[i][0], c[i][1]), make_float2(c[i][2], c[i][3])), inv64, pbs2);
+          acc[nbp] = ffma2(acc[nbp], corr2, fmul2(gv, o));
         }
       }
     }
@@ -379,13 +383,10 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
 
   // ---- merge the warps and write this CTA's partial
   __syncthreads();
-  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.kcodes);
+  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.krec);
   if (j == 0) { mg.m[warp][g] = m_run; mg.l[warp][g] = l_run; }
 #pragma unroll
-  for (int nb = 0; nb < 16; ++nb) {
-    mg.acc[warp][g][8 * nb + 2 * j] = acc[nb][0];
-    mg.acc[warp][g][8 * nb + 2 * j + 1] = acc[nb][1];
-  }
+  for (int nb = 0; nb < 16; ++nb) *reinterpret_cast<float2*>(&mg.acc[warp][g][8 * nb + 2 * j]) = acc[nb];
   __syncthreads();
   for (int i = tid; i < G * D; i += 256) {
     const int gg = i / D, c = i % D;
@@ -405,378 +406,6 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(const __grid_cons
     if (c == 0) { o[0] = M; o[1] = Lsum; }
     o[PACC + c] = A;
   }
-}
-
-// ------------------------------------------------------------------ tcgen05 decode
-// One CTA of 128 threads per (sequence, KV head, chunk of tiles).  Per tile:
-//   QK: thread t unpacks token t's 4-bit K codes (scaled by its step a_t,
-//       exactly, in the same fp16 FMA that removes the 1024 bias) into tensor
-//       memory lane t; the MMA  D1[t][n] = sum_c A_K[t][c] B_q[c][n]  with
-//       B_q = qg hi | lo (n = 0..7 | 8..15) from shared memory gives a_t <qg, code_t>.
-//       A second MMA against an all-ones A gives S = sum_c qg_c for every row.
-//   PV: thread c unpacks channel c's 2-bit V codes into lane c; the MMA
-//       D2[c][n] = sum_t A_V[c][t] B_P[t][n]  with B_P = p_t aV_t (hi | lo) gives
-//       the packed part of the output; an all-ones MMA over B_Pb = p_t bV_t
-//       gives sum_t p_t bV_t.
-// The only CTA-wide reduction per tile is the running maximum of the scores.
-constexpr int TCW = 4;                    // warps per CTA
-constexpr uint32_t TC_COLS = 128;         // tensor-memory columns per CTA
-constexpr uint32_t TC_A = 0;              // A operand: 64 columns = 128 fp16
-constexpr uint32_t TC_D1 = 64, TC_DS = 80, TC_D2 = 96, TC_DPB = 112;
-constexpr uint32_t TC_IDESC = umma_idesc_f16(128, 16, 1);
-
-struct TcSmem {
-  alignas(128) unsigned char rec[2][HEAD_REC];  // two stages of one (tile, head) K+V record pair
-  alignas(128) unsigned char bq[4096];          // B: qg hi|lo, MN-major, K = 128 channels (permuted), N = 16
-  alignas(128) unsigned char bp[4096];          // B: p aV 64 / 4^(t & 3) hi|lo, K = 128 tokens (permuted)
-  alignas(128) unsigned char bpb[4096];         // B: p bV hi|lo, K = 128 tokens
-  alignas(128) unsigned char ones[128];         // one 8 x 8 core matrix of fp16 1.0
-  alignas(16) float qr[8][D];                   // rotated, scaled queries
-  alignas(16) float red[TCW][8];
-  uint64_t rbar[2];
-  uint64_t mbar;
-  uint32_t tmem;
-};
-
-// Byte offset of element (n, k) in an MN-major B operand (K x 16, no
-// swizzle): 8 x 8 core matrices, K-groups 256 B apart, N-groups 128 B apart.
-__device__ __forceinline__ int bmn_off(int k) { return (k >> 3) * 256 + (k & 7) * 16; }
-
-template <typename E>
-__device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
-
-template <typename E>
-__global__ void __launch_bounds__(TCW * 32) decode_tc_kernel(DecodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem_tc[];
-  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int len = p.seq_lens[b];
-  if (len < 0 || len > T * p.max_blocks) {
-    if (tid == 0 && chunk == 0 && h == 0) set_error(p.err, KVARN_DEV_ERR_TOKEN_RANGE);
-    return;
-  }
-  if (chunk == p.n_chunks) {
-    tail_chunk<E>(p, b, h, len, smem_tc);
-    return;
-  }
-  const int first = chunk * p.chunk_tiles;
-  const int n_tiles = min(p.chunk_tiles, len / T - first);
-  if (n_tiles <= 0) return;
-  TcSmem& sm = *reinterpret_cast<TcSmem*>(smem_tc);
-  const int G = p.G;
-  const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
-
-  if (warp == 0) tmem_alloc(&sm.tmem, TC_COLS);
-  if (tid == 0) {
-    mbar_init(&sm.rbar[0], 1);
-    mbar_init(&sm.rbar[1], 1);
-    mbar_init(&sm.mbar, 1);
-    fence_mbar_init();
-  }
-  if (tid < 64) reinterpret_cast<uint32_t*>(sm.ones)[tid & 31] = 0x3C003C00u;
-  auto issue = [&](int k) {  // thread 0: copy tile k's K+V record pair
-    const int s = k & 1;
-    const int32_t blk = tab[first + k];
-    if (blk >= 0 && blk < p.num_blocks) {
-      mbar_expect_tx(&sm.rbar[s], HEAD_REC);
-      bulk_g2s(sm.rec[s], p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC, HEAD_REC, &sm.rbar[s]);
-    } else {
-      set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(&sm.rbar[s])) : "memory");
-    }
-  };
-  __syncthreads();
-  if (tid == 0) {
-    issue(0);
-    if (n_tiles > 1) issue(1);
-  }
-
-  // rotated queries: warp w rotates queries w and w + 4 (128-point butterfly,
-  // 4 channels per lane); then one power-of-two scale for the CTA puts
-  // max |q'| in [0.5, 1) so the fp16 hi/lo parts of q' g stay normal
-  {
-    const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
-    float amax = 0.f;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int qq = warp + 4 * r;
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
-      if (qq < G) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] = to_f(qb[qq * D + 4 * lane + e]);
-      }
-      float u = x[0], v = x[1];
-      x[0] = u + v; x[1] = u - v;
-      u = x[2]; v = x[3];
-      x[2] = u + v; x[3] = u - v;
-      u = x[0]; v = x[2];
-      x[0] = u + v; x[2] = u - v;
-      u = x[1]; v = x[3];
-      x[1] = u + v; x[3] = u - v;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
-          x[e] = upper ? (o - x[e]) : (x[e] + o);
-        }
-      }
-      const float f = p.scale * LOG2E * INV_SQRT_D;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) { x[e] *= f; amax = fmaxf(amax, fabsf(x[e])); }
-      *reinterpret_cast<float4*>(&sm.qr[qq][4 * lane]) = make_float4(x[0], x[1], x[2], x[3]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (lane == 0) sm.red[warp][0] = amax;
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = sm.tmem;
-  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);  // this thread's lane
-  float qscale, qscale_inv;
-  {
-    float amax = fmaxf(fmaxf(sm.red[0][0], sm.red[1][0]), fmaxf(sm.red[2][0], sm.red[3][0]));
-    int ex = 0;
-    if (amax > 0.f) frexpf(amax, &ex);
-    qscale = ldexpf(1.f, -ex);
-    qscale_inv = ldexpf(1.f, ex);
-  }
-  // this thread's channel c = tid: its queries (scaled) and its place in B_q
-  float qc[8];
-#pragma unroll
-  for (int qq = 0; qq < 8; ++qq) qc[qq] = sm.qr[qq][tid] * qscale;
-  const int c = tid, t = tid;
-  const int kq = 8 * (c >> 3) + 2 * (c & 3) + ((c & 7) >> 2);   // K slot of channel c
-  const int kp = 16 * (t >> 4) + 2 * (t & 7) + ((t >> 3) & 1);  // K slot of token t
-  const float pscale = 64.f / (float)(1 << (2 * (t & 3)));       // undo the 4^k field scale of token t
-  const uint64_t ones_desc = umma_desc(smem_u32(sm.ones), 0, 0);
-  const uint32_t bq_s = smem_u32(sm.bq), bp_s = smem_u32(sm.bp), bpb_s = smem_u32(sm.bpb);
-
-  float m_run[8], l_run[8], acc[8];
-#pragma unroll
-  for (int qq = 0; qq < 8; ++qq) { m_run[qq] = -INFINITY; l_run[qq] = 0.f; acc[qq] = 0.f; }
-  uint32_t mphase = 0;
-  bool dead = false;
-
-  for (int k = 0; k < n_tiles && !dead; ++k) {
-    const int s = k & 1;
-    const int32_t blk = tab[first + k];
-    const bool valid = blk >= 0 && blk < p.num_blocks;
-    if (__syncthreads_or(!mbar_wait_bounded(&sm.rbar[s], (k >> 1) & 1, p.err))) { dead = true; break; }
-    const unsigned char* krec = sm.rec[s];
-    const unsigned char* vrec = krec + K_REC;
-
-    // ---- QK operands: B_q (thread c) and A_K = a_t * codes of token t
-    {
-      const float g = e4m3_to_float(krec[c]);
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int qq = 0; qq < 8; qq += 2) {
-        uint16_t h0, l0, h1, l1;
-        split_hl<__half>(qc[qq] * g, h0, l0);
-        split_hl<__half>(qc[qq + 1] * g, h1, l1);
-        hw[qq >> 1] = pack2(h0, h1);
-        lw[qq >> 1] = pack2(l0, l1);
-      }
-      *reinterpret_cast<uint4*>(sm.bq + bmn_off(kq)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(sm.bq + bmn_off(kq) + 128) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    {
-      const float a = e4m3_to_float(krec[128 + t]);
-      const __half2 A1 = __float2half2_rn(a), A16 = __float2half2_rn(a * 0.0625f);
-      const __half2 N1 = __float2half2_rn(-1024.f * a), N16 = __float2half2_rn(-64.f * a);
-      uint32_t f[64];
-      const unsigned char* row = krec + 512 + t * 64;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(row + 16 * q4);
-        const uint32_t wv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int w = 4 * q4 + e;
-          const uint32_t x = wv[e], x8 = x >> 8;
-          __half2 y0 = __hfma2(u2h2((x & 0x000F000Fu) | MAGIC), A1, N1);
-          __half2 y1 = __hfma2(u2h2((x & 0x00F000F0u) | MAGIC), A16, N16);
-          __half2 y2 = __hfma2(u2h2((x8 & 0x000F000Fu) | MAGIC), A1, N1);
-          __half2 y3 = __hfma2(u2h2((x8 & 0x00F000F0u) | MAGIC), A16, N16);
-          f[4 * w] = h22u(y0); f[4 * w + 1] = h22u(y1); f[4 * w + 2] = h22u(y2); f[4 * w + 3] = h22u(y3);
-        }
-      }
-      tmem_st64(lane_base + TC_A, f);
-    }
-    tmem_wait_st();
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t bd = umma_desc(bq_s + 512 * kk, 256, 128);
-        umma_ts(tmem + TC_D1, tmem + TC_A + 8 * kk, bd, TC_IDESC, kk);
-        umma_ss(tmem + TC_DS, ones_desc, bd, TC_IDESC, kk);
-      }
-      umma_commit(&sm.mbar);
-    }
-    // ---- meanwhile: V codes of channel c (fields scaled by 4^(s & 3))
-    uint32_t fv[64];
-    {
-      const unsigned char* row = vrec + 512 + c * 32;
-      const __half2 M = u2h2(MAGIC);
-#pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(row + 16 * q2);
-        const uint32_t wv[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int ww = 4 * q2 + e;
-          const uint32_t x = wv[e], x8 = x >> 8;
-#pragma unroll
-          for (int sh = 0; sh < 4; ++sh) {
-            const uint32_t m = 0x00030003u << (2 * sh);
-            fv[8 * ww + sh] = h22u(__hsub2(u2h2((x & m) | MAGIC), M));
-            fv[8 * ww + 4 + sh] = h22u(__hsub2(u2h2((x8 & m) | MAGIC), M));
-          }
-        }
-      }
-    }
-    const float bK = __half2float(*reinterpret_cast<const __half*>(krec + 256 + 2 * t));
-    const float aV = e4m3_to_float(vrec[128 + t]);
-    const float bV = __half2float(*reinterpret_cast<const __half*>(vrec + 256 + 2 * t));
-    const float gV = e4m3_to_float(vrec[c]);
-    if (__syncthreads_or(!mbar_wait_bounded(&sm.mbar, mphase, p.err))) { dead = true; break; }
-    mphase ^= 1;
-    tc_fence_after();
-    // ---- scores of token t
-    float sc[8];
-    {
-      float d1[16], ds[16];
-      tmem_ld16(lane_base + TC_D1, d1);
-      tmem_ld16(lane_base + TC_DS, ds);
-      tmem_wait_ld();
-#pragma unroll
-      for (int qq = 0; qq < 8; ++qq) sc[qq] = qscale_inv * fmaf(bK, ds[qq] + ds[8 + qq], d1[qq] + d1[8 + qq]);
-    }
-    tmem_st64(lane_base + TC_A, fv);  // QK is done with the A columns
-    // ---- tile maximum of each query: reduce-scatter in the warp, then across warps
-    {
-      const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-      float r4[4], r2[2], r1;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float keep = b4 ? sc[i + 4] : sc[i], send = b4 ? sc[i] : sc[i + 4];
-        r4[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float keep = b3 ? r4[i + 2] : r4[i], send = b3 ? r4[i] : r4[i + 2];
-        r2[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-      }
-      {
-        const float keep = b2 ? r2[1] : r2[0], send = b2 ? r2[0] : r2[1];
-        r1 = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-      }
-      r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, 2));
-      r1 = fmaxf(r1, __shfl_xor_sync(0xffffffffu, r1, 1));
-      if ((lane & 3) == 0) sm.red[warp][(b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0)] = r1;
-    }
-    tmem_wait_st();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    float corr[8];
-    {
-      const float4 r00 = *reinterpret_cast<const float4*>(&sm.red[0][0]), r01 = *reinterpret_cast<const float4*>(&sm.red[0][4]);
-      const float4 r10 = *reinterpret_cast<const float4*>(&sm.red[1][0]), r11 = *reinterpret_cast<const float4*>(&sm.red[1][4]);
-      const float4 r20 = *reinterpret_cast<const float4*>(&sm.red[2][0]), r21 = *reinterpret_cast<const float4*>(&sm.red[2][4]);
-      const float4 r30 = *reinterpret_cast<const float4*>(&sm.red[3][0]), r31 = *reinterpret_cast<const float4*>(&sm.red[3][4]);
-      const float tm[8] = {fmaxf(fmaxf(r00.x, r10.x), fmaxf(r20.x, r30.x)), fmaxf(fmaxf(r00.y, r10.y), fmaxf(r20.y, r30.y)),
-                           fmaxf(fmaxf(r00.z, r10.z), fmaxf(r20.z, r30.z)), fmaxf(fmaxf(r00.w, r10.w), fmaxf(r20.w, r30.w)),
-                           fmaxf(fmaxf(r01.x, r11.x), fmaxf(r21.x, r31.x)), fmaxf(fmaxf(r01.y, r11.y), fmaxf(r21.y, r31.y)),
-                           fmaxf(fmaxf(r01.z, r11.z), fmaxf(r21.z, r31.z)), fmaxf(fmaxf(r01.w, r11.w), fmaxf(r21.w, r31.w))};
-      uint32_t pw[4], plw[4], bw[4], blw[4];
-#pragma unroll
-      for (int qq = 0; qq < 8; ++qq) {
-        const float mn = valid ? fmaxf(m_run[qq], tm[qq]) : m_run[qq];
-        corr[qq] = (m_run[qq] == -INFINITY) ? 0.f : exp2f(m_run[qq] - mn);
-        m_run[qq] = mn;
-        const float pr = valid ? exp2f(sc[qq] - mn) : 0.f;
-        l_run[qq] = fmaf(l_run[qq], corr[qq], pr);
-        uint16_t ph, pl, bh, bl;
-        split_hl<__half>(pr * aV * pscale, ph, pl);
-        split_hl<__half>(pr * bV, bh, bl);
-        if (qq & 1) {
-          pw[qq >> 1] |= (uint32_t)ph << 16; plw[qq >> 1] |= (uint32_t)pl << 16;
-          bw[qq >> 1] |= (uint32_t)bh << 16; blw[qq >> 1] |= (uint32_t)bl << 16;
-        } else {
-          pw[qq >> 1] = ph; plw[qq >> 1] = pl; bw[qq >> 1] = bh; blw[qq >> 1] = bl;
-        }
-      }
-      *reinterpret_cast<uint4*>(sm.bp + bmn_off(kp)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-      *reinterpret_cast<uint4*>(sm.bp + bmn_off(kp) + 128) = make_uint4(plw[0], plw[1], plw[2], plw[3]);
-      *reinterpret_cast<uint4*>(sm.bpb + bmn_off(t)) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-      *reinterpret_cast<uint4*>(sm.bpb + bmn_off(t) + 128) = make_uint4(blw[0], blw[1], blw[2], blw[3]);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        umma_ts(tmem + TC_D2, tmem + TC_A + 8 * kk, umma_desc(bp_s + 512 * kk, 256, 128), TC_IDESC, kk);
-        umma_ss(tmem + TC_DPB, ones_desc, umma_desc(bpb_s + 512 * kk, 256, 128), TC_IDESC, kk);
-      }
-      umma_commit(&sm.mbar);
-      if (k + 2 < n_tiles) {  // every thread is done reading this stage
-        fence_proxy_async();
-        issue(k + 2);
-      }
-    }
-    if (__syncthreads_or(!mbar_wait_bounded(&sm.mbar, mphase, p.err))) { dead = true; break; }
-    mphase ^= 1;
-    tc_fence_after();
-    {
-      float d2[16], dpb[16];
-      tmem_ld16(lane_base + TC_D2, d2);
-      tmem_ld16(lane_base + TC_DPB, dpb);
-      tmem_wait_ld();
-#pragma unroll
-      for (int qq = 0; qq < 8; ++qq)
-        acc[qq] = fmaf(acc[qq], corr[qq], valid ? gV * fmaf(d2[qq] + d2[8 + qq], 1.f / 64.f, dpb[qq] + dpb[8 + qq]) : 0.f);
-    }
-    tc_fence_before();
-  }
-
-  // ---- partial of this CTA: m (uniform), l = sum over threads, acc per channel
-#pragma unroll
-  for (int qq = 0; qq < 8; ++qq) {
-    float v = l_run[qq];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    l_run[qq] = v;
-  }
-  __syncthreads();
-  if (lane == 0) {
-#pragma unroll
-    for (int qq = 0; qq < 8; ++qq) sm.red[warp][qq] = l_run[qq];
-  }
-  __syncthreads();
-  for (int qq = 0; qq < G; ++qq) {
-    float* o = part_ptr(p, b, h, chunk, qq);
-    if (tid == 0) {
-      o[0] = dead ? -INFINITY : m_run[qq];
-      o[1] = dead ? 0.f : sm.red[0][qq] + sm.red[1][qq] + sm.red[2][qq] + sm.red[3][qq];
-    }
-    o[PACC + c] = dead ? 0.f : acc[qq];
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, TC_COLS);
 }
 
 // Raw open tile of (b, h): len % 128 tokens in 16-bit, unrotated query.
@@ -1097,41 +726,12 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
 
 // 2-D view of the packed pool as rows of 128 bytes, read in boxes of 64 rows
 // (one tile's K codes) with the 128-byte swizzle.
-static cudaError_t pool_tensor_map(const DecodeParams& p, CUtensorMap* m) {
-  auto encode = get_encode();
-  if (!encode) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {128, (cuuint64_t)p.num_blocks * (cuuint64_t)p.block_bytes / 128};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<unsigned char*>(p.pool), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <typename E>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
-  CUtensorMap kmap;
-  cudaError_t e = pool_tensor_map(p, &kmap);
+  const size_t smem = sizeof(DecSmem) + 128;
+  cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(DecSmem) + 1024;
-  e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(kmap, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int warps = batch * p.num_q_heads;
-  combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, 1, batch, out);
-  return cudaGetLastError();
-}
-
-template <typename E>
-static cudaError_t launch_decode_tc_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
-  const size_t smem = sizeof(TcSmem);
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  decode_tc_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), TCW * 32, smem, s>>>(p);
+  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
@@ -1140,13 +740,8 @@ static cudaError_t launch_decode_tc_t(DecodeParams p, int batch, float* out, cud
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
-#ifdef KVARN_DECODE_TC
-  return dtype == KVARN_DTYPE_BF16 ? launch_decode_tc_t<__nv_bfloat16>(p, batch, out, s)
-                                   : launch_decode_tc_t<__half>(p, batch, out, s);
-#else
   return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, batch, out, s)
                                    : launch_decode_t<__half>(p, batch, out, s);
-#endif
 }
 
 // ---- fixed-scratch variant of the packed decode (no allocation anywhere)

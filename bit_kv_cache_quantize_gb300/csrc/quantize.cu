@@ -380,7 +380,10 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
       *reinterpret_cast<uint32_t*>(rec + 512 + (tok0 + i) * 64 + 4 * cb) = word;
     }
   } else {
-    uint32_t half[8];  // channel 8cb + k: 2-bit codes of tokens tok0 .. tok0+7
+    // V word layout: token 16w + u of a channel at bit u (u even) or 15 + u
+    // (u odd) of the channel's word w.  Tokens tok0 .. tok0+7 (u = 8h + i)
+    // fill byte h (even i, at bit i) and byte 2 + h (odd i, at bit i - 1).
+    uint32_t half[8];  // channel 8cb + k: even-token byte in bits 0-7, odd-token byte in bits 16-23
 #pragma unroll
     for (int k = 0; k < 8; ++k) half[k] = 0;
 #pragma unroll
@@ -393,13 +396,18 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
         q2.x = fminf(fmaxf(q2.x, 0.f), (float)L);
         q2.y = fminf(fmaxf(q2.y, 0.f), (float)L);
         q2 = fadd2(q2, MAG2);
-        half[2 * pp] |= (__float_as_uint(q2.x) & 3u) << (2 * i);
-        half[2 * pp + 1] |= (__float_as_uint(q2.y) & 3u) << (2 * i);
+        const int sh = (i & 1) ? 15 + i : i;
+        half[2 * pp] |= (__float_as_uint(q2.x) & 3u) << sh;
+        half[2 * pp + 1] |= (__float_as_uint(q2.y) & 3u) << sh;
       }
     }
+    const int hb = (tok0 >> 3) & 1;
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      *reinterpret_cast<uint16_t*>(rec + 512 + (8 * cb + k) * 32 + (tok0 >> 2)) = (uint16_t)half[k];
+    for (int k = 0; k < 8; ++k) {
+      unsigned char* wp = rec + 512 + (8 * cb + k) * 32 + 4 * (tok0 >> 4);
+      wp[hb] = (unsigned char)half[k];
+      wp[2 + hb] = (unsigned char)(half[k] >> 16);
+    }
   }
   __syncthreads();
   const int bytes = IS_V ? V_REC : K_REC;
@@ -489,7 +497,8 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
   float x[D];
 #pragma unroll
   for (int c = 0; c < D; ++c) {
-    int code = kv ? (rec[512 + c * 32 + (t >> 2)] >> (2 * (t & 3))) & 3
+    const int vb = (t & 1) ? 15 + (t & 15) : (t & 15);  // bit of token t in its V word
+    int code = kv ? (rec[512 + c * 32 + 4 * (t >> 4) + (vb >> 3)] >> (vb & 7)) & 3
                   : (rec[512 + t * 64 + (c >> 1)] >> (4 * (c & 1))) & 15;
     x[c] = e4m3_to_float(rec[c]) * fmaf(a, static_cast<float>(code), b);
   }

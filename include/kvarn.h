@@ -39,8 +39,11 @@
  *     per-token step | b[128] FP16 (little-endian) per-token zero-point |
  *     codes[128 tokens][64 B], byte i of token t = code[t][2i] |
  *     code[t][2i+1] << 4.
- *   V record 4608 B: same 512-byte header | codes[128 channels][32 B],
- *     byte j of channel c = sum_i code[4j+i][c] << 2i.
+ *   V record 4608 B: same 512-byte header | codes[128 channels][32 B]:
+ *     channel c holds 8 little-endian 32-bit words; word w carries tokens
+ *     16w .. 16w+15, token 16w+u at bit u (u even) or bit 15+u (u odd),
+ *     i.e. even tokens in the low half-word and odd tokens in the high
+ *     half-word, 2 bits each.
  *   Block b of the pool = for each KV head h: [K record | V record], i.e.
  *     num_kv_heads * 13312 bytes; head h of block b starts at
  *     b * kvarn_block_bytes() + h * 13312.

@@ -319,9 +319,14 @@ int ora_quantize_tile(const double *X, int levels, int iters,
 /*   K (levels 15): g[128] E4M3 | a[128] E4M3 | b[128] FP16 LE |        */
 /*                  codes[128 tokens][64 B], byte i of token t =       */
 /*                  code[t][2i] | code[t][2i+1] << 4          = 8704 B */
-/*   V (levels 3):  same header | codes[128 channels][32 B], byte j of  */
-/*                  channel c = sum_i code[4j+i][c] << 2i     = 4608 B */
+/*   V (levels 3):  same header | codes[128 channels][32 B]: channel c */
+/*                  = 8 little-endian 32-bit words, word w holds tokens */
+/*                  16w..16w+15, token 16w+u at bit u (u even) or bit   */
+/*                  15+u (u odd)                              = 4608 B */
 /* ------------------------------------------------------------------ */
+
+/* bit of token u (0..15) inside its 32-bit V word */
+static int ora_v_bit(int u) { return (u & 1) ? 15 + u : u; }
 
 int ora_record_bytes(int is_v) { return 512 + (is_v ? D * T / 4 : D * T / 2); }
 
@@ -338,10 +343,11 @@ void ora_pack_record(int is_v, const uint8_t *g8, const uint8_t *a8, const uint1
                 p[t * 64 + i] = (uint8_t)(code[t * D + 2 * i] | (code[t * D + 2 * i + 1] << 4));
     } else {
         for (int c = 0; c < D; c++)
-            for (int j = 0; j < T / 4; j++) {
-                uint8_t byte = 0;
-                for (int i = 0; i < 4; i++) byte |= (uint8_t)(code[(4 * j + i) * D + c] << (2 * i));
-                p[c * 32 + j] = byte;
+            for (int w = 0; w < T / 16; w++) {
+                uint32_t word = 0;
+                for (int u = 0; u < 16; u++)
+                    word |= (uint32_t)code[(16 * w + u) * D + c] << ora_v_bit(u);
+                for (int k = 0; k < 4; k++) p[c * 32 + 4 * w + k] = (uint8_t)(word >> (8 * k));
             }
     }
 }
@@ -356,7 +362,8 @@ void ora_unpack_record(int is_v, const uint8_t *rec, uint8_t *g8, uint8_t *a8, u
     for (int t = 0; t < T; t++)
         for (int c = 0; c < D; c++)
             code[t * D + c] = !is_v ? (uint8_t)((p[t * 64 + c / 2] >> (4 * (c & 1))) & 15)
-                                    : (uint8_t)((p[c * 32 + t / 4] >> (2 * (t & 3))) & 3);
+                                    : (uint8_t)((p[c * 32 + 4 * (t / 16) + ora_v_bit(t % 16) / 8]
+                                                 >> (ora_v_bit(t % 16) % 8)) & 3);
 }
 
 /* Dequantise one record [P2 "The four-stage pipeline", fourth stage]:

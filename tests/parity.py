@@ -48,9 +48,10 @@ def unpack(rec: np.ndarray, is_v: bool):
         code[:, 0::2] = by & 15
         code[:, 1::2] = by >> 4
     else:
-        by = body.reshape(D, 32)                      # [channel][byte]
-        crumbs = np.stack([(by >> (2 * i)) & 3 for i in range(4)], axis=-1)  # [c][j][i] -> token 4j+i
-        code = crumbs.reshape(D, T).T.copy()
+        words = body.view("<u4").reshape(D, T // 16)  # [channel][word]: tokens 16w .. 16w+15
+        pos = np.array([u if u % 2 == 0 else 15 + u for u in range(16)], dtype=np.uint32)
+        crumbs = (words[:, :, None] >> pos[None, None, :]) & 3  # [c][w][u] -> token 16w+u
+        code = crumbs.reshape(D, T).T.astype(np.uint8).copy()
     return g8, a8, b16, code
 
 

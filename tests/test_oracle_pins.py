@@ -230,8 +230,11 @@ def test_record_layout_bytes():
     tl.code = tl.code % 4
     rv = O.pack_record(True, tl)
     assert rv.size == 4608
-    c, j = 77, 6                                                     # byte j of channel c
-    assert rv[512 + c * 32 + j] == sum(int(tl.code[4 * j + k, c]) << (2 * k) for k in range(4))
+    c, w = 77, 5                                                     # word w of channel c
+    word = int.from_bytes(bytes(rv[512 + c * 32 + 4 * w: 512 + c * 32 + 4 * w + 4]), "little")
+    even = sum(int(tl.code[16 * w + u, c]) << u for u in range(0, 16, 2))        # low half
+    odd = sum(int(tl.code[16 * w + u, c]) << (15 + u) for u in range(1, 16, 2))  # high half
+    assert word == even | odd
     g8, a8, b16, code = O.unpack_record(True, rv)
     assert np.array_equal(code, tl.code) and np.array_equal(b16, tl.b16)
 
