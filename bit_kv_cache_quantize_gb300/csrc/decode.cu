@@ -724,8 +724,6 @@ size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int c
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
 
-// 2-D view of the packed pool as rows of 128 bytes, read in boxes of 64 rows
-// (one tile's K codes) with the 128-byte swizzle.
 template <typename E>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
   const size_t smem = sizeof(DecSmem) + 128;

@@ -11,7 +11,19 @@
 
 namespace kvarn {
 constexpr int kHeadRec = 13312;
-constexpr int kChunkTiles = 16;  // packed tiles per split-K CTA
+constexpr int kChunkTiles = 16;  // fewest packed tiles per split-K CTA (sizes the workspace)
+
+// Packed tiles per split-K CTA for one call: 32 (longer CTAs amortise the
+// per-CTA query set-up and merge) when that still gives at least three waves
+// of CTAs at two per SM, else 16.
+static int choose_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return kChunkTiles;
+  const long long ctas = (long long)batch * num_kv_heads * ((max_blocks + 31) / 32);
+  return ctas >= 6LL * sms ? 32 : kChunkTiles;
+}
 constexpr int kF16ChunkTiles = 16;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -115,11 +127,12 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
                                  workspace_bytes);
   if (st != KVARN_OK || batch == 0) return st;
   if (!tail_pool || !aligned16(tail_pool)) return KVARN_ERR_INVALID;
-  const int n_chunks = (max_blocks + kChunkTiles - 1) / kChunkTiles;
+  const int chunk = choose_chunk_tiles(batch, cfg->num_kv_heads, max_blocks);
+  const int n_chunks = (max_blocks + chunk - 1) / chunk;
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
                  static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
                  max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads,
-                 cfg->num_blocks, kChunkTiles, n_chunks};
+                 cfg->num_blocks, chunk, n_chunks};
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -136,10 +149,11 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
   if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles) > KVARN_NOALLOC_SCRATCH_BYTES)
     return KVARN_ERR_UNSUPPORTED;  // larger than the fixed scratch: use kvarn_decode_attention
-  const int n_chunks = (max_blocks + kChunkTiles - 1) / kChunkTiles;
+  const int chunk = choose_chunk_tiles(batch, cfg->num_kv_heads, max_blocks);
+  const int n_chunks = (max_blocks + chunk - 1) / chunk;
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool, nullptr, dev_err,
                  static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale, max_blocks, cfg->num_kv_heads,
-                 cfg->num_q_heads, G, cfg->num_blocks, kChunkTiles, n_chunks};
+                 cfg->num_q_heads, G, cfg->num_blocks, chunk, n_chunks};
   return cuda_status(launch_decode_noalloc(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 

@@ -39,7 +39,7 @@ def test_sizes(lib):
     assert K.kvarn_tail_bytes(cfg, 3) == 3 * 8 * 2 * 128 * 128 * 2
     assert K.kvarn_fp16_block_bytes(cfg) == 8 * 65536
     ws = K.kvarn_decode_workspace_bytes(cfg, 32, 128)
-    assert ws == 32 * 8 * (8 + 1) * 8 * 132 * 4
+    assert ws == 32 * 8 * (8 + 1) * 8 * 132 * 4  # the 16-bit kernel's chunks of 16 tiles + open tile bound it
 
 
 @pytest.mark.parametrize("field,value,status", [
