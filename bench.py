@@ -100,6 +100,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# DRAM bytes actually moved by one decode call per algorithmic byte, from the
+# ncu capture of the 16K decode (profiles/decode_call_traffic_qwen3_32b_16k.md:
+# 449 723 392 B for 437 796 992 algorithmic bytes).  The serving step's call is
+# too large to capture, and its traffic grows with the records it reads.
+DECODE_TRAFFIC_PER_BYTE = 449723392 / 437796992
+
+
 def decode_bytes(lens, w):
     """Algorithmic bytes of one decode call: packed records of the closed
     tiles, raw open-tile tokens, queries, outputs, block ids and lengths."""
@@ -198,7 +205,9 @@ def run_gpu(args, rank, world):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": "kvarn_decode_attention (split-K decode + combine)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_source": peak_src, "traffic": None, "algorithmic_bytes_per_launch": dec_bytes,
+                     "peak_source": peak_src, "traffic": DECODE_TRAFFIC_PER_BYTE * dec_bytes,
+                     "traffic_source": "ncu capture of the 16K decode call, scaled by algorithmic bytes",
+                     "algorithmic_bytes_per_launch": dec_bytes,
                      "avg_launch_us": dec_avg_s * 1e6},
         "e2e": e2e,
         "gpu_launches": steps * 3,
