@@ -117,6 +117,28 @@ def decode_bytes(lens, w):
             + closed * 4 + len(lens) * 4)
 
 
+# --------------------------------------------------------------------------- multi-rank host logic
+def rank_seed(rank):
+    """Seed of rank's own serving batch: every rank draws its own sequences,
+    so ranks share no (sequence, KV head) unit and exchange no data."""
+    return 4 + 1000 * rank
+
+
+def reduce_max_ms(ms, device=None):
+    """The slowest rank's time (MAX all-reduce; a no-op without a process group)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(batch, steps, world, ms):
+    """Whole-job throughput: every rank decodes its own batch each step."""
+    return batch * steps * world / (ms / 1e3)
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_gpu(args, rank, world):
     import torch
@@ -131,7 +153,7 @@ def run_gpu(args, rank, world):
     hbm_peak, _, peak_src = measured_peaks()
     steps, warm = args.steps, args.warmup
     n_dec = max(64, steps + warm)
-    w = I.ragged_32b(steps=n_dec, seed=4 + 1000 * rank)
+    w = I.ragged_32b(steps=n_dec, seed=rank_seed(rank))
     c = PagedCache(w, dev)
     c.prefill()
     torch.cuda.synchronize()
@@ -180,14 +202,12 @@ def run_gpu(args, rank, world):
     ms = t0.elapsed_time(t1)
     assert c.check_error() == 0, "device error during the timed steps"
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = reduce_max_ms(ms, dev)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
     dec_avg_s = sum(dec_ms) / len(dec_ms) / 1e3
     dec_bytes = statistics.mean(decode_bytes([int(x) + 1 for x in pos_all[warm + i]], w) for i in range(steps))
     achieved = dec_bytes / dec_avg_s / 1e9
-    tokens_per_s = B_ * steps * world / (ms / 1e3)
+    tokens_per_s = job_tokens_per_s(B_, steps, world, ms)
 
     # e2e: the same steps through the public API with host buffers
     e2e = run_e2e(c, w, kn, vn, qs, pos_all, dev, warm, steps)
