@@ -98,6 +98,70 @@ struct AddOp { __device__ float operator()(float a, float b) const { return a + 
 struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
 struct MaxOp { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
 
+// Step 6 for this thread's 8 tokens x 8 channels: code = rne((Y - b) * (1/a))
+// (two fp32 roundings, as written), clamped below at 0 when CLAMP; adding
+// 1.5 * 2^23 leaves the rounded integer in the low mantissa bits.  K: byte
+// pair p of token t = code[2p] | code[2p+1] << 4.  V: token 16w + u of a
+// channel at bit u (u even) or 15 + u (u odd) of the channel's word w;
+// tokens tok0 .. tok0+7 (u = 8h + i) fill byte h (even i, at bit i) and
+// byte 2 + h (odd i, at bit i - 1).
+template <bool IS_V, bool CLAMP>
+__device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float2* tokv, unsigned char* rec,
+                                            int tok0, int cb) {
+  constexpr int L = IS_V ? 3 : 15;
+  constexpr float RNE_MAGIC = 12582912.0f;
+  const float2 MAG2 = make_float2(RNE_MAGIC, RNE_MAGIC);
+  auto code2 = [&](float2 y, float2 nb, float2 ia) {
+    float2 q2 = fmul2(fadd2(y, nb), ia);
+    // a min between the product and the rounding add keeps the two from being
+    // fused into one FMA (which would round once instead of twice); without
+    // saturation it only ever trims L (1 + 2^-23) to L
+    if constexpr (CLAMP) q2.x = fmaxf(q2.x, 0.f), q2.y = fmaxf(q2.y, 0.f);
+    q2.x = fminf(q2.x, (float)L);
+    q2.y = fminf(q2.y, (float)L);
+    return fadd2(q2, MAG2);
+  };
+  if constexpr (!IS_V) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 ta = tokv[tok0 + i];
+      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
+      uint32_t u[4];
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 q2 = code2(r[i][pp], nb, ia);
+        // low byte = code_x + 16 code_y (both codes in [0, 15], the bits above them zero)
+        u[pp] = (__float_as_uint(q2.y) << 4) + (__float_as_uint(q2.x) & 0xFu);
+      }
+      const uint32_t word = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
+      *reinterpret_cast<uint32_t*>(rec + 512 + (tok0 + i) * 64 + 4 * cb) = word;
+    }
+  } else {
+    uint32_t half[8];  // channel 8cb + k: even-token byte in bits 0-7, odd-token byte in bits 16-23
+#pragma unroll
+    for (int k = 0; k < 8; ++k) half[k] = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 ta = tokv[tok0 + i];
+      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 q2 = code2(r[i][pp], nb, ia);
+        const int sh = (i & 1) ? 15 + i : i;
+        half[2 * pp] |= (__float_as_uint(q2.x) & 3u) << sh;
+        half[2 * pp + 1] |= (__float_as_uint(q2.y) & 3u) << sh;
+      }
+    }
+    const int hb = (tok0 >> 3) & 1;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      unsigned char* wp = rec + 512 + (8 * cb + k) * 32 + 4 * (tok0 >> 4);
+      wp[hb] = (unsigned char)half[k];
+      wp[2 + hb] = (unsigned char)(half[k] >> 16);
+    }
+  }
+}
+
 // Quantise one tile.  src: token rows of 128 16-bit channels, consecutive
 // rows row_stride elements apart (16-byte aligned).  dst: the record in the
 // pool.  All 256 threads of the CTA must call this.  After the rotation every
@@ -317,6 +381,7 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
   __syncthreads();
 
   // ---- 5. per-token zero-point and step
+  bool sat;
   float2 ig[4];
   {
     const float4 g0 = *reinterpret_cast<const float4*>(sm.inv_g + 8 * cb);
@@ -329,7 +394,7 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) r[i][pp] = fmul2(r[i][pp], ig[pp]);   // r now holds Y = R / g
   {
-    float mn[8][2], mx[8][2];
+    float mm[8][2];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       float a = fminf(r[i][0].x, r[i][0].y), bmax = fmaxf(r[i][0].x, r[i][0].y);
@@ -338,18 +403,21 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
         a = fminf(a, fminf(r[i][pp].x, r[i][pp].y));
         bmax = fmaxf(bmax, fmaxf(r[i][pp].x, r[i][pp].y));
       }
-      mn[i][0] = a; mn[i][1] = a;
-      mx[i][0] = bmax; mx[i][1] = bmax;
+      mm[i][0] = -a;     // max of -Y = -(min of Y): one max-reduction for both
+      mm[i][1] = bmax;
     }
-    float ymin, ymax, dummy;
-    halve16(mn, lane, MinOp(), ymin, dummy);
-    halve16(mx, lane, MaxOp(), ymax, dummy);
+    float nymin, ymax;
+    halve16(mm, lane, MaxOp(), nymin, ymax);
+    const float ymin = -nymin;
     const __half bh = (ymin <= -65504.f) ? __float2half_rn(-65504.f) : __float2half_rd(ymin);
     const float bv = __half2float(bh);
     const float step = __fdiv_ru(__fsub_ru(ymax, bv), (float)L);
     uint8_t ac = float_to_e4m3_ru(step);
     if (ac == 0) ac = 0x01;
     const float inv_a = __frcp_rn(e4m3_to_float(ac));
+    // without saturation b <= min Y and a >= (max Y - b) / L, so every
+    // (Y - b) * (1/a) lies in [0, L (1 + 2^-23)]: no clamp at 0 needed
+    sat = !(ymin > -65504.f) || !(step <= 448.f);
     if ((lane & 1) == 0) {
       const int tk = tok0 + ((lane & 15) >> 1);
       rec[128 + tk] = ac;
@@ -357,58 +425,12 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
       tokv[tk] = make_float2(bv, inv_a);
     }
   }
-  __syncthreads();
+  const bool clamp_codes = __syncthreads_or(sat);
 
-  // ---- 6. codes and packing: code = rne((Y - b) * (1/a)) clamped to [0, L];
-  // the rounding adds 1.5 * 2^23, which leaves the integer in the low bits
-  constexpr float RNE_MAGIC = 12582912.0f;
-  const float2 MAG2 = make_float2(RNE_MAGIC, RNE_MAGIC);
-  if constexpr (!IS_V) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 ta = tokv[tok0 + i];
-      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
-      uint32_t word = 0;
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        float2 q2 = fmul2(fadd2(r[i][pp], nb), ia);
-        q2.x = fminf(fmaxf(q2.x, 0.f), (float)L);
-        q2.y = fminf(fmaxf(q2.y, 0.f), (float)L);
-        q2 = fadd2(q2, MAG2);
-        word |= ((__float_as_uint(q2.x) & 0xFu) | ((__float_as_uint(q2.y) & 0xFu) << 4)) << (8 * pp);
-      }
-      *reinterpret_cast<uint32_t*>(rec + 512 + (tok0 + i) * 64 + 4 * cb) = word;
-    }
-  } else {
-    // V word layout: token 16w + u of a channel at bit u (u even) or 15 + u
-    // (u odd) of the channel's word w.  Tokens tok0 .. tok0+7 (u = 8h + i)
-    // fill byte h (even i, at bit i) and byte 2 + h (odd i, at bit i - 1).
-    uint32_t half[8];  // channel 8cb + k: even-token byte in bits 0-7, odd-token byte in bits 16-23
-#pragma unroll
-    for (int k = 0; k < 8; ++k) half[k] = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float2 ta = tokv[tok0 + i];
-      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        float2 q2 = fmul2(fadd2(r[i][pp], nb), ia);
-        q2.x = fminf(fmaxf(q2.x, 0.f), (float)L);
-        q2.y = fminf(fmaxf(q2.y, 0.f), (float)L);
-        q2 = fadd2(q2, MAG2);
-        const int sh = (i & 1) ? 15 + i : i;
-        half[2 * pp] |= (__float_as_uint(q2.x) & 3u) << sh;
-        half[2 * pp + 1] |= (__float_as_uint(q2.y) & 3u) << sh;
-      }
-    }
-    const int hb = (tok0 >> 3) & 1;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      unsigned char* wp = rec + 512 + (8 * cb + k) * 32 + 4 * (tok0 >> 4);
-      wp[hb] = (unsigned char)half[k];
-      wp[2 + hb] = (unsigned char)(half[k] >> 16);
-    }
-  }
+  // ---- 6. codes and packing: code = rne((Y - b) * (1/a)), clamped to [0, L]
+  // only in a tile where some token saturated its zero-point or step
+  if (clamp_codes) encode_pack<IS_V, true>(r, tokv, rec, tok0, cb);
+  else encode_pack<IS_V, false>(r, tokv, rec, tok0, cb);
   __syncthreads();
   const int bytes = IS_V ? V_REC : K_REC;
   for (int i = tid; i < bytes / 16; i += 256)
