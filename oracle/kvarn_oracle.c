@@ -314,11 +314,16 @@ int ora_quantize_tile(const double *X, int levels, int iters,
     return flags;
 }
 
+enum { ORA_K4 = 0, ORA_V2 = 1, ORA_K2 = 2 };
+
 /* ------------------------------------------------------------------ */
 /* Packed record layout (16-byte aligned, scales first)                */
 /*   K (levels 15): g[128] E4M3 | a[128] E4M3 | b[128] FP16 LE |        */
 /*                  codes[128 tokens][64 B], byte i of token t =       */
 /*                  code[t][2i] | code[t][2i+1] << 4          = 8704 B */
+/*   K2 (levels 3, the K2/V2 preset): same header | codes[128 tok]    */
+/*                  [32 B], byte i of token t = sum_k code[t][4i+k]<<2k */
+/*                                                            = 4608 B */
 /*   V (levels 3):  same header | codes[128 channels][32 B]: channel c */
 /*                  = 8 little-endian 32-bit words, word w holds tokens */
 /*                  16w..16w+15, token 16w+u at bit u (u even) or bit   */
@@ -328,19 +333,28 @@ int ora_quantize_tile(const double *X, int levels, int iters,
 /* bit of token u (0..15) inside its 32-bit V word */
 static int ora_v_bit(int u) { return (u & 1) ? 15 + u : u; }
 
-int ora_record_bytes(int is_v) { return 512 + (is_v ? D * T / 4 : D * T / 2); }
+/* record kinds: ORA_K4 (4-bit keys), ORA_V2 (2-bit values), ORA_K2 (2-bit keys) */
+int ora_record_bytes(int kind) { return 512 + (kind == ORA_K4 ? D * T / 2 : D * T / 4); }
+int ora_kind_levels(int kind) { return kind == ORA_K4 ? 15 : 3; }
 
-void ora_pack_record(int is_v, const uint8_t *g8, const uint8_t *a8, const uint16_t *b16,
+void ora_pack_record(int kind, const uint8_t *g8, const uint8_t *a8, const uint16_t *b16,
                      const uint8_t *code, uint8_t *rec)
 {
     memcpy(rec, g8, D);
     memcpy(rec + 128, a8, T);
     for (int t = 0; t < T; t++) { rec[256 + 2 * t] = (uint8_t)(b16[t] & 0xFF); rec[257 + 2 * t] = (uint8_t)(b16[t] >> 8); }
     uint8_t *p = rec + 512;
-    if (!is_v) {
+    if (kind == ORA_K4) {
         for (int t = 0; t < T; t++)
             for (int i = 0; i < D / 2; i++)
                 p[t * 64 + i] = (uint8_t)(code[t * D + 2 * i] | (code[t * D + 2 * i + 1] << 4));
+    } else if (kind == ORA_K2) {
+        for (int t = 0; t < T; t++)
+            for (int i = 0; i < D / 4; i++) {
+                uint8_t byte = 0;
+                for (int k = 0; k < 4; k++) byte |= (uint8_t)(code[t * D + 4 * i + k] << (2 * k));
+                p[t * 32 + i] = byte;
+            }
     } else {
         for (int c = 0; c < D; c++)
             for (int w = 0; w < T / 16; w++) {
@@ -352,7 +366,7 @@ void ora_pack_record(int is_v, const uint8_t *g8, const uint8_t *a8, const uint1
     }
 }
 
-void ora_unpack_record(int is_v, const uint8_t *rec, uint8_t *g8, uint8_t *a8, uint16_t *b16,
+void ora_unpack_record(int kind, const uint8_t *rec, uint8_t *g8, uint8_t *a8, uint16_t *b16,
                        uint8_t *code)
 {
     memcpy(g8, rec, D);
@@ -361,19 +375,20 @@ void ora_unpack_record(int is_v, const uint8_t *rec, uint8_t *g8, uint8_t *a8, u
     const uint8_t *p = rec + 512;
     for (int t = 0; t < T; t++)
         for (int c = 0; c < D; c++)
-            code[t * D + c] = !is_v ? (uint8_t)((p[t * 64 + c / 2] >> (4 * (c & 1))) & 15)
-                                    : (uint8_t)((p[c * 32 + 4 * (t / 16) + ora_v_bit(t % 16) / 8]
-                                                 >> (ora_v_bit(t % 16) % 8)) & 3);
+            code[t * D + c] = kind == ORA_K4 ? (uint8_t)((p[t * 64 + c / 2] >> (4 * (c & 1))) & 15)
+                            : kind == ORA_K2 ? (uint8_t)((p[t * 32 + c / 4] >> (2 * (c & 3))) & 3)
+                                             : (uint8_t)((p[c * 32 + 4 * (t / 16) + ora_v_bit(t % 16) / 8]
+                                                          >> (ora_v_bit(t % 16) % 8)) & 3);
 }
 
 /* Dequantise one record [P2 "The four-stage pipeline", fourth stage]:
  * Rhat[t][c] = g_c (a_t code_tc + b_t), Xhat = Rhat H (unrotated). */
-void ora_dequantize_record(int is_v, const uint8_t *rec, double *Xhat)
+void ora_dequantize_record(int kind, const uint8_t *rec, double *Xhat)
 {
     static __thread double Rh[T * D];
     uint8_t g8[D], a8[T], code[T * D];
     uint16_t b16[T];
-    ora_unpack_record(is_v, rec, g8, a8, b16, code);
+    ora_unpack_record(kind, rec, g8, a8, b16, code);
     for (int t = 0; t < T; t++)
         for (int c = 0; c < D; c++)
             Rh[t * D + c] = ora_e4m3_decode(g8[c]) *
@@ -417,10 +432,11 @@ void ora_attention(const double *q, int G, const double *K, const double *V, int
  * applied at read time]: the key rotation and per-channel key scales are
  * folded into the query, per-token scale/zero into the scores, per-channel
  * value scales into the accumulator, and one inverse rotation is applied to
- * the output.  krec/vrec: n_tiles records each; ktail/vtail: [n_tail][D]. */
+ * the output.  krec/vrec: n_tiles records each (keys of kind kkind, values
+ * ORA_V2); ktail/vtail: [n_tail][D]. */
 void ora_attention_folded(const double *q, int G, const uint8_t *const *krec,
                           const uint8_t *const *vrec, int n_tiles, const double *ktail,
-                          const double *vtail, int n_tail, double scale, double *out)
+                          const double *vtail, int n_tail, double scale, int kkind, double *out)
 {
     int n = n_tiles * T + n_tail;
     double *s = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
@@ -433,7 +449,7 @@ void ora_attention_folded(const double *q, int G, const uint8_t *const *krec,
         for (int d = 0; d < D; d++) qr[d] *= scale;
         double m = -INFINITY;
         for (int tile = 0; tile < n_tiles; tile++) {
-            ora_unpack_record(0, krec[tile], g8, a8, b16, code);
+            ora_unpack_record(kkind, krec[tile], g8, a8, b16, code);
             double qg[D], S = 0.0;
             for (int c = 0; c < D; c++) { qg[c] = qr[c] * ora_e4m3_decode(g8[c]); S += qg[c]; }
             for (int t = 0; t < T; t++) {
@@ -453,7 +469,7 @@ void ora_attention_folded(const double *q, int G, const uint8_t *const *krec,
         double l = 0.0;
         for (int d = 0; d < D; d++) { acc_rot[d] = 0.0; acc_raw[d] = 0.0; }
         for (int tile = 0; tile < n_tiles; tile++) {
-            ora_unpack_record(1, vrec[tile], g8, a8, b16, code);
+            ora_unpack_record(ORA_V2, vrec[tile], g8, a8, b16, code);
             double pb = 0.0, pacc[D];
             for (int c = 0; c < D; c++) pacc[c] = 0.0;
             for (int t = 0; t < T; t++) {
@@ -483,16 +499,17 @@ void ora_attention_folded(const double *q, int G, const uint8_t *const *krec,
 /* Quantise n tiles.  src: 16-bit values (dtype 0 = fp16, 1 = bf16); tile i's
  * token row r starts at element first[i] + r * row_stride, channels
  * contiguous.  levels/iters as above.  rec: n records of
- * ora_record_bytes(is_v) bytes.  flags: n ints (may be NULL). */
+ * ora_record_bytes(kind) bytes, quantised to ora_kind_levels(kind) levels.
+ * flags: n ints (may be NULL). */
 typedef struct {
     const uint16_t *src; int dtype; const int64_t *first; int64_t row_stride;
-    int n, is_v, iters, nthreads, tid; uint8_t *rec; int *flags;
+    int n, kind, iters, nthreads, tid; uint8_t *rec; int *flags;
 } qjob;
 
 static void *quantize_worker(void *arg)
 {
     qjob *j = (qjob *)arg;
-    int L = j->is_v ? 3 : 15, rb = ora_record_bytes(j->is_v);
+    int L = ora_kind_levels(j->kind), rb = ora_record_bytes(j->kind);
     double *X = (double *)malloc(sizeof(double) * T * D);
     uint8_t g8[D], a8[T], *code = (uint8_t *)malloc(T * D);
     uint16_t b16[T];
@@ -503,7 +520,7 @@ static void *quantize_worker(void *arg)
                 X[t * D + c] = j->dtype ? ora_bf16_decode(h) : ora_f16_decode(h);
             }
         int f = ora_quantize_tile(X, L, j->iters, g8, a8, b16, code, NULL, NULL, NULL);
-        ora_pack_record(j->is_v, g8, a8, b16, code, j->rec + (int64_t)i * rb);
+        ora_pack_record(j->kind, g8, a8, b16, code, j->rec + (int64_t)i * rb);
         if (j->flags) j->flags[i] = f;
     }
     free(X); free(code);
@@ -511,14 +528,14 @@ static void *quantize_worker(void *arg)
 }
 
 void ora_quantize_batch(const uint16_t *src, int dtype, const int64_t *first, int64_t row_stride,
-                        int n, int is_v, int iters, uint8_t *rec, int *flags, int nthreads)
+                        int n, int kind, int iters, uint8_t *rec, int *flags, int nthreads)
 {
     if (nthreads < 1) nthreads = 1;
     pthread_t th[256];
     qjob jobs[256];
     if (nthreads > 256) nthreads = 256;
     for (int k = 0; k < nthreads; k++) {
-        jobs[k] = (qjob){src, dtype, first, row_stride, n, is_v, iters, nthreads, k, rec, flags};
+        jobs[k] = (qjob){src, dtype, first, row_stride, n, kind, iters, nthreads, k, rec, flags};
         pthread_create(&th[k], NULL, quantize_worker, &jobs[k]);
     }
     for (int k = 0; k < nthreads; k++) pthread_join(th[k], NULL);
@@ -531,7 +548,7 @@ void ora_quantize_batch(const uint16_t *src, int dtype, const int64_t *first, in
 typedef struct {
     const double *q; int G; const uint8_t *const *krec, *const *vrec; const int64_t *off;
     const int32_t *n_tiles; const double *ktail, *vtail; const int32_t *n_tail; double scale;
-    int n_units, nthreads, tid; double *out;
+    int kkind, n_units, nthreads, tid; double *out;
 } ajob;
 
 static void *attention_worker(void *arg)
@@ -540,13 +557,13 @@ static void *attention_worker(void *arg)
     for (int u = j->tid; u < j->n_units; u += j->nthreads)
         ora_attention_folded(j->q + (int64_t)u * j->G * D, j->G, j->krec + j->off[u], j->vrec + j->off[u],
                              j->n_tiles[u], j->ktail + (int64_t)u * T * D, j->vtail + (int64_t)u * T * D,
-                             j->n_tail[u], j->scale, j->out + (int64_t)u * j->G * D);
+                             j->n_tail[u], j->scale, j->kkind, j->out + (int64_t)u * j->G * D);
     return NULL;
 }
 
 void ora_attention_batch(const double *q, int G, const uint8_t *const *krec, const uint8_t *const *vrec,
                          const int64_t *off, const int32_t *n_tiles, const double *ktail,
-                         const double *vtail, const int32_t *n_tail, double scale, int n_units,
+                         const double *vtail, const int32_t *n_tail, double scale, int kkind, int n_units,
                          double *out, int nthreads)
 {
     if (nthreads < 1) nthreads = 1;
@@ -554,7 +571,7 @@ void ora_attention_batch(const double *q, int G, const uint8_t *const *krec, con
     pthread_t th[256];
     ajob jobs[256];
     for (int k = 0; k < nthreads; k++) {
-        jobs[k] = (ajob){q, G, krec, vrec, off, n_tiles, ktail, vtail, n_tail, scale, n_units, nthreads, k, out};
+        jobs[k] = (ajob){q, G, krec, vrec, off, n_tiles, ktail, vtail, n_tail, scale, kkind, n_units, nthreads, k, out};
         pthread_create(&th[k], NULL, attention_worker, &jobs[k]);
     }
     for (int k = 0; k < nthreads; k++) pthread_join(th[k], NULL);

@@ -239,6 +239,26 @@ def test_record_layout_bytes():
     assert np.array_equal(code, tl.code) and np.array_equal(b16, tl.b16)
 
 
+def test_k2_record_layout_bytes():
+    """K2/V2 preset: 2-bit key codes token-major, 32 B per token, four
+    codes per byte with channel 4i+k at bits 2k of byte i."""
+    tl = O.Tile((np.arange(D) % 120).astype(np.uint8), (np.arange(T) * 5 % 120).astype(np.uint8),
+                (np.arange(T) * 301 % 30000).astype(np.uint16),
+                ((np.arange(T)[:, None] * 7 + np.arange(D)[None, :]) % 4).astype(np.uint8),
+                None, None, None, 0)
+    rk = O.pack_record(False, tl, k_bits=2)
+    assert rk.size == 4608 and O.record_bytes(False, 2) == 4608 and O.levels(False, 2) == 3
+    assert rk[7] == 7 and rk[128 + 3] == 15 and rk[256 + 2 * 5] == (5 * 301) & 0xFF  # header as for 4-bit keys
+    t, i = 41, 19
+    assert rk[512 + t * 32 + i] == sum(int(tl.code[t, 4 * i + k]) << (2 * k) for k in range(4))
+    g8, a8, b16, code = O.unpack_record(False, rk, k_bits=2)
+    assert np.array_equal(code, tl.code) and np.array_equal(g8, tl.g8) and np.array_equal(a8, tl.a8)
+    # the same codes in the 4-bit key layout dequantise to the same values
+    rk4 = O.pack_record(False, tl, k_bits=4)
+    assert np.array_equal(O.dequantize_record(False, rk, 2), O.dequantize_record(False, rk4, 4))
+    assert (O.record_bytes(False, 2) * 8 / (T * D), O.record_bytes(True) * 8 / (T * D)) == (2.25, 2.25)
+
+
 def test_bits_per_element_against_pages():
     """The pages give ~2.3 bits/element including the dual FP8 scales and
     FP16 zero-points, for 4-bit keys / 2-bit values per 128-token tile."""
@@ -271,20 +291,21 @@ def test_attention_matches_torch_sdpa():
     assert np.abs(O.attention(q, K, V, 0.3) - ref.numpy()).max() < 1e-13
 
 
+@pytest.mark.parametrize("k_bits", [4, 2])
 @pytest.mark.parametrize("n_tiles,n_tail", [(1, 0), (2, 37), (0, 5), (3, 127)])
-def test_folded_attention_equals_plain(n_tiles, n_tail):
+def test_folded_attention_equals_plain(n_tiles, n_tail, k_bits):
     rng = np.random.default_rng(10 + n_tiles)
     krec, vrec, Ks, Vs = [], [], [], []
     for i in range(n_tiles):
         Xk = key_tile(20 + i); Xv = rng.standard_normal((T, D))
-        krec.append(O.pack_record(False, O.quantize_tile(Xk, 15)))
+        krec.append(O.pack_record(False, O.quantize_tile(Xk, O.levels(False, k_bits)), k_bits))
         vrec.append(O.pack_record(True, O.quantize_tile(Xv, 3)))
-        Ks.append(O.dequantize_record(False, krec[-1])); Vs.append(O.dequantize_record(True, vrec[-1]))
+        Ks.append(O.dequantize_record(False, krec[-1], k_bits)); Vs.append(O.dequantize_record(True, vrec[-1]))
     kt = rng.standard_normal((n_tail, D)); vt = rng.standard_normal((n_tail, D))
     q = rng.standard_normal((8, D))
     K = np.concatenate(Ks + [kt]); V = np.concatenate(Vs + [vt])
     plain = O.attention(q, K, V, 1 / math.sqrt(D))
-    folded = O.attention_folded(q, krec, vrec, kt, vt, 1 / math.sqrt(D))
+    folded = O.attention_folded(q, krec, vrec, kt, vt, 1 / math.sqrt(D), k_bits)
     assert np.abs(plain - folded).max() < 1e-9
 
 
