@@ -113,7 +113,8 @@ def decode_bytes(lens, w):
     H = w.num_kv_heads
     closed = sum(n // T for n in lens)
     tail = sum(n % T for n in lens)
-    return (closed * H * 13312 + tail * H * 2 * D * 2 + len(lens) * w.num_q_heads * D * (2 + 4)
+    head_rec = 2 * 512 + T * D * (w.k_bits + 2) // 8   # K and V record of one (tile, head)
+    return (closed * H * head_rec + tail * H * 2 * D * 2 + len(lens) * w.num_q_heads * D * (2 + 4)
             + closed * 4 + len(lens) * 4)
 
 
@@ -353,6 +354,21 @@ def components(dev, hbm_peak):
         "fp16_frac_hbm": b_16 / t_16 / 1e9 / hbm_peak, "fp16_bytes": b_16,
         "speedup_vs_fp16": t_16 / t_pk,
         "context_tokens_per_s": w.batch * w.seq_lens[0] / t_pk,
+    }
+    del c
+    torch.cuda.empty_cache()
+
+    # --- the same decode over 2-bit keys (K2/V2 records, 9216 B per tile and head)
+    w.k_bits = 2
+    c = PagedCache(w, dev)
+    c.prefill()
+    t_k2 = timed(lambda: c.decode(q, o), 50)
+    b_k2 = decode_bytes(w.seq_lens, w)
+    assert c.check_error() == 0
+    out["decode_16k_k2v2"] = {
+        "workload": "qwen3_32b_decode_16k with 2-bit keys and values (K2/V2 records)",
+        "us": t_k2 * 1e6, "tokens_per_s": w.batch / t_k2, "GBps": b_k2 / t_k2 / 1e9,
+        "frac_hbm": b_k2 / t_k2 / 1e9 / hbm_peak, "bytes": b_k2, "speedup_vs_fp16": t_16 / t_k2,
     }
     del c, q, o
     torch.cuda.empty_cache()

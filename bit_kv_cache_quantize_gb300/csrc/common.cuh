@@ -5,6 +5,7 @@
 // mbarrier, and the FP8 E4M3 / FP16 conversions the packed format needs.
 #pragma once
 
+#include "params.h"
 #include <cstdint>
 #include <type_traits>
 #include <cuda_fp16.h>
@@ -17,8 +18,9 @@ namespace kvarn {
 
 constexpr int D = 128;               // channels per token (head_dim)
 constexpr int T = 128;               // tokens per tile (one paged block)
-constexpr int K_REC = 8704;          // 512 B header + 128 x 64 B of 4-bit codes
-constexpr int V_REC = 4608;          // 512 B header + 128 x 32 B of 2-bit codes
+constexpr int K_REC = rec_bytes(4);  // 4-bit keys (kvarn_k4v2 preset): 8704 B
+constexpr int K2_REC = rec_bytes(2); // 2-bit keys (K2/V2 preset): 4608 B
+constexpr int V_REC = rec_bytes(2);  // 2-bit values: 4608 B
 constexpr int HEAD_REC = K_REC + V_REC;
 constexpr float INV_SQRT_D = 0.08838834764831845f;  // 1/sqrt(128)
 

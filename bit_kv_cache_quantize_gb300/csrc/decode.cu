@@ -68,8 +68,9 @@ constexpr int DEC_WARPS = 8;
 #define KVARN_PV_ILP 4
 #endif
 constexpr int PV_ILP = KVARN_PV_ILP;  // independent MMA chains interleaved in PV
+template <int KBITS>
 struct DecSmem {
-  alignas(128) unsigned char krec[DEC_WARPS][K_REC];
+  alignas(128) unsigned char krec[DEC_WARPS][rec_bytes(KBITS)];
   alignas(128) unsigned char vrec[DEC_WARPS][V_REC];
   alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order (hi, lo, hi/16, lo/16)
   alignas(16) float qr[8][D];   // rotated, scaled queries (set-up only)
@@ -82,8 +83,40 @@ struct DecMerge {
   float l[DEC_WARPS][8];
   float acc[DEC_WARPS][8][D];
 };
-static_assert(sizeof(DecMerge) <= sizeof(DecSmem::krec), "merge area must fit");
-static_assert(K_REC % 128 == 0 && V_REC % 128 == 0, "record buffers stay 128-byte aligned");
+static_assert(sizeof(DecMerge) <= sizeof(DecSmem<2>::krec), "merge area must fit");
+static_assert(K_REC % 128 == 0 && K2_REC % 128 == 0 && V_REC % 128 == 0, "record buffers stay 128-byte aligned");
+
+// Key layouts.  KBITS = 4: token rows of 64 B, byte i = channels 2i, 2i+1 (nibbles).
+// KBITS = 2: token rows of 32 B, byte i = channels 4i .. 4i+3 (crumbs at bits 2k).
+// A QK k-block kb takes, from the lane's 32 channels 32j .. 32j+31, two channel
+// pairs (one per B register) whose codes sit at the same bits of the two
+// half-words of one 32-bit code word; their entries of the query operand are
+// divided by the power of two the field position multiplies the code by.
+template <int KBITS>
+struct KeyLayout;
+template <>
+struct KeyLayout<4> {
+  // channels (c0, c0+4) at x1 and (c0+1, c0+5) at x16, c0 = 8 (kb >> 1) + 2 (kb & 1)
+  __device__ static int ch_a(int kb) { return 8 * (kb >> 1) + 2 * (kb & 1); }
+  __device__ static int ch_b(int kb) { return ch_a(kb) + 1; }
+  static constexpr int PAIR = 4;                        // distance between the two channels of a pair
+  __device__ static float scale_a(int) { return 1.f; }
+  __device__ static float scale_b(int) { return 1.f / 16.f; }
+  __device__ static int gword_lo(int kb) { return 2 * (kb >> 1); }  // g bytes: word of ch_a, word of ch_a + PAIR
+  __device__ static int gword_hi(int kb) { return 2 * (kb >> 1) + 1; }
+};
+template <>
+struct KeyLayout<2> {
+  // word w = kb >> 2 holds channels 16w .. 16w+15 (low half 0-7, high half 8-15);
+  // (kb >> 1) & 1 selects the word shifted by 8; fields at crumbs s0 = 2 (kb & 1), s0 + 1
+  __device__ static int ch_a(int kb) { return 16 * (kb >> 2) + 4 * ((kb >> 1) & 1) + 2 * (kb & 1); }
+  __device__ static int ch_b(int kb) { return ch_a(kb) + 1; }
+  static constexpr int PAIR = 8;
+  __device__ static float scale_a(int kb) { return (kb & 1) ? 1.f / 16.f : 1.f; }
+  __device__ static float scale_b(int kb) { return (kb & 1) ? 1.f / 64.f : 1.f / 4.f; }
+  __device__ static int gword_lo(int kb) { return 4 * (kb >> 2) + ((kb >> 1) & 1); }
+  __device__ static int gword_hi(int kb) { return gword_lo(kb) + 2; }
+};
 
 template <typename E>
 __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigned char* smem);
@@ -123,8 +156,11 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 //     B = 2-bit codes of channel 8 nbp + g, whose 32-bit words keep even
 //     tokens in the low half and odd tokens in the high half, so each B
 //     register is one masked field of one word.
-template <typename E>
+template <typename E, int KBITS>
 __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
+  using KL = KeyLayout<KBITS>;
+  constexpr int KREC = rec_bytes(KBITS), KROW = D * KBITS / 8;  // KROW: code bytes per token
+  static_assert(KROW == 16 * KBITS, "token row");
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
@@ -142,7 +178,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   const int n_tiles = min(p.chunk_tiles, n_closed - first);
   if (n_tiles <= 0) return;
   const uint32_t sbase = smem_u32(smem_raw);
-  DecSmem& sm = *reinterpret_cast<DecSmem*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
+  DecSmem<KBITS>& sm = *reinterpret_cast<DecSmem<KBITS>*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
   const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
@@ -158,8 +194,8 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     if (blk >= 0 && blk < p.num_blocks) {
-      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * HEAD_REC + (is_v ? K_REC : 0);
-      const uint32_t bytes = is_v ? V_REC : K_REC;
+      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * head_rec(KBITS) + (is_v ? KREC : 0);
+      const uint32_t bytes = is_v ? V_REC : KREC;
       mbar_expect_tx(bar, bytes);
       bulk_g2s(is_v ? sm.vrec[warp] : sm.krec[warp], src, bytes, bar);
     } else {
@@ -214,9 +250,10 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   }
   __syncthreads();
   {  // thread (kb = warp, lane) forms the fp16 high/low query pairs of its A-fragment slot
-    const int kb = warp, c0 = 32 * j + 8 * (kb >> 1) + 2 * (kb & 1);
+    const int kb = warp, ca = 32 * j + KL::ch_a(kb), cb = 32 * j + KL::ch_b(kb);
     const float* q = sm.qr[g];
-    const float v0 = q[c0], v1 = q[c0 + 4], v2 = q[c0 + 1] * (1.f / 16.f), v3 = q[c0 + 5] * (1.f / 16.f);
+    const float sa = KL::scale_a(kb), sb = KL::scale_b(kb);
+    const float v0 = q[ca] * sa, v1 = q[ca + KL::PAIR] * sa, v2 = q[cb] * sb, v3 = q[cb + KL::PAIR] * sb;
     const __half2 h01 = __floats2half2_rn(v0, v1), h23 = __floats2half2_rn(v2, v3);
     const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
     const __half2 l01 = __floats2half2_rn(v0 - f01.x, v1 - f01.y), l23 = __floats2half2_rn(v2 - f23.x, v3 - f23.y);
@@ -253,7 +290,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
         const uint32_t gw[8] = {gA.x, gA.y, gA.z, gA.w, gB.x, gB.y, gB.z, gB.w};  // channels 32j + 4i .. +3
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t lo = gw[2 * (kb >> 1)], hi = gw[2 * (kb >> 1) + 1];
+          const uint32_t lo = gw[KL::gword_lo(kb)], hi = gw[KL::gword_hi(kb)];
           const uint32_t pr = __byte_perm(lo, hi, (kb & 1) ? 0x7362 : 0x5140);
           const __half2 g01 = e4m3x2_to_half2(pr), g23 = e4m3x2_to_half2(pr >> 16);
           const uint4 qv = sm.qf[kb][lane];
@@ -267,12 +304,16 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
       }
       float sacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kb = 0; kb < 8; ++kb) mma_f16(sacc, afr[kb], 0x3C003C00u, 0x4C004C00u);  // B = 1 | 16
+      for (int kb = 0; kb < 8; ++kb) {  // B = the field multipliers (1 | 16 for 4-bit keys; 1 | 4, 16 | 64 for 2-bit)
+        const uint32_t b0 = (KBITS == 4 || !(kb & 1)) ? 0x3C003C00u : 0x4C004C00u;
+        const uint32_t b1 = KBITS == 4 ? 0x4C004C00u : ((kb & 1) ? 0x54005400u : 0x44004400u);
+        mma_f16(sacc, afr[kb], b0, b1);
+      }
       const float S = sacc[0] + sacc[2];
       const float2 S2 = make_float2(S, S);
 
       // ---- QK: scores x qs = aK <qg, code> + bK S
-      const unsigned char* kc = kr + 512 + (32 * (g >> 1) + (g & 1)) * 64 + 16 * j;
+      const unsigned char* kc = kr + 512 + (32 * (g >> 1) + (g & 1)) * KROW + (KROW / 4) * j;
       const unsigned char* ka = kr + 128 + 32 * j;
       const unsigned char* kz = kr + 256 + 64 * j;
 #pragma unroll
@@ -283,13 +324,24 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int nb = 4 * q4 + i;
-          const uint4 v4 = *reinterpret_cast<const uint4*>(kc + nb * 128);
-          const uint32_t kw[4] = {v4.x, v4.y, v4.z, v4.w};
           float c[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (KBITS == 4) {
+            const uint4 v4 = *reinterpret_cast<const uint4*>(kc + nb * 2 * KROW);
+            const uint32_t kw[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-            const uint32_t x = (kb & 1) ? (kw[kb >> 1] >> 8) : kw[kb >> 1];
-            mma_f16(c, afr[kb], field(x, 0x000F000Fu), field(x, 0x00F000F0u));
+            for (int kb = 0; kb < 8; ++kb) {
+              const uint32_t x = (kb & 1) ? (kw[kb >> 1] >> 8) : kw[kb >> 1];
+              mma_f16(c, afr[kb], field(x, 0x000F000Fu), field(x, 0x00F000F0u));
+            }
+          } else {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(kc + nb * 2 * KROW);
+            const uint32_t kw[2] = {v2.x, v2.y};
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+              const uint32_t x = ((kb >> 1) & 1) ? (kw[kb >> 2] >> 8) : kw[kb >> 2];
+              const uint32_t m0 = 0x00030003u << (4 * (kb & 1));
+              mma_f16(c, afr[kb], field(x, m0), field(x, m0 << 2));
+            }
           }
           const float2 a2 = __half22float2(e4m3x2_to_half2(((i & 2) ? a8.y : a8.x) >> (16 * (i & 1))));
           const float2 b2 = __half22float2(u2h2(bw[i]));
@@ -724,12 +776,13 @@ size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int c
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
 
-template <typename E>
+template <typename E, int KBITS>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
-  const size_t smem = sizeof(DecSmem) + 128;
-  cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(DecSmem<KBITS>) + 128;
+  cudaError_t e =
+      cudaFuncSetAttribute(decode_packed_kernel<E, KBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_packed_kernel<E><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
+  decode_packed_kernel<E, KBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
@@ -738,8 +791,11 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
-  return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16>(p, batch, out, s)
-                                   : launch_decode_t<__half>(p, batch, out, s);
+  if (p.k_bits == 2)
+    return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, 2>(p, batch, out, s)
+                                     : launch_decode_t<__half, 2>(p, batch, out, s);
+  return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, 4>(p, batch, out, s)
+                                   : launch_decode_t<__half, 4>(p, batch, out, s);
 }
 
 // ---- fixed-scratch variant of the packed decode (no allocation anywhere)

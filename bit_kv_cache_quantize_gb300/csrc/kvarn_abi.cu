@@ -10,7 +10,6 @@
 #include "params.h"
 
 namespace kvarn {
-constexpr int kHeadRec = 13312;
 constexpr int kChunkTiles = 16;  // fewest packed tiles per split-K CTA (sizes the workspace)
 
 // Packed tiles per split-K CTA for one call: 32 (longer CTAs amortise the
@@ -36,7 +35,9 @@ static kvarn_status check_config(const kvarn_config* c) {
     return KVARN_ERR_INVALID;
   if (c->num_q_heads % c->num_kv_heads) return KVARN_ERR_INVALID;
   if (c->dtype != KVARN_DTYPE_F16 && c->dtype != KVARN_DTYPE_BF16) return KVARN_ERR_INVALID;
-  if (c->head_dim != 128 || c->tile_tokens != 128 || c->k_bits != 4 || c->v_bits != 2) return KVARN_ERR_UNSUPPORTED;
+  // presets: kvarn_k4v2 (4-bit keys) and K2/V2 (2-bit keys); values are 2-bit
+  if (c->head_dim != 128 || c->tile_tokens != 128 || (c->k_bits != 4 && c->k_bits != 2) || c->v_bits != 2)
+    return KVARN_ERR_UNSUPPORTED;
   if (c->num_q_heads / c->num_kv_heads > 8) return KVARN_ERR_UNSUPPORTED;
   return KVARN_OK;
 }
@@ -50,7 +51,7 @@ extern "C" {
 
 size_t kvarn_block_bytes(const kvarn_config* cfg) {
   if (check_config(cfg) != KVARN_OK) return 0;
-  return static_cast<size_t>(cfg->num_kv_heads) * kHeadRec;
+  return static_cast<size_t>(cfg->num_kv_heads) * head_rec(cfg->k_bits);
 }
 
 size_t kvarn_tail_bytes(const kvarn_config* cfg, int32_t batch) {
@@ -85,7 +86,7 @@ kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const 
   if (static_cast<int64_t>(n_tiles) * cfg->num_kv_heads * 2 > 0x7fffffffLL) return KVARN_ERR_INVALID;
   QuantizeParams p{k, v, token_stride_elems, n_tokens, tile_first_token, tile_dst_block,
                    static_cast<unsigned char*>(block_pool), static_cast<int64_t>(kvarn_block_bytes(cfg)),
-                   cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters, dev_err};
+                   cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters, cfg->k_bits, dev_err};
   return cuda_status(launch_quantize(p, cfg->dtype, n_tiles, static_cast<cudaStream_t>(stream)));
 }
 
@@ -102,7 +103,7 @@ kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, con
     return KVARN_ERR_INVALID;
   AppendParams p{k_new, v_new, pos, block_table, max_blocks, cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters,
                  tail_pool, static_cast<unsigned char*>(block_pool), static_cast<int64_t>(kvarn_block_bytes(cfg)),
-                 dev_err};
+                 cfg->k_bits, dev_err};
   return cuda_status(launch_append(p, cfg->dtype, batch, static_cast<cudaStream_t>(stream)));
 }
 
@@ -132,7 +133,7 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
                  static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
                  max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads,
-                 cfg->num_blocks, chunk, n_chunks};
+                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits};
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -153,7 +154,7 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
   const int n_chunks = (max_blocks + chunk - 1) / chunk;
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool, nullptr, dev_err,
                  static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale, max_blocks, cfg->num_kv_heads,
-                 cfg->num_q_heads, G, cfg->num_blocks, chunk, n_chunks};
+                 cfg->num_q_heads, G, cfg->num_blocks, chunk, n_chunks, cfg->k_bits};
   return cuda_status(launch_decode_noalloc(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -168,7 +169,7 @@ kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q,
   const int n_chunks = (max_blocks + kF16ChunkTiles - 1) / kF16ChunkTiles;
   DecodeParams p{q, block_table, seq_lens, nullptr, nullptr, static_cast<float*>(workspace), dev_err, 0,
                  softmax_scale, max_blocks, cfg->num_kv_heads, cfg->num_q_heads,
-                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks};
+                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks, 16};
   cudaError_t e = launch_decode_f16(p, fp16_pool, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidValue) return KVARN_ERR_INVALID;
   if (e == cudaErrorNotSupported) return KVARN_ERR_UNSUPPORTED;
@@ -185,7 +186,7 @@ kvarn_status kvarn_dequantize(const kvarn_config* cfg, const void* block_pool, c
   if (cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
   return cuda_status(launch_dequantize(static_cast<const unsigned char*>(block_pool),
                                        static_cast<int64_t>(kvarn_block_bytes(cfg)), blocks, n, cfg->num_blocks,
-                                       cfg->num_kv_heads, out, dev_err, static_cast<cudaStream_t>(stream)));
+                                       cfg->num_kv_heads, cfg->k_bits, out, dev_err, static_cast<cudaStream_t>(stream)));
 }
 
 const char* kvarn_status_string(kvarn_status s) {

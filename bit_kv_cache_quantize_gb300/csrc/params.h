@@ -8,6 +8,12 @@
 #include <cstdint>
 
 namespace kvarn {
+// Bytes of one (tile, head) record of one role: a 512-byte header (per-channel
+// and per-token FP8 scales, per-token FP16 zero-points) + 128 x 128 codes of
+// `bits` bits; a head holds its key record then its 2-bit value record.
+__host__ __device__ constexpr int rec_bytes(int bits) { return 512 + 128 * 128 * bits / 8; }
+__host__ __device__ constexpr int head_rec(int k_bits) { return rec_bytes(k_bits) + rec_bytes(2); }
+
 struct QuantizeParams {
   const void* k;
   const void* v;
@@ -20,6 +26,7 @@ struct QuantizeParams {
   int32_t num_kv_heads;
   int32_t num_blocks;
   int32_t iters;
+  int32_t k_bits;  // 4 (kvarn_k4v2) or 2 (K2/V2); values are always 2-bit
   int32_t* err;
 };
 struct AppendParams {
@@ -34,6 +41,7 @@ struct AppendParams {
   void* tail;
   unsigned char* pool;
   int64_t block_bytes;
+  int32_t k_bits;
   int32_t* err;
 };
 struct DecodeParams {
@@ -53,11 +61,12 @@ struct DecodeParams {
   int32_t num_blocks;
   int32_t chunk_tiles;
   int32_t n_chunks;
+  int32_t k_bits;
 };
 cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStream_t s);
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
-                              int num_blocks, int num_kv_heads, float* out, int32_t* err, cudaStream_t s);
+                              int num_blocks, int num_kv_heads, int k_bits, float* out, int32_t* err, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s);
 cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* out, cudaStream_t s);
 cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,

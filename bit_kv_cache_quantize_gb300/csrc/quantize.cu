@@ -94,21 +94,28 @@ __device__ __forceinline__ float pick8(const float (&v)[8], int lane) {
   return r;
 }
 
+// Record kinds written by the quantiser.
+constexpr int KIND_K4 = 0;  // 4-bit keys, token-major nibbles (kvarn_k4v2 preset)
+constexpr int KIND_V2 = 1;  // 2-bit values, channel-major even/odd token half-words
+constexpr int KIND_K2 = 2;  // 2-bit keys, token-major, four codes per byte (K2/V2 preset)
+__host__ __device__ constexpr int kind_levels(int kind) { return kind == KIND_K4 ? 15 : 3; }
+__host__ __device__ constexpr int kind_rec_bytes(int kind) { return kind == KIND_K4 ? K_REC : V_REC; }
+
 struct AddOp { __device__ float operator()(float a, float b) const { return a + b; } };
 struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
 struct MaxOp { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
 
 // Step 6 for this thread's 8 tokens x 8 channels: code = rne((Y - b) * (1/a))
 // (two fp32 roundings, as written), clamped below at 0 when CLAMP; adding
-// 1.5 * 2^23 leaves the rounded integer in the low mantissa bits.  K: byte
-// pair p of token t = code[2p] | code[2p+1] << 4.  V: token 16w + u of a
-// channel at bit u (u even) or 15 + u (u odd) of the channel's word w;
-// tokens tok0 .. tok0+7 (u = 8h + i) fill byte h (even i, at bit i) and
-// byte 2 + h (odd i, at bit i - 1).
-template <bool IS_V, bool CLAMP>
+// 1.5 * 2^23 leaves the rounded integer in the low mantissa bits.  K4: byte
+// pair p of token t = code[2p] | code[2p+1] << 4.  K2: byte i of token t =
+// sum_k code[4i+k] << 2k.  V2: token 16w + u of a channel at bit u (u even)
+// or 15 + u (u odd) of the channel's word w; tokens tok0 .. tok0+7
+// (u = 8h + i) fill byte h (even i, at bit i) and byte 2 + h (odd i, at bit i - 1).
+template <int KIND, bool CLAMP>
 __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float2* tokv, unsigned char* rec,
                                             int tok0, int cb) {
-  constexpr int L = IS_V ? 3 : 15;
+  constexpr int L = kind_levels(KIND);
   constexpr float RNE_MAGIC = 12582912.0f;
   const float2 MAG2 = make_float2(RNE_MAGIC, RNE_MAGIC);
   auto code2 = [&](float2 y, float2 nb, float2 ia) {
@@ -121,7 +128,20 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
     q2.y = fminf(q2.y, (float)L);
     return fadd2(q2, MAG2);
   };
-  if constexpr (!IS_V) {
+  if constexpr (KIND == KIND_K2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 ta = tokv[tok0 + i];
+      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
+      uint32_t bits16 = 0;  // channels 8cb .. 8cb+7 of token tok0 + i, channel 8cb + k at bits 2k
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 q2 = code2(r[i][pp], nb, ia);
+        bits16 |= ((__float_as_uint(q2.x) & 3u) << (4 * pp)) | ((__float_as_uint(q2.y) & 3u) << (4 * pp + 2));
+      }
+      *reinterpret_cast<uint16_t*>(rec + 512 + (tok0 + i) * 32 + 2 * cb) = (uint16_t)bits16;
+    }
+  } else if constexpr (KIND == KIND_K4) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float2 ta = tokv[tok0 + i];
@@ -167,10 +187,10 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
 // pool.  All 256 threads of the CTA must call this.  After the rotation every
 // thread holds one 8-token x 8-channel block of R: tokens 16w + 8(l >> 4) +
 // 0..7, channels 8(l & 15) + 0..7 (warp w, lane l).
-template <typename E, bool IS_V>
+template <typename E, int KIND>
 __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride, unsigned char* __restrict__ dst,
                                   int iters, QSmem& sm) {
-  constexpr int L = IS_V ? 3 : 15;
+  constexpr int L = kind_levels(KIND);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, j = lane & 3;          // MMA fragment coordinates
   const int tbl = lane >> 4, cb = lane & 15;       // 8x8 block coordinates
@@ -429,10 +449,10 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
 
   // ---- 6. codes and packing: code = rne((Y - b) * (1/a)), clamped to [0, L]
   // only in a tile where some token saturated its zero-point or step
-  if (clamp_codes) encode_pack<IS_V, true>(r, tokv, rec, tok0, cb);
-  else encode_pack<IS_V, false>(r, tokv, rec, tok0, cb);
+  if (clamp_codes) encode_pack<KIND, true>(r, tokv, rec, tok0, cb);
+  else encode_pack<KIND, false>(r, tokv, rec, tok0, cb);
   __syncthreads();
-  const int bytes = IS_V ? V_REC : K_REC;
+  const int bytes = kind_rec_bytes(KIND);
   for (int i = tid; i < bytes / 16; i += 256)
     *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(rec + 16 * i);
 }
@@ -459,9 +479,10 @@ __global__ void __launch_bounds__(256, 2) quantize_tiles_kernel(QuantizeParams p
     return;
   }
   const E* src = static_cast<const E*>(kv ? prm.v : prm.k) + first * prm.token_stride + h * D;
-  unsigned char* dst = prm.pool + blk * prm.block_bytes + h * HEAD_REC + kv * K_REC;
-  if (kv) quantize_tile_cta<E, true>(src, prm.token_stride, dst, prm.iters, sm);
-  else quantize_tile_cta<E, false>(src, prm.token_stride, dst, prm.iters, sm);
+  unsigned char* dst = prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits) + kv * rec_bytes(prm.k_bits);
+  if (kv) quantize_tile_cta<E, KIND_V2>(src, prm.token_stride, dst, prm.iters, sm);
+  else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(src, prm.token_stride, dst, prm.iters, sm);
+  else quantize_tile_cta<E, KIND_K2>(src, prm.token_stride, dst, prm.iters, sm);
 }
 
 
@@ -491,9 +512,10 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
   }
   __threadfence();
   __syncthreads();
-  unsigned char* dst = prm.pool + blk * prm.block_bytes + h * HEAD_REC + kv * K_REC;
-  if (kv) quantize_tile_cta<E, true>(tile, D, dst, prm.iters, sm);
-  else quantize_tile_cta<E, false>(tile, D, dst, prm.iters, sm);
+  unsigned char* dst = prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits) + kv * rec_bytes(prm.k_bits);
+  if (kv) quantize_tile_cta<E, KIND_V2>(tile, D, dst, prm.iters, sm);
+  else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(tile, D, dst, prm.iters, sm);
+  else quantize_tile_cta<E, KIND_K2>(tile, D, dst, prm.iters, sm);
 }
 
 // Dequantise (tests): one CTA of 128 threads per (block, head, K|V); thread
@@ -501,7 +523,8 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
 // in-register fast Walsh-Hadamard transform.
 __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __restrict__ pool, int64_t block_bytes,
                                                          const int32_t* __restrict__ blocks, int32_t num_blocks,
-                                                         int32_t num_kv_heads, float* __restrict__ out, int32_t* err) {
+                                                         int32_t num_kv_heads, int32_t k_bits, float* __restrict__ out,
+                                                         int32_t* err) {
   __shared__ __align__(16) unsigned char rec[K_REC];
   const int n = blockIdx.x, h = blockIdx.y, kv = blockIdx.z, t = threadIdx.x;
   const int32_t blk = blocks[n];
@@ -509,8 +532,8 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
     if (t == 0) set_error(err, KVARN_DEV_ERR_BLOCK_RANGE);
     return;
   }
-  const unsigned char* src = pool + blk * block_bytes + h * HEAD_REC + kv * K_REC;
-  const int bytes = kv ? V_REC : K_REC;
+  const unsigned char* src = pool + blk * block_bytes + h * head_rec(k_bits) + kv * rec_bytes(k_bits);
+  const int bytes = kv ? V_REC : rec_bytes(k_bits);
   for (int i = t; i < bytes / 16; i += 128)
     reinterpret_cast<uint4*>(rec)[i] = reinterpret_cast<const uint4*>(src)[i];
   __syncthreads();
@@ -521,7 +544,8 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
   for (int c = 0; c < D; ++c) {
     const int vb = (t & 1) ? 15 + (t & 15) : (t & 15);  // bit of token t in its V word
     int code = kv ? (rec[512 + c * 32 + 4 * (t >> 4) + (vb >> 3)] >> (vb & 7)) & 3
-                  : (rec[512 + t * 64 + (c >> 1)] >> (4 * (c & 1))) & 15;
+               : k_bits == 4 ? (rec[512 + t * 64 + (c >> 1)] >> (4 * (c & 1))) & 15
+                             : (rec[512 + t * 32 + (c >> 2)] >> (2 * (c & 3))) & 3;
     x[c] = e4m3_to_float(rec[c]) * fmaf(a, static_cast<float>(code), b);
   }
 #pragma unroll
@@ -572,8 +596,9 @@ cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStrea
 }
 
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
-                              int num_blocks, int num_kv_heads, float* out, int32_t* err, cudaStream_t s) {
-  dequantize_kernel<<<dim3(n, num_kv_heads, 2), 128, 0, s>>>(pool, block_bytes, blocks, num_blocks, num_kv_heads, out, err);
+                              int num_blocks, int num_kv_heads, int k_bits, float* out, int32_t* err, cudaStream_t s) {
+  dequantize_kernel<<<dim3(n, num_kv_heads, 2), 128, 0, s>>>(pool, block_bytes, blocks, num_blocks, num_kv_heads,
+                                                              k_bits, out, err);
   return cudaGetLastError();
 }
 

@@ -116,6 +116,7 @@ class Workload:
     max_tokens: int = 0             # token stride of the generated K/V streams
     block_perm: bool = False        # physical blocks randomly permuted
     extra: dict = field(default_factory=dict)
+    k_bits: int = 4                 # key code width: 4 (kvarn_k4v2 preset) or 2 (K2/V2 preset)
 
     @property
     def G(self) -> int:

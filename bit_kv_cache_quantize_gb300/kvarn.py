@@ -18,9 +18,19 @@ LIB_PATH = os.path.join(PKG, "_build", "libkvarn.so")
 KVARN_OK, KVARN_ERR_INVALID, KVARN_ERR_UNSUPPORTED, KVARN_ERR_CUDA = 0, 1, 2, 3
 KVARN_DTYPE_F16, KVARN_DTYPE_BF16 = 0, 1
 KVARN_DEV_ERR_BLOCK_RANGE, KVARN_DEV_ERR_TOKEN_RANGE, KVARN_DEV_ERR_TIMEOUT = 1, 2, 3
-HEAD_REC = 13312
+HEAD_REC = 13312          # kvarn_k4v2: 4-bit key record + 2-bit value record
 K_REC = 8704
 V_REC = 4608
+
+
+def rec_bytes(bits: int) -> int:
+    """Bytes of one (tile, head) record of one role: 512-byte header + codes."""
+    return 512 + 128 * 128 * bits // 8
+
+
+def head_rec(k_bits: int = 4) -> int:
+    """Bytes of one head of a block: key record then 2-bit value record."""
+    return rec_bytes(k_bits) + V_REC
 
 # every function declared in include/kvarn.h
 EXPORTS = (

@@ -36,13 +36,16 @@ def f16_order(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
-def unpack(rec: np.ndarray, is_v: bool):
+def unpack(rec: np.ndarray, is_v: bool, k_bits: int = 4):
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     g8 = rec[:128].copy()
     a8 = rec[128:256].copy()
     b16 = rec[256:512].view(np.uint16).copy()
     body = rec[512:]
-    if not is_v:
+    if not is_v and k_bits == 2:
+        by = body.reshape(T, 32)                      # [token][byte]: channels 4i .. 4i+3 at bits 2k
+        code = np.stack([(by >> (2 * k)) & 3 for k in range(4)], axis=-1).reshape(T, D).astype(np.uint8)
+    elif not is_v:
         by = body.reshape(T, 64)
         code = np.empty((T, D), np.uint8)
         code[:, 0::2] = by & 15
@@ -66,10 +69,10 @@ class Stats:
                 f"b_flip={self.b_flip} tie_diff={self.tie_diff} checked_vs_own_scales={self.valid_checked}")
 
 
-def compare_record(gpu_rec: np.ndarray, tile, is_v: bool, st: Stats, where: str = ""):
+def compare_record(gpu_rec: np.ndarray, tile, is_v: bool, st: Stats, where: str = "", k_bits: int = 4):
     """tile: oracle.Tile of the same input."""
-    L = 3 if is_v else 15
-    g8, a8, b16, code = unpack(gpu_rec, is_v)
+    L = 3 if (is_v or k_bits == 2) else 15
+    g8, a8, b16, code = unpack(gpu_rec, is_v, k_bits)
     st.tiles += 1
     st.codes += code.size
     assert code.max() <= L, where

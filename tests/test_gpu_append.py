@@ -57,13 +57,13 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
             for h in range(w.num_kv_heads):
                 jobs += [(full_k[:, h], 0), (full_v[:, h], 1)]
                 keys += [(b, t, h, 0), (b, t, h, 1)]
-        tiles = oracle_tiles(jobs, w.dtype)
+        tiles = oracle_tiles(jobs, w.dtype, k_bits=w.k_bits)
         for (b, t, h, kv), tl in zip(keys, tiles):
             blk = int(c.table[b, t])
             PR.compare_record(c.record(blk, h, kv).cpu().numpy(), tl, bool(kv), st,
-                              where=f"step {s} seq {b} closed tile {t} head {h} kv {kv}")
+                              where=f"step {s} seq {b} closed tile {t} head {h} kv {kv}", k_bits=w.k_bits)
             if b in ctx:  # decode parity reads oracle records only
-                rec = O.pack_record(bool(kv), tl)
+                rec = O.pack_record(bool(kv), tl, w.k_bits)
                 recs[(b, t, h, kv)] = rec
                 c.set_record(blk, h, kv, torch.from_numpy(rec).to(dev))
         if s % attend_every and s != steps - 1:
@@ -85,7 +85,7 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
                                   ktail=O.decode16(bits(k[nf * T:n, h]), w.dtype).reshape(-1, D),
                                   vtail=O.decode16(bits(v[nf * T:n, h]), w.dtype).reshape(-1, D)))
                 ukeys.append((b, h))
-        for (b, h), o in zip(ukeys, oracle_attention_units(units, w.scale)):
+        for (b, h), o in zip(ukeys, oracle_attention_units(units, w.scale, w.k_bits)):
             worst = max(worst, np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max())
     print(w.name, PR.finish(st), f"max |gpu - oracle| = {worst:.3e}")
     assert worst <= TOL
@@ -97,6 +97,13 @@ def test_append_close_small():
                    max_tokens=310, block_perm=True)
     st = run_steps(w, 4)
     assert st.tiles == 4 * 2 * 2   # seqs 0..3 close one tile each
+
+
+def test_k2_append_close_small():
+    w = I.Workload("append_small_k2", 6, 16, 2, "f16", [125, 126, 127, 255, 300, 10], seed=47, decode_steps=4,
+                   max_tokens=310, block_perm=True, k_bits=2)
+    st = run_steps(w, 4)
+    assert st.tiles == 4 * 2 * 2
 
 
 def test_append_close_bf16():

@@ -31,9 +31,9 @@ def load_oracle_records(w, c: PagedCache, seqs, ctx):
                 for kv, src in ((0, k), (1, v)):
                     jobs.append((src[t * T:(t + 1) * T, h], kv))
                     keys.append((b, t, h, kv))
-    tiles = oracle_tiles(jobs, w.dtype)
+    tiles = oracle_tiles(jobs, w.dtype, k_bits=w.k_bits)
     for (b, t, h, kv), tl in zip(keys, tiles):
-        rec = O.pack_record(bool(kv), tl)
+        rec = O.pack_record(bool(kv), tl, w.k_bits)
         recs[(b, t, h, kv)] = rec
         c.set_record(int(c.table[b, t]), h, kv, torch.from_numpy(rec).to(c.device))
     for b in seqs:
@@ -62,7 +62,7 @@ def oracle_outputs(w, seqs, ctx, recs, q, lens=None):
                 ktail=O.decode16(bits(k[n_full * T:n, h]), w.dtype).reshape(-1, D),
                 vtail=O.decode16(bits(v[n_full * T:n, h]), w.dtype).reshape(-1, D)))
             keys.append((b, h))
-    outs = oracle_attention_units(units, w.scale)
+    outs = oracle_attention_units(units, w.scale, w.k_bits)
     return dict(zip(keys, outs))
 
 
@@ -107,6 +107,24 @@ def ragged_small():
 
 def test_ragged_tails_and_empty_sequence():
     run_decode_case(ragged_small())
+
+
+def test_k2_single_tile():
+    w = I.single_tile()
+    w.k_bits = 2
+    run_decode_case(w)
+
+
+def test_k2_qwen3_4b_layer():
+    w = I.qwen3_4b()
+    w.k_bits = 2
+    run_decode_case(w)
+
+
+def test_k2_ragged_tails_and_empty_sequence():
+    w = ragged_small()
+    w.k_bits = 2
+    run_decode_case(w)
 
 
 def test_group_sizes_bf16():
