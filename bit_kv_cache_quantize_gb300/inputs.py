@@ -169,7 +169,7 @@ def ragged_lengths(seed: int, batch: int, lo: int = 128, hi: int = 32768) -> lis
 
 
 # streams: one per tensor so K, V and queries never share random numbers
-S_K, S_V, S_Q, S_OUTL, S_PERM = 10, 11, 12, 13, 14
+S_K, S_V, S_Q, S_OUTL, S_PERM, S_MQ = 10, 11, 12, 13, 14, 15
 
 
 def outlier_gain(w: Workload, device="cpu") -> torch.Tensor:
@@ -225,6 +225,14 @@ def queries(w: Workload, step: int = 0, device="cpu") -> torch.Tensor:
     n = w.batch * w.num_q_heads * D
     idx = torch.arange(n, dtype=torch.int64, device=device) + step * n
     return to16(normal(w.seed, S_Q, idx), torch_dtype(w.dtype)).reshape(w.batch, w.num_q_heads, D)
+
+
+def multi_queries(w: Workload, n_queries: int, device="cpu") -> torch.Tensor:
+    """n_queries new query tokens per sequence and query head, N(0, 1):
+    [B, n_queries, H_q, D] 16-bit."""
+    n = w.batch * n_queries * w.num_q_heads * D
+    idx = torch.arange(n, dtype=torch.int64, device=device)
+    return to16(normal(w.seed, S_MQ, idx), torch_dtype(w.dtype)).reshape(w.batch, n_queries, w.num_q_heads, D)
 
 
 def permutation(seed: int, n: int, device="cpu") -> torch.Tensor:

@@ -235,6 +235,27 @@ def attention_folded(q, krecs, vrecs, ktail, vtail, scale, k_bits: int = 4) -> n
     return out
 
 
+def cache_values(krecs, vrecs, ktail, vtail, k_bits: int = 4):
+    """The cache as attention reads it ("Huawei's KVarN puts KV-cache
+    quantization inside vLLM's backend", section "The four-stage pipeline":
+    dequantisation at read time): the dequantised closed tiles in order, then
+    the raw open-tile tokens.  Returns K, V as [n, D] fp64."""
+    ks = [dequantize_record(False, r, k_bits) for r in krecs] + [np.asarray(ktail, np.float64).reshape(-1, D)]
+    vs = [dequantize_record(True, r, k_bits) for r in vrecs] + [np.asarray(vtail, np.float64).reshape(-1, D)]
+    return np.concatenate(ks), np.concatenate(vs)
+
+
+def causal_attention(q, K, V, scale) -> np.ndarray:
+    """Several new query tokens over a cache of n tokens: q [Q, G, D] holds
+    the G heads of each of the last Q positions n - Q .. n - 1 of K, V
+    ([n, D]); query i attends to positions 0 .. n - Q + i.  Plain softmax
+    attention (``attention``) over each prefix; returns [Q, G, D]."""
+    q = np.asarray(q, np.float64)
+    n, Q = K.shape[0], q.shape[0]
+    assert n >= Q
+    return np.stack([attention(q[i], K[:n - Q + i + 1], V[:n - Q + i + 1], scale) for i in range(Q)])
+
+
 def quantize_batch(src_bits: np.ndarray, dtype: str, first: np.ndarray, row_stride: int, is_v: bool,
                    iters: int = 8, nthreads: int | None = None, k_bits: int = 4):
     """Quantise len(first) tiles read from flat 16-bit storage; returns

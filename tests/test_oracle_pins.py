@@ -319,3 +319,62 @@ def test_batch_drivers_agree_with_single_calls():
         X = O.decode16(np.stack([flat[f + r * 8 * D: f + r * 8 * D + D] for r in range(T)]), "bf16")
         assert np.array_equal(rec[i], O.pack_record(False, O.quantize_tile(X, 15)))
     assert not flags.any()
+
+
+# ---------------------------------------------------------------- causal multi-query attention
+def _cache(n_tiles, n_tail, seed, k_bits=4):
+    rng = np.random.default_rng(seed)
+    krec = [O.pack_record(False, O.quantize_tile(key_tile(40 + seed + i), O.levels(False, k_bits)), k_bits)
+            for i in range(n_tiles)]
+    vrec = [O.pack_record(True, O.quantize_tile(rng.standard_normal((T, D)), 3)) for _ in range(n_tiles)]
+    return krec, vrec, rng.standard_normal((n_tail, D)), rng.standard_normal((n_tail, D)), rng
+
+
+def test_causal_attention_matches_torch_causal_sdpa():
+    """Against torch's scaled_dot_product_attention with an explicit causal
+    mask over the last Q positions (fp64)."""
+    krec, vrec, kt, vt, rng = _cache(2, 45, 3)
+    K, V = O.cache_values(krec, vrec, kt, vt)
+    n, Q, G = K.shape[0], 7, 3
+    q = rng.standard_normal((Q, G, D))
+    want = O.causal_attention(q, K, V, 1 / math.sqrt(D))
+    pos = torch.arange(n - Q, n)[:, None]
+    mask = torch.arange(n)[None, :] <= pos                              # [Q, n]
+    qt = torch.from_numpy(q).permute(1, 0, 2)                            # [G, Q, D]
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qt, torch.from_numpy(K)[None].expand(G, n, D), torch.from_numpy(V)[None].expand(G, n, D),
+        attn_mask=mask[None].expand(G, Q, n)).permute(1, 0, 2).numpy()
+    assert np.abs(want - ref).max() < 1e-12
+
+
+def test_causal_attention_ignores_later_tokens():
+    """Query i must not change when any token after its position changes."""
+    krec, vrec, kt, vt, rng = _cache(1, 60, 4)
+    K, V = O.cache_values(krec, vrec, kt, vt)
+    n, Q = K.shape[0], 5
+    q = rng.standard_normal((Q, 2, D))
+    base = O.causal_attention(q, K, V, 0.1)
+    for i in range(Q - 1):
+        K2, V2 = K.copy(), V.copy()
+        K2[n - Q + i + 1:] *= 50.0
+        V2[n - Q + i + 1:] += 7.0
+        assert np.array_equal(O.causal_attention(q, K2, V2, 0.1)[:i + 1], base[:i + 1])
+        # the next query sees that token: with a zero query (uniform weights
+        # over its prefix of n - Q + i + 2 tokens) the output moves by 7 / prefix
+        q0 = q.copy()
+        q0[i + 1] = 0.0
+        V3 = V.copy()
+        V3[n - Q + i + 1] += 7.0
+        moved = O.causal_attention(q0, K, V3, 0.1)[i + 1] - O.causal_attention(q0, K, V, 0.1)[i + 1]
+        assert np.abs(moved - 7.0 / (n - Q + i + 2)).max() < 1e-12
+
+
+@pytest.mark.parametrize("k_bits", [4, 2])
+def test_causal_attention_last_query_equals_decode_form(k_bits):
+    """The last query sees the whole cache: the folded decode form."""
+    krec, vrec, kt, vt, rng = _cache(3, 17, 5, k_bits)
+    K, V = O.cache_values(krec, vrec, kt, vt, k_bits)
+    q = rng.standard_normal((4, 8, D))
+    got = O.causal_attention(q, K, V, 1 / math.sqrt(D))
+    want = O.attention_folded(q[-1], krec, vrec, kt, vt, 1 / math.sqrt(D), k_bits)
+    assert np.abs(got[-1] - want).max() < 1e-9
