@@ -237,7 +237,7 @@ def run_gpu(args, rank, world):
     del c, kn, vn, qs
     torch.cuda.empty_cache()
     if not args.no_components and rank == 0:
-        res["components"] = components(dev, hbm_peak)
+        res["components"] = components(dev, hbm_peak, measured_peaks()[1])
     res["clocks"] = clk.summary()
     return res
 
@@ -312,7 +312,7 @@ def flush_l2(buf):
     buf.zero_()
 
 
-def components(dev, hbm_peak):
+def components(dev, hbm_peak, bf16_peak):
     """16K decode (packed vs 16-bit kernel) and the prefill quantiser."""
     import torch
     from bit_kv_cache_quantize_gb300 import inputs as I
@@ -346,6 +346,27 @@ def components(dev, hbm_peak):
     b_pk = decode_bytes(w.seq_lens, w)
     b_16 = sum(w.seq_lens) * w.num_kv_heads * 2 * D * 2 + w.batch * w.num_q_heads * D * 6
     assert c.check_error() == 0
+    # --- multi-query: the last 16 tokens of every sequence as causal queries
+    #     (a prefill chunk / speculative verify), one call vs 16 decode calls
+    Qn = 16
+    qm = I.multi_queries(w, Qn, device=dev)
+    om = torch.empty(w.batch, Qn, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    t_mq = timed(lambda: c.multiquery(qm, Qn, om), 20)
+    lens_i = [c.lens - (Qn - 1 - i) for i in range(Qn)]
+    qd = [qm[:, i].contiguous() for i in range(Qn)]
+    od = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    t_dq = timed(lambda: [c.decode(qd[i], od, lens=lens_i[i]) for i in range(Qn)], 5)
+    assert c.check_error() == 0
+    L = w.seq_lens[0]
+    flops = 4 * D * w.batch * w.num_q_heads * sum(L - Qn + i + 1 for i in range(Qn))
+    out["multiquery_16k"] = {
+        "workload": "qwen3_32b_decode_16k cache, last 16 tokens of each of the 32 sequences as causal queries "
+                    "(16 x 8 GQA rows = one 128-row block per KV head)",
+        "us": t_mq * 1e6, "query_tokens_per_s": w.batch * Qn / t_mq,
+        "algorithmic_tflops": flops / t_mq / 1e12, "frac_bf16_peak": flops / t_mq / 1e12 / bf16_peak,
+        "executed_over_algorithmic": 2.25, "bytes": b_pk, "GBps": b_pk / t_mq / 1e9,
+        "sixteen_decode_calls_us": t_dq * 1e6, "speedup_vs_decode_calls": t_dq / t_mq,
+    }
     out["decode_16k"] = {
         "workload": "qwen3_32b_decode_16k: 32 seqs x 16384 tokens, 64 q / 8 KV heads, fp16, permuted blocks",
         "kvarn_us": t_pk * 1e6, "kvarn_tokens_per_s": w.batch / t_pk, "kvarn_GBps": b_pk / t_pk / 1e9,
@@ -500,6 +521,13 @@ def profile_case(name, launches):
         q = I.queries(w, device=dev)
         o = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
         fn = (lambda: c.decode(q, o)) if name == "decode16k" else (lambda: c.decode_fp16(q, o))
+    elif name == "multiquery16k":
+        w = I.qwen3_32b()
+        c = PagedCache(w, dev)
+        c.prefill()
+        q = I.multi_queries(w, 16, device=dev)
+        o = torch.empty(w.batch, 16, w.num_q_heads, D, dtype=torch.float32, device=dev)
+        fn = lambda: c.multiquery(q, 16, o)
     else:
         w = I.prefill_32b()
         w.batch = 4
@@ -530,7 +558,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=16)
     ap.add_argument("--ref-seqs", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode16k", "fp16", "quantize"], default=None)
+    ap.add_argument("--profile-case", choices=["decode16k", "fp16", "quantize", "multiquery16k"], default=None)
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

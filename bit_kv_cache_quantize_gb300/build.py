@@ -15,8 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libkvarn.so")
-SOURCES = ["kvarn_abi.cu", "quantize.cu", "decode.cu"]
-HEADERS = ["common.cuh", "params.h"]
+SOURCES = ["kvarn_abi.cu", "quantize.cu", "decode.cu", "multiquery.cu"]
+HEADERS = ["common.cuh", "tcgen05.cuh", "params.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"] + ARCH

@@ -78,6 +78,16 @@ class PagedCache:
                                  self.w.batch, self.pool, self.tail, self.w.scale, out, self.ws, self.ws_bytes,
                                  self.err, stream)
 
+    def multiquery(self, q, n_queries, out, lens=None, stream=None):
+        """q [B][n_queries][Hq][D]: the last n_queries tokens of each sequence
+        attend causally to the cache (workspace grown on first use)."""
+        need = K.kvarn_multiquery_workspace_bytes(self.cfg, self.w.batch, self.max_blocks, n_queries)
+        if getattr(self, "mq_ws", None) is None or self.mq_ws.numel() * 4 < need:
+            self.mq_ws = torch.empty(need // 4 + 4, dtype=torch.float32, device=self.device)
+        K.kvarn_multiquery_attention(self.cfg, q, n_queries, self.table, self.max_blocks,
+                                     self.lens if lens is None else lens, self.w.batch, self.pool, self.tail,
+                                     self.w.scale, out, self.mq_ws, self.mq_ws.numel() * 4, self.err, stream)
+
     def decode_fp16(self, q, out, lens=None, stream=None):
         K.kvarn_fp16_decode_attention(self.cfg, q, self.table, self.max_blocks, self.lens if lens is None else lens,
                                       self.w.batch, self.pool16, self.w.scale, out, self.ws, self.ws_bytes,

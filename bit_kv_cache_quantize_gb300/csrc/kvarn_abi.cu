@@ -137,6 +137,52 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
+// Packed tiles per split-K CTA of the multi-query kernel (one CTA per SM):
+// 32 while that leaves at least three waves, else 16 (sizes the workspace).
+static int choose_mq_chunk(int units, int max_blocks) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return kChunkTiles;
+  const long long ctas = (long long)units * ((max_blocks + 31) / 32);
+  return ctas >= 3LL * sms ? 32 : kChunkTiles;
+}
+
+static int mq_rowblocks(const kvarn_config* cfg, int n_queries) {
+  const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  return (n_queries * G + 127) / 128;
+}
+
+size_t kvarn_multiquery_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks,
+                                        int32_t n_queries) {
+  if (check_config(cfg) != KVARN_OK || batch < 0 || max_blocks < 1 || n_queries < 1 || n_queries > 4096) return 0;
+  return multiquery_ws_bytes(batch, cfg->num_kv_heads, mq_rowblocks(cfg, n_queries), max_blocks, kChunkTiles);
+}
+
+kvarn_status kvarn_multiquery_attention(const kvarn_config* cfg, const void* q, int32_t n_queries,
+                                        const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                                        int32_t batch, const void* block_pool, const void* tail_pool,
+                                        float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_err, void* stream) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (batch < 0 || max_blocks < 1 || batch > 65535 || n_queries < 1 || n_queries > 4096) return KVARN_ERR_INVALID;
+  if (batch == 0) return KVARN_OK;
+  if (!q || !block_table || !seq_lens || !block_pool || !tail_pool || !out || !workspace) return KVARN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(block_pool) || !aligned16(tail_pool) || !aligned16(out) || !aligned16(workspace))
+    return KVARN_ERR_INVALID;
+  if (workspace_bytes < kvarn_multiquery_workspace_bytes(cfg, batch, max_blocks, n_queries)) return KVARN_ERR_INVALID;
+  const int n_rb = mq_rowblocks(cfg, n_queries);
+  if ((long long)cfg->num_kv_heads * n_rb > 65535) return KVARN_ERR_UNSUPPORTED;
+  const int chunk = choose_mq_chunk(batch * cfg->num_kv_heads * n_rb, max_blocks);
+  const int n_chunks = (max_blocks + chunk - 1) / chunk;
+  MQParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
+             static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
+             max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks,
+             n_queries, n_rb, chunk, n_chunks, cfg->k_bits};
+  return cuda_status(launch_multiquery(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
+}
+
 kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void* q, const int32_t* block_table,
                                             int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
                                             const void* block_pool, const void* tail_pool, float softmax_scale,

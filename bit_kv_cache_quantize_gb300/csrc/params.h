@@ -63,6 +63,31 @@ struct DecodeParams {
   int32_t n_chunks;
   int32_t k_bits;
 };
+// Multi-query causal attention: n_queries query tokens per sequence at the
+// last n_queries positions, grouped with their GQA heads into row blocks of
+// 128 (query, head-in-group) rows per KV head.
+struct MQParams {
+  const void* q;  // [batch][n_queries][num_q_heads][128]
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const unsigned char* pool;
+  const void* tail;
+  float* ws;
+  int32_t* err;
+  int64_t block_bytes;
+  float scale;
+  int32_t max_blocks;
+  int32_t num_kv_heads;
+  int32_t num_q_heads;
+  int32_t G;
+  int32_t num_blocks;
+  int32_t n_queries;
+  int32_t n_rowblocks;
+  int32_t chunk_tiles;
+  int32_t n_chunks;
+  int32_t k_bits;
+};
+
 cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStream_t s);
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
@@ -71,6 +96,8 @@ cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* ou
 cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* out, cudaStream_t s);
 cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,
                               cudaStream_t s);
+cudaError_t launch_multiquery(const MQParams& p, int dtype, int batch, float* out, cudaStream_t s);
+size_t multiquery_ws_bytes(int batch, int num_kv_heads, int n_rowblocks, int max_blocks, int chunk_tiles);
 size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int chunk_tiles);
 
 }  // namespace kvarn

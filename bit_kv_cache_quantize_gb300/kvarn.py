@@ -37,7 +37,7 @@ EXPORTS = (
     "kvarn_block_bytes", "kvarn_tail_bytes", "kvarn_quantize_tiles", "kvarn_append_tokens",
     "kvarn_decode_workspace_bytes", "kvarn_decode_attention", "kvarn_dequantize",
     "kvarn_fp16_block_bytes", "kvarn_fp16_decode_attention", "kvarn_status_string",
-    "kvarn_decode_attention_noalloc",
+    "kvarn_decode_attention_noalloc", "kvarn_multiquery_workspace_bytes", "kvarn_multiquery_attention",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
             "kvarn_fp16_decode_attention": (i32, [C, P, P, i32, P, i32, P, f32, P, P, sz, P, P]),
             "kvarn_decode_attention_noalloc": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, P]),
             "kvarn_dequantize": (i32, [C, P, P, i32, P, P, P]),
+            "kvarn_multiquery_workspace_bytes": (sz, [C, i32, i32, i32]),
+            "kvarn_multiquery_attention": (i32, [C, P, i32, P, i32, P, i32, P, P, f32, P, P, sz, P, P]),
             "kvarn_status_string": (ctypes.c_char_p, [i32]),
         }
         for name, (res, args) in sig.items():
@@ -169,6 +171,22 @@ def kvarn_decode_attention_noalloc(cfg, q, block_table, max_blocks, seq_lens, ba
                                               _p(seq_lens), int(batch), _p(block_pool), _p(tail_pool),
                                               float(softmax_scale), _p(out), _p(dev_err), _s(stream))
     return _check(st, "kvarn_decode_attention_noalloc", check)
+
+
+def kvarn_multiquery_workspace_bytes(cfg, batch: int, max_blocks: int, n_queries: int) -> int:
+    return int(lib().kvarn_multiquery_workspace_bytes(ctypes.byref(cfg), batch, max_blocks, n_queries))
+
+
+def kvarn_multiquery_attention(cfg, q, n_queries, block_table, max_blocks, seq_lens, batch, block_pool, tail_pool,
+                               softmax_scale, out, workspace, workspace_bytes, dev_err, stream=None,
+                               check=True) -> int:
+    """Causal attention of the last n_queries tokens of every sequence over
+    the packed cache + open tile (see include/kvarn.h)."""
+    st = lib().kvarn_multiquery_attention(ctypes.byref(cfg), _p(q), int(n_queries), _p(block_table), int(max_blocks),
+                                          _p(seq_lens), int(batch), _p(block_pool), _p(tail_pool),
+                                          float(softmax_scale), _p(out), _p(workspace), int(workspace_bytes),
+                                          _p(dev_err), _s(stream))
+    return _check(st, "kvarn_multiquery_attention", check)
 
 
 def kvarn_fp16_decode_attention(cfg, q, block_table, max_blocks, seq_lens, batch, fp16_pool, softmax_scale, out,

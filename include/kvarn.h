@@ -182,6 +182,41 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
                                     float* out, void* workspace, size_t workspace_bytes,
                                     int32_t* dev_err, void* stream);
 
+/* Workspace bytes kvarn_multiquery_attention needs for this batch, table
+ * width and query count (split-K partial rows).  0 if invalid. */
+size_t kvarn_multiquery_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks,
+                                        int32_t n_queries);
+
+/*
+ * Causal attention of several new query tokens per sequence over the packed
+ * paged cache plus the raw open tile: the read side of the pages' pipeline
+ * ("Huawei's KVarN puts KV-cache quantization inside vLLM's backend",
+ * section "The four-stage pipeline": dequantisation at read time inside
+ * attention) for a chunk of prefill or a speculative step that verifies
+ * several draft tokens.  The caller has already appended the n_queries new
+ * tokens (kvarn_append_tokens, kvarn_quantize_tiles), so sequence s holds
+ * seq_lens[s] tokens laid out as for kvarn_decode_attention.  Query i of
+ * sequence s sits at position seq_lens[s] - n_queries + i and attends to the
+ * tokens at positions 0 .. seq_lens[s] - n_queries + i:
+ *   out[s][i][j] = softmax(scale * q[s][i][j] K[0..pos]^T) V[0..pos].
+ *
+ *  q           device, 16-bit (cfg->dtype) [batch][n_queries][num_q_heads][128].
+ *  n_queries   1 .. 4096.
+ *  seq_lens    device int32[batch]; each must satisfy n_queries <= seq_lens[s]
+ *              <= 128 * max_blocks, else KVARN_DEV_ERR_TOKEN_RANGE is stored
+ *              and the rows of s are zero.
+ *  out         device float32 [batch][n_queries][num_q_heads][128].
+ *  workspace   device, >= kvarn_multiquery_workspace_bytes(cfg, batch,
+ *              max_blocks, n_queries).
+ * Other arguments as kvarn_decode_attention.  The query rows of a KV head
+ * (n_queries x group size) run in blocks of 128 on the tensor cores.
+ */
+kvarn_status kvarn_multiquery_attention(const kvarn_config* cfg, const void* q, int32_t n_queries,
+                                        const int32_t* block_table, int32_t max_blocks, const int32_t* seq_lens,
+                                        int32_t batch, const void* block_pool, const void* tail_pool,
+                                        float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_err, void* stream);
+
 /* Size of the fixed device scratch used by kvarn_decode_attention_noalloc. */
 #define KVARN_NOALLOC_SCRATCH_BYTES (16u << 20)
 

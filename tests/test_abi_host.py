@@ -87,3 +87,25 @@ def test_argument_validation_is_host_side(lib):
     assert K.kvarn_status_string(K.KVARN_ERR_UNSUPPORTED) == "unsupported configuration"
     with pytest.raises(K.KvarnError):
         K.kvarn_dequantize(cfg, 16, 16, -1, 16, 16, stream=0)
+
+
+def test_multiquery_sizes_and_validation(lib):
+    cfg = K.make_config(8, 64, 100, "f16")
+    # 16 queries x 8 heads = one row block; 2 sequences, 40 blocks -> 16-tile chunks (3 + the open tile)
+    assert K.kvarn_multiquery_workspace_bytes(cfg, 2, 40, 16) == 2 * 8 * 1 * (3 + 1) * 128 * 132 * 4
+    assert K.kvarn_multiquery_workspace_bytes(cfg, 2, 40, 17) == 2 * 8 * 2 * (3 + 1) * 128 * 132 * 4
+    assert K.kvarn_multiquery_workspace_bytes(cfg, 2, 40, 0) == 0
+    assert K.kvarn_multiquery_workspace_bytes(cfg, 2, 40, 4097) == 0
+    ws = K.kvarn_multiquery_workspace_bytes(cfg, 2, 4, 3)
+    mq = lambda **kw: K.kvarn_multiquery_attention(
+        cfg, kw.get("q", 16), kw.get("nq", 3), 16, kw.get("mb", 4), 16, kw.get("batch", 2), 16, kw.get("tail", 16),
+        0.1, 16, 16, kw.get("ws", ws), 16, stream=0, check=False)
+    assert mq(batch=0, q=None) == 0                      # nothing to do
+    assert mq(nq=0) == K.KVARN_ERR_INVALID
+    assert mq(ws=ws - 4) == K.KVARN_ERR_INVALID
+    assert mq(q=17) == K.KVARN_ERR_INVALID                # misaligned
+    assert mq(tail=None) == K.KVARN_ERR_INVALID
+    assert mq(mb=0) == K.KVARN_ERR_INVALID
+    bad = K.make_config(8, 64, 100, "f16", k_bits=3)
+    assert K.kvarn_multiquery_attention(bad, 16, 3, 16, 4, 16, 2, 16, 16, 0.1, 16, 16, ws, 16, stream=0,
+                                        check=False) == K.KVARN_ERR_UNSUPPORTED
