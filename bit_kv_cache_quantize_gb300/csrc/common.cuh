@@ -134,6 +134,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// Bounded wait in which the hardware may park the thread until the phase
+// completes (try_wait with a suspend-time hint of 0.2 ms) instead of
+// re-polling; false (and the error word set) after about 2 s.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_wait_parked(uint64_t* bar, uint32_t parity, int32_t* err) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(200000u)
+        : "memory");
+    if (ok) return true;
+    if (global_ns() - t0 > 2000000000ull) break;
+  }
+  set_error(err, KVARN_DEV_ERR_TIMEOUT);
+  return false;
+}
+
 // 2^x, flushing results below the normal range to zero (PTX ex2.approx.ftz).
 __device__ __forceinline__ float ex2_ftz(float x) {
   float y;

@@ -51,9 +51,12 @@ constexpr int VT_BYTES = D * VT_K * 2;       // V~, bf16, K-major core matrices
 constexpr int QA_BYTES = MQ_ROWS * D * 2;
 constexpr int REC_STAGES = 3;
 // tensor-memory columns: accumulator O, then two score buffers S (144 each).
-// Once a tile's scores are in registers, its P~ operand overwrites the same
-// buffer: hi at +0 (72 columns with beta), lo at +72 (64 columns).
-constexpr uint32_t TM_O = 0, TM_S = 128, TM_SSTRIDE = 144, TM_PH = 0, TM_PL = 72, TM_COLS = 512;
+// The softmax overwrites a tile's scores in place, first with the scaled
+// scores, then with the P~ operand: for tokens 16 j .. 16 j + 15 the bf16 hi
+// parts go to columns 16 j .. 16 j + 7 and the lo parts to 16 j + 8 .. 16 j + 15
+// (exactly the columns those tokens' scores occupied); columns 128..135 take
+// the beta entries (k 128..143).
+constexpr uint32_t TM_O = 0, TM_S = 128, TM_SSTRIDE = 144, TM_COLS = 512;
 constexpr uint32_t TM_QA = 416;  // Q' hi (the A operand of the first QK pass), 64 columns
 constexpr uint32_t IDESC_QK = umma_idesc(128, KT_ROWS, 0);
 constexpr uint32_t IDESC_PV = umma_idesc(128, D, 1);
@@ -143,7 +146,7 @@ __device__ __forceinline__ void mq_block_extent(const MQParams& p, int rb, int l
 
 // Warp-uniform bounded wait: every lane waits, all report failure together.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int32_t* err) {
-  const bool ok = mbar_wait_bounded(bar, parity, err);
+  const bool ok = mbar_wait_parked(bar, parity, err);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -558,30 +561,30 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       auto issue_pv = [&](int k) {  // D_O += P~ V~^T over the hi (with beta) then the lo halves
         const uint32_t vb = smem_u32(sm.vt), pa = tmem + TM_S + TM_SSTRIDE * (k & 1);
 #pragma unroll
-        for (int kk = 0; kk < 9; ++kk)
-          umma_ts(tmem + TM_O, pa + TM_PH + 8 * kk, umma_desc(vb + 256 * kk, 128, VT_K * 16), IDESC_PV,
+        for (int kk = 0; kk < 9; ++kk)  // hi parts of tokens 16 kk .. 16 kk + 15, then the beta block
+          umma_ts(tmem + TM_O, pa + 16 * kk, umma_desc(vb + 256 * kk, 128, VT_K * 16), IDESC_PV,
                   (k > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + TM_O, pa + TM_PL + 8 * kk, umma_desc(vb + 256 * kk, 128, VT_K * 16), IDESC_PV, 1);
+        for (int kk = 0; kk < 8; ++kk)  // lo parts
+          umma_ts(tmem + TM_O, pa + 16 * kk + 8, umma_desc(vb + 256 * kk, 128, VT_K * 16), IDESC_PV, 1);
         umma_commit(&sm.pv_done);
       };
       bool ok = true;
       for (int k = 0; k < min(n_tiles, REC_STAGES); ++k) issue_rec(k);
       for (int k = 0; ok && k < min(n_tiles, 2); ++k) {  // both score buffers start free
-        ok = mbar_wait_bounded(&sm.kt_full[k], 0, p.err);
+        ok = mbar_wait_parked(&sm.kt_full[k], 0, p.err);
         if (!ok) break;
         tc_fence_after();
         issue_qk(k);
       }
       for (int k = 0; ok && k < n_tiles; ++k) {
-        ok = mbar_wait_bounded(&sm.p_full[k & 1], (k >> 1) & 1, p.err) && mbar_wait_bounded(&sm.vt_full, k & 1, p.err);
+        ok = mbar_wait_parked(&sm.p_full[k & 1], (k >> 1) & 1, p.err) && mbar_wait_parked(&sm.vt_full, k & 1, p.err);
         if (!ok) break;
         tc_fence_after();
         issue_pv(k);
         if (k + 2 < n_tiles) {  // buffer k & 1 is free once PV(k) has read its P~
-          ok = mbar_wait_bounded(&sm.kt_full[k & 1], ((k + 2) >> 1) & 1, p.err) &&
-               mbar_wait_bounded(&sm.pv_done, k & 1, p.err);
+          ok = mbar_wait_parked(&sm.kt_full[k & 1], ((k + 2) >> 1) & 1, p.err) &&
+               mbar_wait_parked(&sm.pv_done, k & 1, p.err);
           if (!ok) break;
           tc_fence_after();
           issue_qk(k + 2);
@@ -589,7 +592,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       }
       // every MMA this thread issued has finished before the memory is released
       umma_commit(&sm.fin);
-      mbar_wait_bounded(&sm.fin, 0, p.err);
+      mbar_wait_parked(&sm.fin, 0, p.err);
     }
     __syncwarp();
   } else if (warp >= 8) {
@@ -639,13 +642,13 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
         mbar_arrive(&sm.vt_full);
         mbar_arrive(&sm.rec_empty[k % REC_STAGES]);
         if (pth == 0 && k + REC_STAGES < n_tiles) {  // every producer is done with this stage: refill it
-          if (mbar_wait_bounded(&sm.rec_empty[k % REC_STAGES], (k / REC_STAGES) & 1, p.err)) issue_rec(k + REC_STAGES);
+          if (mbar_wait_parked(&sm.rec_empty[k % REC_STAGES], (k / REC_STAGES) & 1, p.err)) issue_rec(k + REC_STAGES);
         }
       }
     }
     // copies still in flight (an early exit) land before the CTA ends
     if (!ok && pth == 0) {
-      for (int k = 0; k < n_tiles; ++k) mbar_wait_bounded(&sm.rec_full[k % REC_STAGES], (k / REC_STAGES) & 1, p.err);
+      for (int k = 0; k < n_tiles; ++k) mbar_wait_parked(&sm.rec_full[k % REC_STAGES], (k / REC_STAGES) & 1, p.err);
     }
   } else {
     // ------------------------------------------------------------ softmax: row r, tokens 64 half .. +63
@@ -660,51 +663,54 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       const uint32_t sb = lane_base + TM_S + TM_SSTRIDE * s;  // this tile's score / P~ buffer
       if (!wait_all(&sm.s_full[s], (k >> 1) & 1, p.err)) { dead = true; break; }
       tc_fence_after();
-      float sv[64];
+      // pass 1: scores s = aK D_t + bK D_128 (units of 1 / cr) of this half's 64
+      // tokens, written back in place, and their maximum; masked tokens -> -inf
       float d128;
       {
-        uint32_t d[16], e[16], f[16], g[16], d1;
-        tmem_ld16(sb + 64 * half, d);
-        tmem_ld16(sb + 64 * half + 16, e);
-        tmem_ld16(sb + 64 * half + 32, f);
-        tmem_ld16(sb + 64 * half + 48, g);
+        uint32_t d1;
         tmem_ld1(sb + 128, d1);
         tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          sv[i] = __uint_as_float(d[i]);
-          sv[16 + i] = __uint_as_float(e[i]);
-          sv[32 + i] = __uint_as_float(f[i]);
-          sv[48 + i] = __uint_as_float(g[i]);
-        }
         d128 = __uint_as_float(d1);
       }
-      tc_fence_before();  // both halves read their scores before either writes P~ (ordered by xbar)
       // the scales of this tile (written with its K~; that phase is complete)
       if (!wait_all(&sm.kt_full[s], (k >> 1) & 1, p.err)) { dead = true; break; }
-      // scores (units of 1 / cr) and the half-row maximum; masked tokens -> -inf
       const int t0 = (first + k) * T + 64 * half;
       const int nvis = ((vmask >> k) & 1u) ? min(64, pos - t0 + 1) : 0;  // tokens of this half the row sees
       const float2 d2 = make_float2(d128, d128);
       float tmax = -INFINITY;
-      const float4* ka4 = reinterpret_cast<const float4*>(sm.ka[s] + 64 * half);
-      const float4* kb4 = reinterpret_cast<const float4*>(sm.kb[s] + 64 * half);
+#pragma unroll 1
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t d[16];
+        tmem_ld16(sb + 64 * half + c, d);
+        const float4* ka4 = reinterpret_cast<const float4*>(sm.ka[s] + 64 * half + c);
+        const float4* kb4 = reinterpret_cast<const float4*>(sm.kb[s] + 64 * half + c);
+        float4 a4[4], b4[4];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 a = ka4[j], bb = kb4[j];
-        float2 s01 = ffma2(make_float2(a.x, a.y), make_float2(sv[4 * j], sv[4 * j + 1]),
-                           fmul2(make_float2(bb.x, bb.y), d2));
-        float2 s23 = ffma2(make_float2(a.z, a.w), make_float2(sv[4 * j + 2], sv[4 * j + 3]),
-                           fmul2(make_float2(bb.z, bb.w), d2));
-        if (nvis < 64) {
-          if (4 * j >= nvis) s01.x = -INFINITY;
-          if (4 * j + 1 >= nvis) s01.y = -INFINITY;
-          if (4 * j + 2 >= nvis) s23.x = -INFINITY;
-          if (4 * j + 3 >= nvis) s23.y = -INFINITY;
+        for (int j = 0; j < 4; ++j) { a4[j] = ka4[j]; b4[j] = kb4[j]; }
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float2 s01 = ffma2(make_float2(a4[j].x, a4[j].y),
+                             make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
+                             fmul2(make_float2(b4[j].x, b4[j].y), d2));
+          float2 s23 = ffma2(make_float2(a4[j].z, a4[j].w),
+                             make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                             fmul2(make_float2(b4[j].z, b4[j].w), d2));
+          const int t = c + 4 * j;
+          if (nvis < 64) {
+            if (t >= nvis) s01.x = -INFINITY;
+            if (t + 1 >= nvis) s01.y = -INFINITY;
+            if (t + 2 >= nvis) s23.x = -INFINITY;
+            if (t + 3 >= nvis) s23.y = -INFINITY;
+          }
+          tmax = fmaxf(tmax, fmaxf(fmaxf(s01.x, s01.y), fmaxf(s23.x, s23.y)));
+          d[4 * j] = __float_as_uint(s01.x); d[4 * j + 1] = __float_as_uint(s01.y);
+          d[4 * j + 2] = __float_as_uint(s23.x); d[4 * j + 3] = __float_as_uint(s23.y);
         }
-        sv[4 * j] = s01.x; sv[4 * j + 1] = s01.y; sv[4 * j + 2] = s23.x; sv[4 * j + 3] = s23.y;
-        tmax = fmaxf(tmax, fmaxf(fmaxf(s01.x, s01.y), fmaxf(s23.x, s23.y)));
+        tmem_st16(sb + 64 * half + c, d);
       }
+      tmem_wait_st();
+      tc_fence_before();  // both halves read D_128 before either writes beta (ordered by xbar)
       // the row maximum: exchange with the other half through shared memory
       sm.xmax[k & 1][half][r] = tmax;
       mbar_arrive(&sm.xbar[k & 1]);
@@ -735,44 +741,49 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
           tmem_st16(lane_base + TM_O + 64 * half + c, d);
         }
       }
+      // pass 2: P~ = p aV (bf16 hi, lo) over the scores of each 16-token group,
+      // l += sum p, beta += sum p bV
       const float2 nm2 = make_float2(-m_ref, -m_ref);
-      const float4* va4 = reinterpret_cast<const float4*>(sm.va[s] + 64 * half);
-      const float4* vb4 = reinterpret_cast<const float4*>(sm.vb[s] + 64 * half);
       float2 lt = make_float2(0.f, 0.f), bt = make_float2(0.f, 0.f);
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 64; c += 16) {
-        uint32_t ph[8], pl[8];
+        uint32_t d[16];
+        tmem_ld16(sb + 64 * half + c, d);
+        const float4* va4 = reinterpret_cast<const float4*>(sm.va[s] + 64 * half + c);
+        const float4* vb4 = reinterpret_cast<const float4*>(sm.vb[s] + 64 * half + c);
+        float4 a4[4], b4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) { a4[j] = va4[j]; b4[j] = vb4[j]; }
+        tmem_wait_ld();
+        uint32_t pw[16];  // hi words 0..7, lo words 8..15
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int t = c + 4 * j;
-          const float4 a = va4[t >> 2], bb = vb4[t >> 2];
-          const float2 e01 = ffma2(cr2, make_float2(sv[t], sv[t + 1]), nm2);
-          const float2 e23 = ffma2(cr2, make_float2(sv[t + 2], sv[t + 3]), nm2);
+          const float2 e01 = ffma2(cr2, make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), nm2);
+          const float2 e23 = ffma2(cr2, make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), nm2);
           float2 p01 = make_float2(ex2_ftz(e01.x), ex2_ftz(e01.y)), p23 = make_float2(ex2_ftz(e23.x), ex2_ftz(e23.y));
           if (!live) p01 = p23 = make_float2(0.f, 0.f);
           lt = fadd2(lt, fadd2(p01, p23));
-          bt = ffma2(p01, make_float2(bb.x, bb.y), ffma2(p23, make_float2(bb.z, bb.w), bt));
-          const float2 x01 = fmul2(p01, make_float2(a.x, a.y)), x23 = fmul2(p23, make_float2(a.z, a.w));
+          bt = ffma2(p01, make_float2(b4[j].x, b4[j].y), ffma2(p23, make_float2(b4[j].z, b4[j].w), bt));
+          const float2 x01 = fmul2(p01, make_float2(a4[j].x, a4[j].y)), x23 = fmul2(p23, make_float2(a4[j].z, a4[j].w));
           const __nv_bfloat162 h01 = __floats2bfloat162_rn(x01.x, x01.y), h23 = __floats2bfloat162_rn(x23.x, x23.y);
           const float2 r01 = fadd2(x01, fmul2(__bfloat1622float2(h01), make_float2(-1.f, -1.f)));
           const float2 r23 = fadd2(x23, fmul2(__bfloat1622float2(h23), make_float2(-1.f, -1.f)));
-          ph[2 * j] = b2u(h01);
-          ph[2 * j + 1] = b2u(h23);
-          pl[2 * j] = b2u(__floats2bfloat162_rn(r01.x, r01.y));
-          pl[2 * j + 1] = b2u(__floats2bfloat162_rn(r23.x, r23.y));
+          pw[2 * j] = b2u(h01);
+          pw[2 * j + 1] = b2u(h23);
+          pw[8 + 2 * j] = b2u(__floats2bfloat162_rn(r01.x, r01.y));
+          pw[8 + 2 * j + 1] = b2u(__floats2bfloat162_rn(r23.x, r23.y));
         }
-        tmem_st8(sb + TM_PH + 32 * half + (c >> 1), ph);
-        tmem_st8(sb + TM_PL + 32 * half + (c >> 1), pl);
+        tmem_st16(sb + 64 * half + c, pw);
       }
       l_sum += lt.x + lt.y;
       {
         const float beta = bt.x + bt.y;
         const __nv_bfloat16 bh = __float2bfloat16_rn(beta);
         const __nv_bfloat16 bl = __float2bfloat16_rn(beta - __bfloat162float(bh));
-        tmem_st1(sb + TM_PH + 64 + half, (uint32_t)__bfloat16_as_ushort(bh) | ((uint32_t)__bfloat16_as_ushort(bl) << 16));
-        if (half) {  // k 132..143 of the hi operand are zero
-          tmem_st2(sb + TM_PH + 66, 0u, 0u);
-          tmem_st4(sb + TM_PH + 68, 0u, 0u, 0u, 0u);
+        tmem_st1(sb + 128 + half, (uint32_t)__bfloat16_as_ushort(bh) | ((uint32_t)__bfloat16_as_ushort(bl) << 16));
+        if (half) {  // k 132..143 of the beta block are zero
+          tmem_st2(sb + 130, 0u, 0u);
+          tmem_st4(sb + 132, 0u, 0u, 0u, 0u);
         }
       }
       tmem_wait_st();
