@@ -65,6 +65,9 @@ def lib():
         L.ora_pack_record.argtypes = [i32, P, P, P, P, P]
         L.ora_unpack_record.argtypes = [i32, P, P, P, P, P]
         L.ora_dequantize_record.argtypes = [i32, P, P]
+        L.ora_quantize_tile_ex.restype = i32
+        L.ora_quantize_tile_ex.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, P]
+        L.ora_dequantize_record_ex.argtypes = [i32, P, i32, P]
         L.ora_attention.argtypes = [P, i32, P, P, i32, dbl, P]
         L.ora_attention_folded.argtypes = [P, i32, P, P, i32, P, P, i32, dbl, i32, P]
         L.ora_quantize_batch.argtypes = [P, i32, P, i64, i32, i32, i32, P, P, i32]
@@ -156,12 +159,14 @@ class Tile:
         return self.b16.view(np.float16).astype(np.float64)
 
 
-def quantize_tile(X: np.ndarray, levels: int, iters: int = 8) -> Tile:
+def quantize_tile(X: np.ndarray, levels: int, iters: int = 8, rotate: bool = True) -> Tile:
+    """rotate=False quantises X itself (the no-rotation ablation)."""
     X = np.ascontiguousarray(X, dtype=np.float64)
     assert X.shape == (T, D)
     g8 = np.empty(D, np.uint8); a8 = np.empty(T, np.uint8); b16 = np.empty(T, np.uint16)
     code = np.empty((T, D), np.uint8); pre = np.empty((T, D)); R = np.empty((T, D)); v = np.empty(D)
-    f = lib().ora_quantize_tile(_p(X), levels, iters, _p(g8), _p(a8), _p(b16), _p(code), _p(pre), _p(R), _p(v))
+    f = lib().ora_quantize_tile_ex(_p(X), levels, iters, 1 if rotate else 0, _p(g8), _p(a8), _p(b16), _p(code),
+                                   _p(pre), _p(R), _p(v))
     return Tile(g8, a8, b16, code, pre, R, v, f)
 
 
@@ -198,11 +203,23 @@ def unpack_record(is_v: bool, rec: np.ndarray, k_bits: int = 4):
     return g8, a8, b16, code
 
 
-def dequantize_record(is_v: bool, rec: np.ndarray, k_bits: int = 4) -> np.ndarray:
+def dequantize_record(is_v: bool, rec: np.ndarray, k_bits: int = 4, rotate: bool = True) -> np.ndarray:
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     out = np.empty((T, D))
-    lib().ora_dequantize_record(kind(is_v, k_bits), _p(rec), _p(out))
+    lib().ora_dequantize_record_ex(kind(is_v, k_bits), _p(rec), 1 if rotate else 0, _p(out))
     return out
+
+
+def token_errors(X: np.ndarray, is_v: bool, k_bits: int = 4, iters: int = 8, rotate: bool = True):
+    """Per-token reconstruction error of one tile ("Huawei's KVarN puts
+    KV-cache quantization inside vLLM's backend", section "Why KV-cache
+    quantization degrades under autoregressive decoding": per-token errors):
+    quantise, pack, dequantise, then for each token t
+      err2[t] = sum_c (Xhat[t][c] - X[t][c])^2,  norm2[t] = sum_c X[t][c]^2."""
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    tl = quantize_tile(X, levels(is_v, k_bits), iters, rotate)
+    Xh = dequantize_record(is_v, pack_record(is_v, tl, k_bits), k_bits, rotate)
+    return ((Xh - X) ** 2).sum(axis=1), (X ** 2).sum(axis=1)
 
 
 # ---------------------------------------------------------------- attention

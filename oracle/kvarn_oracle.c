@@ -256,15 +256,38 @@ void ora_sinkhorn(const double *R, int iters, double *u, double *v)
  * codes, b16[T] FP16 bits, code[T][D] (token-major), and optionally the fp64
  * pre-rounding value (Y - b) / a of every code (pre[T][D]), the rotated tile
  * (Rout[T][D]) and the centred column log-factors (vout[D]).  Returns flags. */
+int ora_quantize_tile_ex(const double *X, int levels, int iters, int rotate,
+                         uint8_t *g8, uint8_t *a8, uint16_t *b16, uint8_t *code,
+                         double *pre, double *Rout, double *vout);
+void ora_dequantize_record_ex(int kind, const uint8_t *rec, int rotate, double *Xhat);
+
 int ora_quantize_tile(const double *X, int levels, int iters,
                       uint8_t *g8, uint8_t *a8, uint16_t *b16, uint8_t *code,
                       double *pre, double *Rout, double *vout)
+{
+    return ora_quantize_tile_ex(X, levels, iters, 1, g8, a8, b16, code, pre, Rout, vout);
+}
+
+/* The same steps with the rotation optional: rotate = 0 quantises X itself
+ * (R = X).  With iters = 0 as well the tile gets plain per-token asymmetric
+ * round-to-nearest under unit channel scales.  These are the ablations of the
+ * per-token error study ("Huawei's KVarN puts KV-cache quantization inside
+ * vLLM's backend", section "Why KV-cache quantization degrades under
+ * autoregressive decoding": the largest 5% of per-token errors drive the
+ * accuracy loss; section "The four-stage pipeline": rotation and variance
+ * normalisation are the stages that shrink them). */
+int ora_quantize_tile_ex(const double *X, int levels, int iters, int rotate,
+                         uint8_t *g8, uint8_t *a8, uint16_t *b16, uint8_t *code,
+                         double *pre, double *Rout, double *vout)
 {
     static __thread double R[T * D];
     double u[T], v[D], gval[D], mv = 0.0;
     int flags = 0;
 
-    ora_rotate(X, T, R);
+    if (rotate)
+        ora_rotate(X, T, R);
+    else
+        memcpy(R, X, sizeof(double) * T * D);
     ora_sinkhorn(R, iters, u, v);
 
     /* gauge: geometric mean of the column factors = 1 */
@@ -385,6 +408,13 @@ void ora_unpack_record(int kind, const uint8_t *rec, uint8_t *g8, uint8_t *a8, u
  * Rhat[t][c] = g_c (a_t code_tc + b_t), Xhat = Rhat H (unrotated). */
 void ora_dequantize_record(int kind, const uint8_t *rec, double *Xhat)
 {
+    ora_dequantize_record_ex(kind, rec, 1, Xhat);
+}
+
+/* Dequantise without the inverse rotation when rotate = 0 (records made by
+ * ora_quantize_tile_ex with rotate = 0). */
+void ora_dequantize_record_ex(int kind, const uint8_t *rec, int rotate, double *Xhat)
+{
     static __thread double Rh[T * D];
     uint8_t g8[D], a8[T], code[T * D];
     uint16_t b16[T];
@@ -393,7 +423,10 @@ void ora_dequantize_record(int kind, const uint8_t *rec, double *Xhat)
         for (int c = 0; c < D; c++)
             Rh[t * D + c] = ora_e4m3_decode(g8[c]) *
                             (ora_e4m3_decode(a8[t]) * code[t * D + c] + ora_f16_decode(b16[t]));
-    ora_rotate(Rh, T, Xhat);
+    if (rotate)
+        ora_rotate(Rh, T, Xhat);
+    else
+        memcpy(Xhat, Rh, sizeof(double) * T * D);
 }
 
 /* ------------------------------------------------------------------ */

@@ -378,3 +378,51 @@ def test_causal_attention_last_query_equals_decode_form(k_bits):
     got = O.causal_attention(q, K, V, 1 / math.sqrt(D))
     want = O.attention_folded(q[-1], krec, vrec, kt, vt, 1 / math.sqrt(D), k_bits)
     assert np.abs(got[-1] - want).max() < 1e-9
+
+
+# ---------------------------------------------------------------- per-token error ablations
+@pytest.mark.parametrize("levels,seed", [(15, 2), (3, 3)])
+def test_unrotated_quantize_properties(levels, seed):
+    """Without the rotation the record describes X itself: codes are the
+    nearest level (brute force) except exact ties, and every value is within
+    half a step of its reconstruction."""
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((T, D)) * (1 + 5 * (np.arange(D) % 17 == 0))
+    tl = O.quantize_tile(X, levels, 8, rotate=False)
+    g = np.array([O.e4m3_decode(c) for c in tl.g8]); a = np.array([O.e4m3_decode(c) for c in tl.a8])
+    b = np.array([O.f16_decode(c) for c in tl.b16])
+    Y = X / g[None, :]
+    lv = a[:, None, None] * np.arange(levels + 1)[None, None, :] + b[:, None, None]
+    best = np.abs(Y[:, :, None] - lv).argmin(axis=2)
+    tie = np.abs(tl.pre - np.floor(tl.pre) - 0.5) < 1e-9
+    assert np.array_equal(best[~tie], tl.code[~tie])
+    Xh = O.dequantize_record(levels == 3, O.pack_record(levels == 3, tl), rotate=False)
+    assert (np.abs(Xh - X) <= 0.5 * a[:, None] * g[None, :] * (1 + 1e-9)).all()
+
+
+def test_plain_rtn_is_per_token_min_max():
+    """No rotation and no normalisation: unit channel scales (g = 1), and each
+    token's zero-point / step cover its own min / max (b <= min, b + L a >= max)."""
+    rng = np.random.default_rng(7)
+    X = rng.standard_normal((T, D))
+    tl = O.quantize_tile(X, 15, 0, rotate=False)
+    assert (tl.g8 == O.e4m3_encode_rne(1.0)).all()
+    a = np.array([O.e4m3_decode(c) for c in tl.a8]); b = np.array([O.f16_decode(c) for c in tl.b16])
+    assert (b <= X.min(axis=1)).all() and (b + 15 * a >= X.max(axis=1)).all()
+
+
+def test_token_errors_definition_and_rotation_benefit():
+    """err2 / norm2 are the plain sums of the reconstruction; on keys with
+    outlier channels the rotation + normalisation shrink the largest token
+    errors relative to plain per-token RTN (the pages' claim, checked on
+    synthetic tiles)."""
+    X = key_tile(11)
+    e_full, n_full = O.token_errors(X, False)
+    tl = O.quantize_tile(X, 15)
+    Xh = O.dequantize_record(False, O.pack_record(False, tl))
+    assert np.allclose(e_full, ((Xh - X) ** 2).sum(1), rtol=0, atol=1e-12)
+    assert np.allclose(n_full, (X ** 2).sum(1), rtol=0, atol=1e-9)
+    e_plain, _ = O.token_errors(X, False, iters=0, rotate=False)
+    rel_full, rel_plain = np.sqrt(e_full / n_full), np.sqrt(e_plain / n_full)
+    top = lambda r: np.sort(r)[-max(1, len(r) // 20):].mean()
+    assert top(rel_full) < top(rel_plain)
