@@ -90,6 +90,32 @@ kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const 
   return cuda_status(launch_quantize(p, cfg->dtype, n_tiles, static_cast<cudaStream_t>(stream)));
 }
 
+size_t kvarn_token_errors_scratch_bytes(const kvarn_config* cfg, int32_t n_tiles, int32_t is_v) {
+  if (check_config(cfg) != KVARN_OK || n_tiles < 0) return 0;
+  return static_cast<size_t>(n_tiles) * cfg->num_kv_heads * static_cast<size_t>(is_v ? rec_bytes(2) : rec_bytes(cfg->k_bits));
+}
+
+kvarn_status kvarn_token_errors(const kvarn_config* cfg, const void* x, int64_t token_stride_elems, int64_t n_tokens,
+                                const int64_t* tile_first_token, int32_t n_tiles, int32_t is_v, int32_t rotate,
+                                int32_t sinkhorn_iters, void* scratch, size_t scratch_bytes, float* out,
+                                int32_t* dev_err, void* stream) {
+  kvarn_status st = check_config(cfg);
+  if (st != KVARN_OK) return st;
+  if (n_tiles < 0 || n_tokens < 0 || (is_v != 0 && is_v != 1) || (rotate != 0 && rotate != 1) ||
+      sinkhorn_iters < 0 || sinkhorn_iters > 64)
+    return KVARN_ERR_INVALID;
+  if (n_tiles == 0) return KVARN_OK;
+  if (!x || !tile_first_token || !scratch || !out) return KVARN_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(scratch) || !aligned16(out)) return KVARN_ERR_INVALID;
+  if (token_stride_elems % 8 || token_stride_elems < static_cast<int64_t>(cfg->num_kv_heads) * 128)
+    return KVARN_ERR_INVALID;
+  if (static_cast<int64_t>(n_tiles) * cfg->num_kv_heads > 0x7fffffffLL) return KVARN_ERR_INVALID;
+  if (scratch_bytes < kvarn_token_errors_scratch_bytes(cfg, n_tiles, is_v)) return KVARN_ERR_INVALID;
+  ErrParams p{x, token_stride_elems, n_tokens, tile_first_token, static_cast<unsigned char*>(scratch), out,
+              cfg->num_kv_heads, sinkhorn_iters, cfg->k_bits, is_v, rotate, dev_err};
+  return cuda_status(launch_token_errors(p, cfg->dtype, n_tiles, static_cast<cudaStream_t>(stream)));
+}
+
 kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, const void* v_new, const int32_t* pos,
                                  const int32_t* block_table, int32_t max_blocks, int32_t batch, void* tail_pool,
                                  void* block_pool, int32_t* dev_err, void* stream) {

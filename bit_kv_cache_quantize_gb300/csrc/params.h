@@ -88,6 +88,24 @@ struct MQParams {
   int32_t k_bits;
 };
 
+// Per-token reconstruction errors of quantised tiles (the error study):
+// quantise (rotation and normalisation optional), dequantise, compare.
+struct ErrParams {
+  const void* x;
+  int64_t token_stride;
+  int64_t n_tokens;
+  const int64_t* tile_first_token;
+  unsigned char* scratch;  // one record per (tile, head)
+  float* out;              // [n_tiles][num_kv_heads][128] x (err2, norm2)
+  int32_t num_kv_heads;
+  int32_t iters;
+  int32_t k_bits;
+  int32_t is_v;
+  int32_t rotate;
+  int32_t* err;
+};
+cudaError_t launch_token_errors(const ErrParams& p, int dtype, int n_tiles, cudaStream_t s);
+
 cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStream_t s);
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,

@@ -187,7 +187,7 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
 // pool.  All 256 threads of the CTA must call this.  After the rotation every
 // thread holds one 8-token x 8-channel block of R: tokens 16w + 8(l >> 4) +
 // 0..7, channels 8(l & 15) + 0..7 (warp w, lane l).
-template <typename E, int KIND>
+template <typename E, int KIND, bool ROT = true>
 __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride, unsigned char* __restrict__ dst,
                                   int iters, QSmem& sm) {
   constexpr int L = kind_levels(KIND);
@@ -203,6 +203,16 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
   }
   cp_async_wait_all();
   __syncthreads();
+  float2 r[8][4];  // r[i][p] = R[tok0 + i][8cb + 2p .. 2p+1]
+  if constexpr (!ROT) {  // the no-rotation ablation: R = X
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(sm.xs + (tok0 + i) * X_ROW + (8 * cb + 2 * pp) * 2);
+        r[i][pp] = make_float2(bits2f<E>((uint16_t)(w & 0xFFFFu)), bits2f<E>((uint16_t)(w >> 16)));
+      }
+  } else {
   uint32_t afr[8][4];
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks)
@@ -213,7 +223,6 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
   // For k = 16ks + kk, n = 8nb + g:  popcount(k & n) = popcount(kk & g)
   // + (kk >> 3) * (nb & 1) + popcount(ks & (nb >> 1)), so every B fragment is
   // +-F with F the lane's base sign pair.
-  float2 r[8][4];  // r[i][p] = R[tok0 + i][8cb + 2p .. 2p+1]
   {
     const uint32_t one = Bits16<E>::one;
     const uint32_t F = ((__popc((2 * j) & g) & 1) ? (one | 0x8000u) : one) |
@@ -248,6 +257,7 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
         r[i][2 * hh] = make_float2(v.x, v.y);
         r[i][2 * hh + 1] = make_float2(v.z, v.w);
       }
+  }
   }
   float2* part = reinterpret_cast<float2*>(sm.xs + OFF_PART);
   float2* tokv = reinterpret_cast<float2*>(sm.xs + OFF_TOK);
@@ -575,6 +585,104 @@ static cudaError_t launch_quantize_t(const QuantizeParams& p, int n_tiles, cudaS
   const int64_t jobs = static_cast<int64_t>(n_tiles) * p.num_kv_heads * 2;
   quantize_tiles_kernel<E><<<static_cast<unsigned>(jobs), 256, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+// ---- per-token errors: quantise a tile into a scratch record, dequantise it
+// and compare with the input.  One CTA (256 threads) per (tile, head); in the
+// comparison thread 2t + hf takes channels 64 hf .. 64 hf + 63 of token t.
+template <typename E, int KIND, bool ROT>
+__global__ void __launch_bounds__(256, 2) token_errors_kernel(ErrParams prm) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  QSmem& sm = *reinterpret_cast<QSmem*>(smem_raw);
+  const int job = blockIdx.x, h = job % prm.num_kv_heads, tile = job / prm.num_kv_heads;
+  const int64_t first = prm.tile_first_token[tile];
+  if (first < 0 || first + T > prm.n_tokens) {
+    if (threadIdx.x == 0) set_error(prm.err, KVARN_DEV_ERR_TOKEN_RANGE);
+    return;
+  }
+  const E* src = static_cast<const E*>(prm.x) + first * prm.token_stride + h * D;
+  unsigned char* rec = prm.scratch + (int64_t)job * kind_rec_bytes(KIND);
+  quantize_tile_cta<E, KIND, ROT>(src, prm.token_stride, rec, prm.iters, sm);
+  __syncthreads();  // the record is in global memory, written by this CTA
+  const int t = threadIdx.x >> 1, hf = threadIdx.x & 1;
+  const float a = e4m3_to_float(rec[128 + t]);
+  const float b = __half2float(*reinterpret_cast<const __half*>(rec + 256 + 2 * t));
+  float x[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const int c = 64 * hf + i;
+    int code;
+    if constexpr (KIND == KIND_V2) {
+      const int vb = (t & 1) ? 15 + (t & 15) : (t & 15);  // bit of token t in its channel word
+      code = (rec[512 + c * 32 + 4 * (t >> 4) + (vb >> 3)] >> (vb & 7)) & 3;
+    } else if constexpr (KIND == KIND_K4) {
+      code = (rec[512 + t * 64 + (c >> 1)] >> (4 * (c & 1))) & 15;
+    } else {
+      code = (rec[512 + t * 32 + (c >> 2)] >> (2 * (c & 3))) & 3;
+    }
+    x[i] = e4m3_to_float(rec[c]) * fmaf(a, static_cast<float>(code), b);
+  }
+  if constexpr (ROT) {  // x = R H / sqrt(128): 64-point butterflies here, the last stage across the lane pair
+#pragma unroll
+    for (int m = 1; m < 64; m <<= 1)
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (!(i & m)) {
+          const float u = x[i], w = x[i + m];
+          x[i] = u + w;
+          x[i + m] = u - w;
+        }
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], 1);
+      x[i] = (hf ? (o - x[i]) : (x[i] + o)) * INV_SQRT_D;
+    }
+  }
+  float e2 = 0.f, n2 = 0.f;
+  const E* row = src + (int64_t)t * prm.token_stride + 64 * hf;
+#pragma unroll
+  for (int i = 0; i < 64; i += 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float x0 = bits2f<E>((uint16_t)(w[k] & 0xFFFFu)), x1 = bits2f<E>((uint16_t)(w[k] >> 16));
+      const float d0 = x[i + 2 * k] - x0, d1 = x[i + 2 * k + 1] - x1;
+      e2 = fmaf(d0, d0, fmaf(d1, d1, e2));
+      n2 = fmaf(x0, x0, fmaf(x1, x1, n2));
+    }
+  }
+  e2 += __shfl_xor_sync(0xffffffffu, e2, 1);
+  n2 += __shfl_xor_sync(0xffffffffu, n2, 1);
+  if (hf == 0) *reinterpret_cast<float2*>(prm.out + ((int64_t)job * T + t) * 2) = make_float2(e2, n2);
+}
+
+template <typename E, int KIND>
+static cudaError_t launch_errors_k(const ErrParams& p, int n_tiles, cudaStream_t s) {
+  const size_t smem = sizeof(QSmem);
+  const dim3 grid(n_tiles * p.num_kv_heads);
+  if (p.rotate) {
+    cudaError_t e =
+        cudaFuncSetAttribute(token_errors_kernel<E, KIND, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    token_errors_kernel<E, KIND, true><<<grid, 256, smem, s>>>(p);
+  } else {
+    cudaError_t e =
+        cudaFuncSetAttribute(token_errors_kernel<E, KIND, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    token_errors_kernel<E, KIND, false><<<grid, 256, smem, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+template <typename E>
+static cudaError_t launch_errors_t(const ErrParams& p, int n_tiles, cudaStream_t s) {
+  if (p.is_v) return launch_errors_k<E, KIND_V2>(p, n_tiles, s);
+  return p.k_bits == 2 ? launch_errors_k<E, KIND_K2>(p, n_tiles, s) : launch_errors_k<E, KIND_K4>(p, n_tiles, s);
+}
+
+cudaError_t launch_token_errors(const ErrParams& p, int dtype, int n_tiles, cudaStream_t s) {
+  return dtype == KVARN_DTYPE_BF16 ? launch_errors_t<__nv_bfloat16>(p, n_tiles, s) : launch_errors_t<__half>(p, n_tiles, s);
 }
 
 cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cudaStream_t s) {

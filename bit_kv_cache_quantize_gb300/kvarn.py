@@ -38,6 +38,7 @@ EXPORTS = (
     "kvarn_decode_workspace_bytes", "kvarn_decode_attention", "kvarn_dequantize",
     "kvarn_fp16_block_bytes", "kvarn_fp16_decode_attention", "kvarn_status_string",
     "kvarn_decode_attention_noalloc", "kvarn_multiquery_workspace_bytes", "kvarn_multiquery_attention",
+    "kvarn_token_errors_scratch_bytes", "kvarn_token_errors",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
             "kvarn_decode_attention_noalloc": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, P]),
             "kvarn_dequantize": (i32, [C, P, P, i32, P, P, P]),
             "kvarn_multiquery_workspace_bytes": (sz, [C, i32, i32, i32]),
+            "kvarn_token_errors_scratch_bytes": (sz, [C, i32, i32]),
+            "kvarn_token_errors": (i32, [C, P, i64, i64, P, i32, i32, i32, i32, P, sz, P, P, P]),
             "kvarn_multiquery_attention": (i32, [C, P, i32, P, i32, P, i32, P, P, f32, P, P, sz, P, P]),
             "kvarn_status_string": (ctypes.c_char_p, [i32]),
         }
@@ -187,6 +190,20 @@ def kvarn_multiquery_attention(cfg, q, n_queries, block_table, max_blocks, seq_l
                                           float(softmax_scale), _p(out), _p(workspace), int(workspace_bytes),
                                           _p(dev_err), _s(stream))
     return _check(st, "kvarn_multiquery_attention", check)
+
+
+def kvarn_token_errors_scratch_bytes(cfg, n_tiles: int, is_v: int) -> int:
+    return int(lib().kvarn_token_errors_scratch_bytes(ctypes.byref(cfg), n_tiles, is_v))
+
+
+def kvarn_token_errors(cfg, x, token_stride_elems, n_tokens, tile_first_token, n_tiles, is_v, rotate, sinkhorn_iters,
+                       scratch, scratch_bytes, out, dev_err, stream=None, check=True) -> int:
+    """Per-token (squared error, squared norm) of quantise -> dequantise,
+    with the rotation and the normalisation optional (see include/kvarn.h)."""
+    st = lib().kvarn_token_errors(ctypes.byref(cfg), _p(x), int(token_stride_elems), int(n_tokens),
+                                  _p(tile_first_token), int(n_tiles), int(is_v), int(rotate), int(sinkhorn_iters),
+                                  _p(scratch), int(scratch_bytes), _p(out), _p(dev_err), _s(stream))
+    return _check(st, "kvarn_token_errors", check)
 
 
 def kvarn_fp16_decode_attention(cfg, q, block_table, max_blocks, seq_lens, batch, fp16_pool, softmax_scale, out,

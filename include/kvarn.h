@@ -257,6 +257,32 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
 kvarn_status kvarn_dequantize(const kvarn_config* cfg, const void* block_pool, const int32_t* blocks,
                               int32_t n, float* out, int32_t* dev_err, void* stream);
 
+/* Scratch bytes kvarn_token_errors needs: one record per (tile, head). */
+size_t kvarn_token_errors_scratch_bytes(const kvarn_config* cfg, int32_t n_tiles, int32_t is_v);
+
+/*
+ * Per-token reconstruction errors (an analysis tool, not part of serving):
+ * quantise each (tile, KV head) of x as the K (is_v = 0) or V (is_v = 1)
+ * record of cfg's preset, dequantise it and compare with the input.  The
+ * pages single out the per-token error distribution ("Huawei's KVarN puts
+ * KV-cache quantization inside vLLM's backend", section "Why KV-cache
+ * quantization degrades under autoregressive decoding": the largest 5% of
+ * per-token errors cause most of the loss); rotate = 0 skips the Hadamard
+ * rotation and sinkhorn_iters = 0 the variance normalisation, so the same
+ * call measures each stage's effect.
+ *  x, token_stride_elems, n_tokens, tile_first_token, n_tiles: as
+ *              kvarn_quantize_tiles (one input tensor).
+ *  scratch     device, >= kvarn_token_errors_scratch_bytes(cfg, n_tiles, is_v).
+ *  out         device float32 [n_tiles][num_kv_heads][128 tokens][2]:
+ *              (sum_c (xhat - x)^2, sum_c x^2) per token.
+ * A tile whose first token is out of range stores KVARN_DEV_ERR_TOKEN_RANGE
+ * and leaves its rows unwritten.
+ */
+kvarn_status kvarn_token_errors(const kvarn_config* cfg, const void* x, int64_t token_stride_elems, int64_t n_tokens,
+                                const int64_t* tile_first_token, int32_t n_tiles, int32_t is_v, int32_t rotate,
+                                int32_t sinkhorn_iters, void* scratch, size_t scratch_bytes, float* out,
+                                int32_t* dev_err, void* stream);
+
 /* Bytes of one block of the 16-bit comparison pool: num_kv_heads * 2 * 128 *
  * 128 * 2, layout [kv_head][K=0,V=1][token][channel]. */
 size_t kvarn_fp16_block_bytes(const kvarn_config* cfg);
