@@ -104,7 +104,7 @@ class ClockSampler:
 # ncu capture of the 16K decode (profiles/decode_call_traffic_qwen3_32b_16k.md:
 # 449 723 392 B for 437 796 992 algorithmic bytes).  The serving step's call is
 # too large to capture, and its traffic grows with the records it reads.
-DECODE_TRAFFIC_PER_BYTE = 449723392 / 437796992
+DECODE_TRAFFIC_PER_BYTE = 449662976 / 437796992
 
 
 def decode_bytes(lens, w):
