@@ -69,9 +69,9 @@ def lib():
         L.ora_quantize_tile_ex.argtypes = [P, i32, i32, i32, P, P, P, P, P, P, P]
         L.ora_dequantize_record_ex.argtypes = [i32, P, i32, P]
         L.ora_attention.argtypes = [P, i32, P, P, i32, dbl, P]
-        L.ora_attention_folded.argtypes = [P, i32, P, P, i32, P, P, i32, dbl, i32, P]
+        L.ora_attention_folded.argtypes = [P, i32, P, P, i32, P, P, i32, dbl, i32, i32, P]
         L.ora_quantize_batch.argtypes = [P, i32, P, i64, i32, i32, i32, P, P, i32]
-        L.ora_attention_batch.argtypes = [P, i32, P, P, P, P, P, P, P, dbl, i32, i32, P, i32]
+        L.ora_attention_batch.argtypes = [P, i32, P, P, P, P, P, P, P, dbl, i32, i32, i32, P, i32]
         _lib = L
     return _lib
 
@@ -171,54 +171,59 @@ def quantize_tile(X: np.ndarray, levels: int, iters: int = 8, rotate: bool = Tru
 
 
 # Record kinds: 4-bit keys (the kvarn_k4v2 preset), 2-bit values, 2-bit keys
-# (the K2/V2 preset).  Functions take is_v and the key width.
-K4, V2, K2 = 0, 1, 2
+# (the K2/V2 preset), 4-bit values (the K4/V4 preset).  Functions take is_v
+# and the key and value widths.
+K4, V2, K2, V4 = 0, 1, 2, 3
 
 
-def kind(is_v: bool, k_bits: int = 4) -> int:
-    assert k_bits in (2, 4)
-    return V2 if is_v else (K4 if k_bits == 4 else K2)
+def kind(is_v: bool, k_bits: int = 4, v_bits: int = 2) -> int:
+    assert k_bits in (2, 4) and v_bits in (2, 4)
+    if is_v:
+        return V2 if v_bits == 2 else V4
+    return K4 if k_bits == 4 else K2
 
 
-def levels(is_v: bool, k_bits: int = 4) -> int:
-    return 3 if (is_v or k_bits == 2) else 15
+def levels(is_v: bool, k_bits: int = 4, v_bits: int = 2) -> int:
+    return 15 if (v_bits if is_v else k_bits) == 4 else 3
 
 
-def record_bytes(is_v: bool, k_bits: int = 4) -> int:
-    return int(lib().ora_record_bytes(kind(is_v, k_bits)))
+def record_bytes(is_v: bool, k_bits: int = 4, v_bits: int = 2) -> int:
+    return int(lib().ora_record_bytes(kind(is_v, k_bits, v_bits)))
 
 
-def pack_record(is_v: bool, tile: Tile, k_bits: int = 4) -> np.ndarray:
-    rec = np.zeros(record_bytes(is_v, k_bits), np.uint8)
-    lib().ora_pack_record(kind(is_v, k_bits), _p(tile.g8), _p(tile.a8), _p(tile.b16),
+def pack_record(is_v: bool, tile: Tile, k_bits: int = 4, v_bits: int = 2) -> np.ndarray:
+    rec = np.zeros(record_bytes(is_v, k_bits, v_bits), np.uint8)
+    lib().ora_pack_record(kind(is_v, k_bits, v_bits), _p(tile.g8), _p(tile.a8), _p(tile.b16),
                           _p(np.ascontiguousarray(tile.code)), _p(rec))
     return rec
 
 
-def unpack_record(is_v: bool, rec: np.ndarray, k_bits: int = 4):
+def unpack_record(is_v: bool, rec: np.ndarray, k_bits: int = 4, v_bits: int = 2):
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     g8 = np.empty(D, np.uint8); a8 = np.empty(T, np.uint8); b16 = np.empty(T, np.uint16)
     code = np.empty((T, D), np.uint8)
-    lib().ora_unpack_record(kind(is_v, k_bits), _p(rec), _p(g8), _p(a8), _p(b16), _p(code))
+    lib().ora_unpack_record(kind(is_v, k_bits, v_bits), _p(rec), _p(g8), _p(a8), _p(b16), _p(code))
     return g8, a8, b16, code
 
 
-def dequantize_record(is_v: bool, rec: np.ndarray, k_bits: int = 4, rotate: bool = True) -> np.ndarray:
+def dequantize_record(is_v: bool, rec: np.ndarray, k_bits: int = 4, rotate: bool = True,
+                      v_bits: int = 2) -> np.ndarray:
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     out = np.empty((T, D))
-    lib().ora_dequantize_record_ex(kind(is_v, k_bits), _p(rec), 1 if rotate else 0, _p(out))
+    lib().ora_dequantize_record_ex(kind(is_v, k_bits, v_bits), _p(rec), 1 if rotate else 0, _p(out))
     return out
 
 
-def token_errors(X: np.ndarray, is_v: bool, k_bits: int = 4, iters: int = 8, rotate: bool = True):
+def token_errors(X: np.ndarray, is_v: bool, k_bits: int = 4, iters: int = 8, rotate: bool = True,
+                 v_bits: int = 2):
     """Per-token reconstruction error of one tile ("Huawei's KVarN puts
     KV-cache quantization inside vLLM's backend", section "Why KV-cache
     quantization degrades under autoregressive decoding": per-token errors):
     quantise, pack, dequantise, then for each token t
       err2[t] = sum_c (Xhat[t][c] - X[t][c])^2,  norm2[t] = sum_c X[t][c]^2."""
     X = np.ascontiguousarray(X, dtype=np.float64)
-    tl = quantize_tile(X, levels(is_v, k_bits), iters, rotate)
-    Xh = dequantize_record(is_v, pack_record(is_v, tl, k_bits), k_bits, rotate)
+    tl = quantize_tile(X, levels(is_v, k_bits, v_bits), iters, rotate)
+    Xh = dequantize_record(is_v, pack_record(is_v, tl, k_bits, v_bits), k_bits, rotate, v_bits)
     return ((Xh - X) ** 2).sum(axis=1), (X ** 2).sum(axis=1)
 
 
@@ -239,7 +244,7 @@ def _ptr_array(recs):
     return arr
 
 
-def attention_folded(q, krecs, vrecs, ktail, vtail, scale, k_bits: int = 4) -> np.ndarray:
+def attention_folded(q, krecs, vrecs, ktail, vtail, scale, k_bits: int = 4, v_bits: int = 2) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.float64).reshape(-1, D)
     krecs = [np.ascontiguousarray(r, dtype=np.uint8) for r in krecs]
     vrecs = [np.ascontiguousarray(r, dtype=np.uint8) for r in vrecs]
@@ -248,17 +253,18 @@ def attention_folded(q, krecs, vrecs, ktail, vtail, scale, k_bits: int = 4) -> n
     out = np.empty_like(q)
     ka, va = _ptr_array(krecs), _ptr_array(vrecs)
     lib().ora_attention_folded(_p(q), q.shape[0], ka, va, len(krecs), _p(ktail), _p(vtail),
-                               ktail.shape[0], float(scale), kind(False, k_bits), _p(out))
+                               ktail.shape[0], float(scale), kind(False, k_bits), kind(True, k_bits, v_bits),
+                               _p(out))
     return out
 
 
-def cache_values(krecs, vrecs, ktail, vtail, k_bits: int = 4):
+def cache_values(krecs, vrecs, ktail, vtail, k_bits: int = 4, v_bits: int = 2):
     """The cache as attention reads it ("Huawei's KVarN puts KV-cache
     quantization inside vLLM's backend", section "The four-stage pipeline":
     dequantisation at read time): the dequantised closed tiles in order, then
     the raw open-tile tokens.  Returns K, V as [n, D] fp64."""
     ks = [dequantize_record(False, r, k_bits) for r in krecs] + [np.asarray(ktail, np.float64).reshape(-1, D)]
-    vs = [dequantize_record(True, r, k_bits) for r in vrecs] + [np.asarray(vtail, np.float64).reshape(-1, D)]
+    vs = [dequantize_record(True, r, k_bits, v_bits=v_bits) for r in vrecs] + [np.asarray(vtail, np.float64).reshape(-1, D)]
     return np.concatenate(ks), np.concatenate(vs)
 
 
@@ -274,21 +280,22 @@ def causal_attention(q, K, V, scale) -> np.ndarray:
 
 
 def quantize_batch(src_bits: np.ndarray, dtype: str, first: np.ndarray, row_stride: int, is_v: bool,
-                   iters: int = 8, nthreads: int | None = None, k_bits: int = 4):
+                   iters: int = 8, nthreads: int | None = None, k_bits: int = 4, v_bits: int = 2):
     """Quantise len(first) tiles read from flat 16-bit storage; returns
     (records [n, record_bytes], flags [n])."""
     src_bits = np.ascontiguousarray(src_bits, dtype=np.uint16).reshape(-1)
     first = np.ascontiguousarray(first, dtype=np.int64)
     n = first.shape[0]
-    rec = np.zeros((n, record_bytes(is_v, k_bits)), np.uint8)
+    rec = np.zeros((n, record_bytes(is_v, k_bits, v_bits)), np.uint8)
     flags = np.zeros(n, np.int32)
     nthreads = nthreads or os.cpu_count() or 1
     lib().ora_quantize_batch(_p(src_bits), 1 if dtype == "bf16" else 0, _p(first), int(row_stride), n,
-                             kind(is_v, k_bits), iters, _p(rec), _p(flags), int(nthreads))
+                             kind(is_v, k_bits, v_bits), iters, _p(rec), _p(flags), int(nthreads))
     return rec, flags
 
 
-def attention_batch(q, krec_lists, vrec_lists, ktails, vtails, n_tail, scale, nthreads=None, k_bits: int = 4):
+def attention_batch(q, krec_lists, vrec_lists, ktails, vtails, n_tail, scale, nthreads=None, k_bits: int = 4,
+                    v_bits: int = 2):
     """q [U, G, D]; krec_lists/vrec_lists: per unit a list of records;
     ktails/vtails [U, T, D] fp64 (rows beyond n_tail[u] ignored)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
@@ -304,6 +311,7 @@ def attention_batch(q, krec_lists, vrec_lists, ktails, vtails, n_tail, scale, nt
     out = np.empty((U, G, D))
     nthreads = nthreads or os.cpu_count() or 1
     lib().ora_attention_batch(_p(q), G, _ptr_array(flatk), _ptr_array(flatv), _p(off), _p(n_tiles),
-                              _p(ktails), _p(vtails), _p(n_tail), float(scale), kind(False, k_bits), U, _p(out),
+                              _p(ktails), _p(vtails), _p(n_tail), float(scale), kind(False, k_bits),
+                              kind(True, k_bits, v_bits), U, _p(out),
                               int(nthreads))
     return out

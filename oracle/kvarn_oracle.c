@@ -337,7 +337,7 @@ int ora_quantize_tile_ex(const double *X, int levels, int iters, int rotate,
     return flags;
 }
 
-enum { ORA_K4 = 0, ORA_V2 = 1, ORA_K2 = 2 };
+enum { ORA_K4 = 0, ORA_V2 = 1, ORA_K2 = 2, ORA_V4 = 3 };
 
 /* ------------------------------------------------------------------ */
 /* Packed record layout (16-byte aligned, scales first)                */
@@ -351,14 +351,22 @@ enum { ORA_K4 = 0, ORA_V2 = 1, ORA_K2 = 2 };
 /*                  = 8 little-endian 32-bit words, word w holds tokens */
 /*                  16w..16w+15, token 16w+u at bit u (u even) or bit   */
 /*                  15+u (u odd)                              = 4608 B */
+/*   V4 (levels 15, the K4/V4 preset): same header | codes[128 ch]    */
+/*                  [64 B]: channel c = 16 LE 32-bit words, word w    */
+/*                  holds tokens 8w..8w+7, token 8w+u at bit 2u (u     */
+/*                  even) or 14+2u (u odd)                    = 8704 B */
 /* ------------------------------------------------------------------ */
 
 /* bit of token u (0..15) inside its 32-bit V word */
 static int ora_v_bit(int u) { return (u & 1) ? 15 + u : u; }
+/* bit of token u (0..7) inside its 32-bit V4 word: even tokens in the low
+ * half-word, odd tokens in the high half-word, 4 bits each */
+static int ora_v4_bit(int u) { return (u & 1) ? 14 + 2 * u : 2 * u; }
 
-/* record kinds: ORA_K4 (4-bit keys), ORA_V2 (2-bit values), ORA_K2 (2-bit keys) */
-int ora_record_bytes(int kind) { return 512 + (kind == ORA_K4 ? D * T / 2 : D * T / 4); }
-int ora_kind_levels(int kind) { return kind == ORA_K4 ? 15 : 3; }
+/* record kinds: ORA_K4 (4-bit keys), ORA_V2 (2-bit values), ORA_K2 (2-bit
+ * keys), ORA_V4 (4-bit values) */
+int ora_record_bytes(int kind) { return 512 + ((kind == ORA_K4 || kind == ORA_V4) ? D * T / 2 : D * T / 4); }
+int ora_kind_levels(int kind) { return (kind == ORA_K4 || kind == ORA_V4) ? 15 : 3; }
 
 void ora_pack_record(int kind, const uint8_t *g8, const uint8_t *a8, const uint16_t *b16,
                      const uint8_t *code, uint8_t *rec)
@@ -377,6 +385,14 @@ void ora_pack_record(int kind, const uint8_t *g8, const uint8_t *a8, const uint1
                 uint8_t byte = 0;
                 for (int k = 0; k < 4; k++) byte |= (uint8_t)(code[t * D + 4 * i + k] << (2 * k));
                 p[t * 32 + i] = byte;
+            }
+    } else if (kind == ORA_V4) {
+        for (int c = 0; c < D; c++)
+            for (int w = 0; w < T / 8; w++) {
+                uint32_t word = 0;
+                for (int u = 0; u < 8; u++)
+                    word |= (uint32_t)code[(8 * w + u) * D + c] << ora_v4_bit(u);
+                for (int k = 0; k < 4; k++) p[c * 64 + 4 * w + k] = (uint8_t)(word >> (8 * k));
             }
     } else {
         for (int c = 0; c < D; c++)
@@ -400,6 +416,8 @@ void ora_unpack_record(int kind, const uint8_t *rec, uint8_t *g8, uint8_t *a8, u
         for (int c = 0; c < D; c++)
             code[t * D + c] = kind == ORA_K4 ? (uint8_t)((p[t * 64 + c / 2] >> (4 * (c & 1))) & 15)
                             : kind == ORA_K2 ? (uint8_t)((p[t * 32 + c / 4] >> (2 * (c & 3))) & 3)
+                            : kind == ORA_V4 ? (uint8_t)((p[c * 64 + 4 * (t / 8) + ora_v4_bit(t % 8) / 8]
+                                                          >> (ora_v4_bit(t % 8) % 8)) & 15)
                                              : (uint8_t)((p[c * 32 + 4 * (t / 16) + ora_v_bit(t % 16) / 8]
                                                           >> (ora_v_bit(t % 16) % 8)) & 3);
 }
@@ -466,10 +484,10 @@ void ora_attention(const double *q, int G, const double *K, const double *V, int
  * folded into the query, per-token scale/zero into the scores, per-channel
  * value scales into the accumulator, and one inverse rotation is applied to
  * the output.  krec/vrec: n_tiles records each (keys of kind kkind, values
- * ORA_V2); ktail/vtail: [n_tail][D]. */
+ * of kind vkind); ktail/vtail: [n_tail][D]. */
 void ora_attention_folded(const double *q, int G, const uint8_t *const *krec,
                           const uint8_t *const *vrec, int n_tiles, const double *ktail,
-                          const double *vtail, int n_tail, double scale, int kkind, double *out)
+                          const double *vtail, int n_tail, double scale, int kkind, int vkind, double *out)
 {
     int n = n_tiles * T + n_tail;
     double *s = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
@@ -502,7 +520,7 @@ void ora_attention_folded(const double *q, int G, const uint8_t *const *krec,
         double l = 0.0;
         for (int d = 0; d < D; d++) { acc_rot[d] = 0.0; acc_raw[d] = 0.0; }
         for (int tile = 0; tile < n_tiles; tile++) {
-            ora_unpack_record(ORA_V2, vrec[tile], g8, a8, b16, code);
+            ora_unpack_record(vkind, vrec[tile], g8, a8, b16, code);
             double pb = 0.0, pacc[D];
             for (int c = 0; c < D; c++) pacc[c] = 0.0;
             for (int t = 0; t < T; t++) {
@@ -581,7 +599,7 @@ void ora_quantize_batch(const uint16_t *src, int dtype, const int64_t *first, in
 typedef struct {
     const double *q; int G; const uint8_t *const *krec, *const *vrec; const int64_t *off;
     const int32_t *n_tiles; const double *ktail, *vtail; const int32_t *n_tail; double scale;
-    int kkind, n_units, nthreads, tid; double *out;
+    int kkind, vkind, n_units, nthreads, tid; double *out;
 } ajob;
 
 static void *attention_worker(void *arg)
@@ -590,21 +608,22 @@ static void *attention_worker(void *arg)
     for (int u = j->tid; u < j->n_units; u += j->nthreads)
         ora_attention_folded(j->q + (int64_t)u * j->G * D, j->G, j->krec + j->off[u], j->vrec + j->off[u],
                              j->n_tiles[u], j->ktail + (int64_t)u * T * D, j->vtail + (int64_t)u * T * D,
-                             j->n_tail[u], j->scale, j->kkind, j->out + (int64_t)u * j->G * D);
+                             j->n_tail[u], j->scale, j->kkind, j->vkind, j->out + (int64_t)u * j->G * D);
     return NULL;
 }
 
 void ora_attention_batch(const double *q, int G, const uint8_t *const *krec, const uint8_t *const *vrec,
                          const int64_t *off, const int32_t *n_tiles, const double *ktail,
-                         const double *vtail, const int32_t *n_tail, double scale, int kkind, int n_units,
-                         double *out, int nthreads)
+                         const double *vtail, const int32_t *n_tail, double scale, int kkind, int vkind,
+                         int n_units, double *out, int nthreads)
 {
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     pthread_t th[256];
     ajob jobs[256];
     for (int k = 0; k < nthreads; k++) {
-        jobs[k] = (ajob){q, G, krec, vrec, off, n_tiles, ktail, vtail, n_tail, scale, kkind, n_units, nthreads, k, out};
+        jobs[k] = (ajob){q, G, krec, vrec, off, n_tiles, ktail, vtail, n_tail, scale, kkind, vkind, n_units,
+                         nthreads, k, out};
         pthread_create(&th[k], NULL, attention_worker, &jobs[k]);
     }
     for (int k = 0; k < nthreads; k++) pthread_join(th[k], NULL);

@@ -259,6 +259,27 @@ def test_k2_record_layout_bytes():
     assert (O.record_bytes(False, 2) * 8 / (T * D), O.record_bytes(True) * 8 / (T * D)) == (2.25, 2.25)
 
 
+def test_v4_record_layout_bytes():
+    """K4/V4 preset: 4-bit value codes channel-major, 64 B per channel as 16
+    little-endian words of 8 tokens, even tokens in the low half-word and odd
+    tokens in the high half-word (token 8w + u at bit 2u or 14 + 2u)."""
+    tl = O.Tile((np.arange(D) % 120).astype(np.uint8), (np.arange(T) * 5 % 120).astype(np.uint8),
+                (np.arange(T) * 301 % 30000).astype(np.uint16),
+                ((np.arange(T)[:, None] * 7 + np.arange(D)[None, :] * 3) % 16).astype(np.uint8),
+                None, None, None, 0)
+    rv = O.pack_record(True, tl, v_bits=4)
+    assert rv.size == 8704 and O.record_bytes(True, 4, 4) == 8704 and O.levels(True, 4, 4) == 15
+    assert rv[7] == 7 and rv[128 + 3] == 15
+    c, w = 37, 11
+    word = int.from_bytes(rv[512 + c * 64 + 4 * w: 512 + c * 64 + 4 * w + 4].tobytes(), "little")
+    for u in range(8):
+        bit = 14 + 2 * u if u & 1 else 2 * u
+        assert (word >> bit) & 15 == tl.code[8 * w + u, c]
+    g8, a8, b16, code = O.unpack_record(True, rv, v_bits=4)
+    assert np.array_equal(code, tl.code) and np.array_equal(b16, tl.b16)
+    assert O.record_bytes(True, 4, 4) * 8 / (T * D) == 4.25
+
+
 def test_bits_per_element_against_pages():
     """The pages give ~2.3 bits/element including the dual FP8 scales and
     FP16 zero-points, for 4-bit keys / 2-bit values per 128-token tile."""
@@ -291,21 +312,22 @@ def test_attention_matches_torch_sdpa():
     assert np.abs(O.attention(q, K, V, 0.3) - ref.numpy()).max() < 1e-13
 
 
-@pytest.mark.parametrize("k_bits", [4, 2])
+@pytest.mark.parametrize("k_bits,v_bits", [(4, 2), (2, 2), (4, 4)])
 @pytest.mark.parametrize("n_tiles,n_tail", [(1, 0), (2, 37), (0, 5), (3, 127)])
-def test_folded_attention_equals_plain(n_tiles, n_tail, k_bits):
+def test_folded_attention_equals_plain(n_tiles, n_tail, k_bits, v_bits):
     rng = np.random.default_rng(10 + n_tiles)
     krec, vrec, Ks, Vs = [], [], [], []
     for i in range(n_tiles):
         Xk = key_tile(20 + i); Xv = rng.standard_normal((T, D))
         krec.append(O.pack_record(False, O.quantize_tile(Xk, O.levels(False, k_bits)), k_bits))
-        vrec.append(O.pack_record(True, O.quantize_tile(Xv, 3)))
-        Ks.append(O.dequantize_record(False, krec[-1], k_bits)); Vs.append(O.dequantize_record(True, vrec[-1]))
+        vrec.append(O.pack_record(True, O.quantize_tile(Xv, O.levels(True, v_bits=v_bits)), v_bits=v_bits))
+        Ks.append(O.dequantize_record(False, krec[-1], k_bits))
+        Vs.append(O.dequantize_record(True, vrec[-1], v_bits=v_bits))
     kt = rng.standard_normal((n_tail, D)); vt = rng.standard_normal((n_tail, D))
     q = rng.standard_normal((8, D))
     K = np.concatenate(Ks + [kt]); V = np.concatenate(Vs + [vt])
     plain = O.attention(q, K, V, 1 / math.sqrt(D))
-    folded = O.attention_folded(q, krec, vrec, kt, vt, 1 / math.sqrt(D), k_bits)
+    folded = O.attention_folded(q, krec, vrec, kt, vt, 1 / math.sqrt(D), k_bits, v_bits)
     assert np.abs(plain - folded).max() < 1e-9
 
 
