@@ -107,13 +107,21 @@ class ClockSampler:
 DECODE_TRAFFIC_PER_BYTE = 449662976 / 437796992
 
 
+# The quantiser's FP32 work per (tile, head) job: 8 normalisation iterations x
+# 2 half-steps x 16384 elements x 3 lane operations (shifted product, sum,
+# sum of squares) plus ~6 per element for the row range and the encode.
+QUANT_LANE_OPS_PER_JOB = 8 * 2 * 16384 * 3 + 6 * 16384
+# FP32 lane operations per second: 152 SMs x 128 FP32 lanes x 2070 MHz.
+FP32_LANE_OPS_PEAK = 152 * 128 * 2.07e9
+
+
 def decode_bytes(lens, w):
     """Algorithmic bytes of one decode call: packed records of the closed
     tiles, raw open-tile tokens, queries, outputs, block ids and lengths."""
     H = w.num_kv_heads
     closed = sum(n // T for n in lens)
     tail = sum(n % T for n in lens)
-    head_rec = 2 * 512 + T * D * (w.k_bits + 2) // 8   # K and V record of one (tile, head)
+    head_rec = 2 * 512 + T * D * (w.k_bits + w.v_bits) // 8   # K and V record of one (tile, head)
     return (closed * H * head_rec + tail * H * 2 * D * 2 + len(lens) * w.num_q_heads * D * (2 + 4)
             + closed * 4 + len(lens) * 4)
 
@@ -391,7 +399,51 @@ def components(dev, hbm_peak, bf16_peak):
         "us": t_k2 * 1e6, "tokens_per_s": w.batch / t_k2, "GBps": b_k2 / t_k2 / 1e9,
         "frac_hbm": b_k2 / t_k2 / 1e9 / hbm_peak, "bytes": b_k2, "speedup_vs_fp16": t_16 / t_k2,
     }
+    del c
+    torch.cuda.empty_cache()
+
+    # --- the same decode over 4-bit values (K4/V4 records, 17408 B per tile and head)
+    w.k_bits, w.v_bits = 4, 4
+    c = PagedCache(w, dev)
+    c.prefill()
+    t_v4 = timed(lambda: c.decode(q, o), 50)
+    b_v4 = decode_bytes(w.seq_lens, w)
+    assert c.check_error() == 0
+    out["decode_16k_k4v4"] = {
+        "workload": "qwen3_32b_decode_16k with 4-bit keys and values (K4/V4 records)",
+        "us": t_v4 * 1e6, "tokens_per_s": w.batch / t_v4, "GBps": b_v4 / t_v4 / 1e9,
+        "frac_hbm": b_v4 / t_v4 / 1e9 / hbm_peak, "bytes": b_v4, "speedup_vs_fp16": t_16 / t_v4,
+    }
     del c, q, o
+    torch.cuda.empty_cache()
+
+    # --- one tile (latency of a quantise call and a decode call)
+    w = I.single_tile()
+    c = PagedCache(w, dev)
+    k1 = I.kv_sequence(w, "k", 0, T, dev)
+    v1 = I.kv_sequence(w, "v", 0, T, dev)
+    q1 = I.queries(w, device=dev)
+    o1 = torch.empty(1, 1, D, dtype=torch.float32, device=dev)
+    t_q1 = timed(lambda: c.quantize_sequence(0, k1, v1), 50)
+    t_d1 = timed(lambda: c.decode(q1, o1), 50)
+    assert c.check_error() == 0
+    out["single_tile"] = {"workload": "1 KV head, 1 query head, 128 tokens, fp16: latency of one call",
+                          "quantize_us": t_q1 * 1e6, "decode_us": t_d1 * 1e6}
+    del c
+
+    # --- Qwen3-4B-shaped layer decode: 8 x 4096 tokens, 32 q / 8 KV heads, bf16 (27 MB packed: L2 flushed)
+    w = I.qwen3_4b()
+    c = PagedCache(w, dev)
+    c.prefill()
+    q4 = I.queries(w, device=dev)
+    o4 = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    t_4b = timed(lambda: c.decode(q4, o4), 50)
+    b_4b = decode_bytes(w.seq_lens, w)
+    assert c.check_error() == 0
+    out["decode_qwen3_4b"] = {"workload": "qwen3_4b_layer: 8 seqs x 4096 tokens, 32 q / 8 KV heads, bf16",
+                              "us": t_4b * 1e6, "tokens_per_s": w.batch / t_4b, "GBps": b_4b / t_4b / 1e9,
+                              "frac_hbm": b_4b / t_4b / 1e9 / hbm_peak, "bytes": b_4b}
+    del c
     torch.cuda.empty_cache()
 
     # --- write path: quantise 32 x 16384 tokens x 8 heads of bf16 (65536 tile jobs)
@@ -412,10 +464,13 @@ def components(dev, hbm_peak, bf16_peak):
     assert c.check_error() == 0
     jobs = n_tiles * w.num_kv_heads * 2
     byt = jobs * (T * D * 2) + n_tiles * w.num_kv_heads * 13312 + n_tiles * 12
+    alu_ops = jobs * QUANT_LANE_OPS_PER_JOB
     out["quantizer"] = {
         "workload": "prefill_32b_16k: 32 x 16384 tokens x 8 KV heads, bf16, K and V tiles (65536 tile jobs)",
         "us": t_q * 1e6, "tiles_per_s": jobs / t_q, "GBps": byt / t_q / 1e9, "frac_hbm": byt / t_q / 1e9 / hbm_peak,
         "bytes": byt,
+        "alu": {"bound": "alu", "lane_ops_per_job": QUANT_LANE_OPS_PER_JOB, "achieved_tops": alu_ops / t_q / 1e12,
+                "peak_tops": FP32_LANE_OPS_PEAK / 1e12, "frac": alu_ops / t_q / FP32_LANE_OPS_PEAK},
     }
     return out
 

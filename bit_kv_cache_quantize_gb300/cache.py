@@ -23,7 +23,8 @@ class PagedCache:
         self.table = table.to(device)
         self.max_blocks = table.shape[1]
         self.num_blocks = total + extra_blocks
-        self.cfg = K.make_config(w.num_kv_heads, w.num_q_heads, self.num_blocks, w.dtype, k_bits=w.k_bits)
+        self.cfg = K.make_config(w.num_kv_heads, w.num_q_heads, self.num_blocks, w.dtype, k_bits=w.k_bits,
+                                 v_bits=w.v_bits)
         self.block_bytes = K.kvarn_block_bytes(self.cfg)
         self.pool = torch.zeros(self.num_blocks * self.block_bytes, dtype=torch.uint8, device=device)
         self.tail = torch.zeros(w.batch, w.num_kv_heads, 2, T, D, dtype=I.torch_dtype(w.dtype), device=device)
@@ -95,9 +96,9 @@ class PagedCache:
 
     # ------------------------------------------------------------ access
     def record(self, blk: int, head: int, kv: int) -> torch.Tensor:
-        kb = self.cfg.k_bits
-        off = blk * self.block_bytes + head * K.head_rec(kb) + kv * K.rec_bytes(kb)
-        return self.pool[off:off + (K.V_REC if kv else K.rec_bytes(kb))]
+        kb, vb = self.cfg.k_bits, self.cfg.v_bits
+        off = blk * self.block_bytes + head * K.head_rec(kb, vb) + kv * K.rec_bytes(kb)
+        return self.pool[off:off + K.rec_bytes(vb if kv else kb)]
 
     def set_record(self, blk: int, head: int, kv: int, rec: torch.Tensor):
         self.record(blk, head, kv).copy_(rec)

@@ -21,7 +21,8 @@ constexpr int T = 128;               // tokens per tile (one paged block)
 constexpr int K_REC = rec_bytes(4);  // 4-bit keys (kvarn_k4v2 preset): 8704 B
 constexpr int K2_REC = rec_bytes(2); // 2-bit keys (K2/V2 preset): 4608 B
 constexpr int V_REC = rec_bytes(2);  // 2-bit values: 4608 B
-constexpr int HEAD_REC = K_REC + V_REC;
+constexpr int V4_REC = rec_bytes(4); // 4-bit values (K4/V4 preset): 8704 B
+constexpr int HEAD_REC_MAX = K_REC + V4_REC;  // largest (tile, head) pair of records
 constexpr float INV_SQRT_D = 0.08838834764831845f;  // 1/sqrt(128)
 
 // First error wins; the failing unit skips its work.  Never traps, never waits.

@@ -68,10 +68,10 @@ constexpr int DEC_WARPS = 8;
 #define KVARN_PV_ILP 4
 #endif
 constexpr int PV_ILP = KVARN_PV_ILP;  // independent MMA chains interleaved in PV
-template <int KBITS>
+template <int KBITS, int VBITS>
 struct DecSmem {
   alignas(128) unsigned char krec[DEC_WARPS][rec_bytes(KBITS)];
-  alignas(128) unsigned char vrec[DEC_WARPS][V_REC];
+  alignas(128) unsigned char vrec[DEC_WARPS][rec_bytes(VBITS)];
   alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order (hi, lo, hi/16, lo/16)
   alignas(16) float qr[8][D];   // rotated, scaled queries (set-up only)
   float qsi[8];                 // per query: inverse of its power-of-two operand scale
@@ -83,8 +83,9 @@ struct DecMerge {
   float l[DEC_WARPS][8];
   float acc[DEC_WARPS][8][D];
 };
-static_assert(sizeof(DecMerge) <= sizeof(DecSmem<2>::krec), "merge area must fit");
-static_assert(K_REC % 128 == 0 && K2_REC % 128 == 0 && V_REC % 128 == 0, "record buffers stay 128-byte aligned");
+static_assert(sizeof(DecMerge) <= sizeof(DecSmem<2, 2>::krec), "merge area must fit");
+static_assert(K_REC % 128 == 0 && K2_REC % 128 == 0 && V_REC % 128 == 0 && V4_REC % 128 == 0,
+              "record buffers stay 128-byte aligned");
 
 // Key layouts.  KBITS = 4: token rows of 64 B, byte i = channels 2i, 2i+1 (nibbles).
 // KBITS = 2: token rows of 32 B, byte i = channels 4i .. 4i+3 (crumbs at bits 2k).
@@ -156,10 +157,11 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 //     B = 2-bit codes of channel 8 nbp + g, whose 32-bit words keep even
 //     tokens in the low half and odd tokens in the high half, so each B
 //     register is one masked field of one word.
-template <typename E, int KBITS>
+template <typename E, int KBITS, int VBITS>
 __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   using KL = KeyLayout<KBITS>;
   constexpr int KREC = rec_bytes(KBITS), KROW = D * KBITS / 8;  // KROW: code bytes per token
+  constexpr int VREC = rec_bytes(VBITS);
   static_assert(KROW == 16 * KBITS, "token row");
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -178,7 +180,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
   const int n_tiles = min(p.chunk_tiles, n_closed - first);
   if (n_tiles <= 0) return;
   const uint32_t sbase = smem_u32(smem_raw);
-  DecSmem<KBITS>& sm = *reinterpret_cast<DecSmem<KBITS>*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
+  DecSmem<KBITS, VBITS>& sm = *reinterpret_cast<DecSmem<KBITS, VBITS>*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
   const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
@@ -194,8 +196,8 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     if (blk >= 0 && blk < p.num_blocks) {
-      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * head_rec(KBITS) + (is_v ? KREC : 0);
-      const uint32_t bytes = is_v ? V_REC : KREC;
+      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * head_rec(KBITS, VBITS) + (is_v ? KREC : 0);
+      const uint32_t bytes = is_v ? VREC : KREC;
       mbar_expect_tx(bar, bytes);
       bulk_g2s(is_v ? sm.vrec[warp] : sm.krec[warp], src, bytes, bar);
     } else {
@@ -383,7 +385,9 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
           const float2 pr = make_float2(ex2_ftz(fmaf(sc[nb].x, qsi, nm)), ex2_ftz(fmaf(sc[nb].y, qsi, nm)));
           psum = fadd2(psum, pr);
           pb = ffma2(pr, __half22float2(u2h2(bw[i])), pb);
-          const __half2 f2 = __float2half2_rn(64.f / (float)(1 << (2 * (nb & 3))));
+          // undo the field multiplier of the V operand: 4^(nb & 3) for 2-bit fields, 16^(nb & 1) for 4-bit
+          const __half2 f2 = __float2half2_rn(VBITS == 2 ? 64.f / (float)(1 << (2 * (nb & 3)))
+                                                         : 16.f / (float)(1 << (4 * (nb & 1))));
           const __half2 av = __hmul2(e4m3x2_to_half2(((i & 2) ? a8.y : a8.x) >> (16 * (i & 1))), f2);  // exact
           const float2 pa = fmul2(pr, __half22float2(av));
           const __half2 hi = __float22half2_rn(pa);
@@ -395,7 +399,38 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
       l_run = l_run * corr + quad_sum(psum.x + psum.y);
       const float pbs = quad_sum(pb.x + pb.y);
       const float2 corr2 = make_float2(corr, corr), pbs2 = make_float2(pbs, pbs);
-      const float2 inv64 = make_float2(1.f / 64.f, 1.f / 64.f);
+      constexpr float PSC = VBITS == 2 ? 1.f / 64.f : 1.f / 16.f;  // the constant factor of P'
+      const float2 inv64 = make_float2(PSC, PSC);
+      if constexpr (VBITS == 4) {
+      // ---- PV: B = 4-bit codes of channel 8 nbp + g, tokens 32j .. 32j+31 (words 4j .. 4j+3)
+      const unsigned char* vc = vr + 512 + g * 64 + 16 * j;
+#pragma unroll
+      for (int n4 = 0; n4 < 16; n4 += PV_ILP) {
+        uint4 vw[PV_ILP];
+#pragma unroll
+        for (int i = 0; i < PV_ILP; ++i) vw[i] = *reinterpret_cast<const uint4*>(vc + (n4 + i) * 512);
+        float c[PV_ILP][4];
+#pragma unroll
+        for (int i = 0; i < PV_ILP; ++i) c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          // tokens 32j + 4kb + {0,1} | {2,3}: nibbles at bits 0 | 4 of word kb >> 1, shifted by 8 when kb & 1
+#pragma unroll
+          for (int i = 0; i < PV_ILP; ++i) {
+            const uint32_t w = (kb >> 1) == 0 ? vw[i].x : (kb >> 1) == 1 ? vw[i].y : (kb >> 1) == 2 ? vw[i].z : vw[i].w;
+            const uint32_t x = (kb & 1) ? (w >> 8) : w;
+            mma_f16(c[i], pfr[kb], field(x, 0x000F000Fu), field(x, 0x00F000F0u));
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < PV_ILP; ++i) {
+          const int nbp = n4 + i;
+          const float2 gv = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(vr + 8 * nbp + 2 * j));
+          const float2 o = ffma2(fadd2(make_float2(c[i][0], c[i][1]), make_float2(c[i][2], c[i][3])), inv64, pbs2);
+          acc[nbp] = ffma2(acc[nbp], corr2, fmul2(gv, o));
+        }
+      }
+      } else {
       // ---- PV: B = 2-bit codes of channel 8 nbp + g, tokens 32j .. 32j+31
       const unsigned char* vc = vr + 512 + g * 32 + 8 * j;
 #pragma unroll
@@ -424,6 +459,7 @@ __global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
           const float2 o = ffma2(fadd2(make_float2(c[i][0], c[i][1]), make_float2(c[i][2], c[i][3])), inv64, pbs2);
           acc[nbp] = ffma2(acc[nbp], corr2, fmul2(gv, o));
         }
+      }
       }
     }
     __syncwarp();
@@ -776,13 +812,13 @@ size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int c
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
 
-template <typename E, int KBITS>
+template <typename E, int KBITS, int VBITS>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
-  const size_t smem = sizeof(DecSmem<KBITS>) + 128;
-  cudaError_t e =
-      cudaFuncSetAttribute(decode_packed_kernel<E, KBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(DecSmem<KBITS, VBITS>) + 128;
+  cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E, KBITS, VBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  decode_packed_kernel<E, KBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
+  decode_packed_kernel<E, KBITS, VBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
@@ -791,11 +827,12 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
+  const bool bf = dtype == KVARN_DTYPE_BF16;
+  if (p.v_bits == 4)  // the K4/V4 preset
+    return bf ? launch_decode_t<__nv_bfloat16, 4, 4>(p, batch, out, s) : launch_decode_t<__half, 4, 4>(p, batch, out, s);
   if (p.k_bits == 2)
-    return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, 2>(p, batch, out, s)
-                                     : launch_decode_t<__half, 2>(p, batch, out, s);
-  return dtype == KVARN_DTYPE_BF16 ? launch_decode_t<__nv_bfloat16, 4>(p, batch, out, s)
-                                   : launch_decode_t<__half, 4>(p, batch, out, s);
+    return bf ? launch_decode_t<__nv_bfloat16, 2, 2>(p, batch, out, s) : launch_decode_t<__half, 2, 2>(p, batch, out, s);
+  return bf ? launch_decode_t<__nv_bfloat16, 4, 2>(p, batch, out, s) : launch_decode_t<__half, 4, 2>(p, batch, out, s);
 }
 
 // ---- fixed-scratch variant of the packed decode (no allocation anywhere)

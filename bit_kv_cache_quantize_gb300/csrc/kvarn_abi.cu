@@ -35,9 +35,10 @@ static kvarn_status check_config(const kvarn_config* c) {
     return KVARN_ERR_INVALID;
   if (c->num_q_heads % c->num_kv_heads) return KVARN_ERR_INVALID;
   if (c->dtype != KVARN_DTYPE_F16 && c->dtype != KVARN_DTYPE_BF16) return KVARN_ERR_INVALID;
-  // presets: kvarn_k4v2 (4-bit keys) and K2/V2 (2-bit keys); values are 2-bit
-  if (c->head_dim != 128 || c->tile_tokens != 128 || (c->k_bits != 4 && c->k_bits != 2) || c->v_bits != 2)
-    return KVARN_ERR_UNSUPPORTED;
+  // presets: kvarn_k4v2 (4-bit keys, 2-bit values), K2/V2 and K4/V4
+  const bool preset = (c->k_bits == 4 && c->v_bits == 2) || (c->k_bits == 2 && c->v_bits == 2) ||
+                      (c->k_bits == 4 && c->v_bits == 4);
+  if (c->head_dim != 128 || c->tile_tokens != 128 || !preset) return KVARN_ERR_UNSUPPORTED;
   if (c->num_q_heads / c->num_kv_heads > 8) return KVARN_ERR_UNSUPPORTED;
   return KVARN_OK;
 }
@@ -51,7 +52,7 @@ extern "C" {
 
 size_t kvarn_block_bytes(const kvarn_config* cfg) {
   if (check_config(cfg) != KVARN_OK) return 0;
-  return static_cast<size_t>(cfg->num_kv_heads) * head_rec(cfg->k_bits);
+  return static_cast<size_t>(cfg->num_kv_heads) * head_rec(cfg->k_bits, cfg->v_bits);
 }
 
 size_t kvarn_tail_bytes(const kvarn_config* cfg, int32_t batch) {
@@ -86,13 +87,14 @@ kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const 
   if (static_cast<int64_t>(n_tiles) * cfg->num_kv_heads * 2 > 0x7fffffffLL) return KVARN_ERR_INVALID;
   QuantizeParams p{k, v, token_stride_elems, n_tokens, tile_first_token, tile_dst_block,
                    static_cast<unsigned char*>(block_pool), static_cast<int64_t>(kvarn_block_bytes(cfg)),
-                   cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters, cfg->k_bits, dev_err};
+                   cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters, cfg->k_bits, cfg->v_bits, dev_err};
   return cuda_status(launch_quantize(p, cfg->dtype, n_tiles, static_cast<cudaStream_t>(stream)));
 }
 
 size_t kvarn_token_errors_scratch_bytes(const kvarn_config* cfg, int32_t n_tiles, int32_t is_v) {
   if (check_config(cfg) != KVARN_OK || n_tiles < 0) return 0;
-  return static_cast<size_t>(n_tiles) * cfg->num_kv_heads * static_cast<size_t>(is_v ? rec_bytes(2) : rec_bytes(cfg->k_bits));
+  return static_cast<size_t>(n_tiles) * cfg->num_kv_heads *
+         static_cast<size_t>(is_v ? rec_bytes(cfg->v_bits) : rec_bytes(cfg->k_bits));
 }
 
 kvarn_status kvarn_token_errors(const kvarn_config* cfg, const void* x, int64_t token_stride_elems, int64_t n_tokens,
@@ -112,7 +114,7 @@ kvarn_status kvarn_token_errors(const kvarn_config* cfg, const void* x, int64_t 
   if (static_cast<int64_t>(n_tiles) * cfg->num_kv_heads > 0x7fffffffLL) return KVARN_ERR_INVALID;
   if (scratch_bytes < kvarn_token_errors_scratch_bytes(cfg, n_tiles, is_v)) return KVARN_ERR_INVALID;
   ErrParams p{x, token_stride_elems, n_tokens, tile_first_token, static_cast<unsigned char*>(scratch), out,
-              cfg->num_kv_heads, sinkhorn_iters, cfg->k_bits, is_v, rotate, dev_err};
+              cfg->num_kv_heads, sinkhorn_iters, cfg->k_bits, cfg->v_bits, is_v, rotate, dev_err};
   return cuda_status(launch_token_errors(p, cfg->dtype, n_tiles, static_cast<cudaStream_t>(stream)));
 }
 
@@ -129,7 +131,7 @@ kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, con
     return KVARN_ERR_INVALID;
   AppendParams p{k_new, v_new, pos, block_table, max_blocks, cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters,
                  tail_pool, static_cast<unsigned char*>(block_pool), static_cast<int64_t>(kvarn_block_bytes(cfg)),
-                 cfg->k_bits, dev_err};
+                 cfg->k_bits, cfg->v_bits, dev_err};
   return cuda_status(launch_append(p, cfg->dtype, batch, static_cast<cudaStream_t>(stream)));
 }
 
@@ -159,7 +161,7 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
                  static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
                  max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads,
-                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits};
+                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits, cfg->v_bits};
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -205,7 +207,7 @@ kvarn_status kvarn_multiquery_attention(const kvarn_config* cfg, const void* q, 
   MQParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
              static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
              max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks,
-             n_queries, n_rb, chunk, n_chunks, cfg->k_bits};
+             n_queries, n_rb, chunk, n_chunks, cfg->k_bits, cfg->v_bits};
   return cuda_status(launch_multiquery(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -226,7 +228,7 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
   const int n_chunks = (max_blocks + chunk - 1) / chunk;
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool, nullptr, dev_err,
                  static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale, max_blocks, cfg->num_kv_heads,
-                 cfg->num_q_heads, G, cfg->num_blocks, chunk, n_chunks, cfg->k_bits};
+                 cfg->num_q_heads, G, cfg->num_blocks, chunk, n_chunks, cfg->k_bits, cfg->v_bits};
   return cuda_status(launch_decode_noalloc(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -241,7 +243,7 @@ kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q,
   const int n_chunks = (max_blocks + kF16ChunkTiles - 1) / kF16ChunkTiles;
   DecodeParams p{q, block_table, seq_lens, nullptr, nullptr, static_cast<float*>(workspace), dev_err, 0,
                  softmax_scale, max_blocks, cfg->num_kv_heads, cfg->num_q_heads,
-                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks, 16};
+                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks, 16, 16};
   cudaError_t e = launch_decode_f16(p, fp16_pool, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidValue) return KVARN_ERR_INVALID;
   if (e == cudaErrorNotSupported) return KVARN_ERR_UNSUPPORTED;
@@ -258,7 +260,8 @@ kvarn_status kvarn_dequantize(const kvarn_config* cfg, const void* block_pool, c
   if (cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
   return cuda_status(launch_dequantize(static_cast<const unsigned char*>(block_pool),
                                        static_cast<int64_t>(kvarn_block_bytes(cfg)), blocks, n, cfg->num_blocks,
-                                       cfg->num_kv_heads, cfg->k_bits, out, dev_err, static_cast<cudaStream_t>(stream)));
+                                       cfg->num_kv_heads, cfg->k_bits, cfg->v_bits, out, dev_err,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 const char* kvarn_status_string(kvarn_status s) {

@@ -63,10 +63,10 @@ constexpr uint32_t IDESC_PV = umma_idesc(128, D, 1);
 constexpr float MQ_TAU = 8.f;  // log2 headroom before the row reference moves
 
 struct MQSmem {
-  alignas(128) unsigned char qa[2][QA_BYTES];  // Q' hi, lo
+  alignas(128) unsigned char qa_lo[QA_BYTES];  // Q' lo (the hi half lives in tensor memory)
   alignas(128) unsigned char kt[2][KT_BYTES];
   alignas(128) unsigned char vt[VT_BYTES];
-  alignas(128) unsigned char rec[REC_STAGES][HEAD_REC];  // K record (either width) | V record
+  alignas(128) unsigned char rec[REC_STAGES][HEAD_REC_MAX];  // K record | V record (either widths)
   alignas(16) float ka[2][T], kb[2][T];  // aK, bK per token (per K~ stage)
   alignas(16) float va[2][T], vb[2][T];  // aV, bV per token
   alignas(16) float xmax[2][2][MQ_ROWS];  // tile maximum of each row half (exchanged between halves)
@@ -231,7 +231,30 @@ __device__ __forceinline__ void zero_v(unsigned char* vt, int c) {
 }
 
 // ---- producers: V~ row of channel c (128 tokens) plus its gV entries
+template <int VBITS>
 __device__ __forceinline__ void unpack_v(const unsigned char* vr, unsigned char* vt, int c) {
+  if constexpr (VBITS == 4) {
+    // 16 words of 8 tokens; token pair (2s, 2s + 1) of word w at bits 4s, 16 + 4s:
+    // shifted to bits 0 and 16, each field reads 128 + code in bf16
+    const float gv = e4m3_to_float(vr[c]);
+    const __nv_bfloat162 m0 = __float2bfloat162_rn(gv), a0 = __float2bfloat162_rn(-128.f * gv);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 c4 = *reinterpret_cast<const uint4*>(vr + 512 + 64 * c + 16 * q);
+      const uint32_t wv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t x = wv[e];
+        uint32_t o[4];
+#pragma unroll
+        for (int s2 = 0; s2 < 4; ++s2) o[s2] = fma_b(lop_magic(x >> (4 * s2), 0x000F000Fu, MAGIC_BF16), m0, a0);
+        *reinterpret_cast<uint4*>(vt + cm_off(c, 8 * (4 * q + e), VT_K / 8)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    const uint32_t g2 = b2u(m0);  // k 128..131: beta hi, lo of the two row halves
+    *reinterpret_cast<uint4*>(vt + cm_off(c, 128, VT_K / 8)) = make_uint4(g2, g2, 0u, 0u);
+    return;
+  }
   // a field at bit q reads 128 + 2^q code: times gV / 2^q, minus 128 gV / 2^q
   const float gv = e4m3_to_float(vr[c]);
   const __nv_bfloat162 m0 = __float2bfloat162_rn(gv), m2 = __float2bfloat162_rn(gv * 0.25f),
@@ -361,7 +384,7 @@ __device__ void mq_tail(const MQParams& p, int b, int h, int rb, int len, unsign
 
 // grid (n_chunks + 1, num_kv_heads * n_rowblocks, batch) x 416 threads;
 // chunk n_chunks handles the raw open tile.
-template <typename E, int KBITS>
+template <typename E, int KBITS, int VBITS>
 __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const int chunk = blockIdx.x, h = blockIdx.y / p.n_rowblocks, rb = blockIdx.y % p.n_rowblocks, b = blockIdx.z;
@@ -382,7 +405,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   const int first = chunk * p.chunk_tiles;
   const int n_tiles = min(p.chunk_tiles, n_need - first);
   if (n_tiles <= 0) return;
-  constexpr int KREC = rec_bytes(KBITS);
+  constexpr int KREC = rec_bytes(KBITS), VREC = rec_bytes(VBITS);
   MQSmem& sm = *reinterpret_cast<MQSmem*>(base);
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks + first;
 
@@ -489,15 +512,12 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
           hw[i] = h2u(hi);
           lw[i] = h2u(__floats2half2_rn(av[i] - hf.x, bv[i] - hf.y));
         }
-        *reinterpret_cast<uint4*>(sm.qa[0] + cm_off(row, 8 * g, 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(sm.qa[1] + cm_off(row, 8 * g, 16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        // hi: staged in the V~ buffer (free until the main loop), lo: the shared-memory operand
+        *reinterpret_cast<uint4*>(sm.vt + cm_off(row, 8 * g, 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(sm.qa_lo + cm_off(row, 8 * g, 16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
       }
       __syncwarp();
     }
-  } else if (warp < 12) {
-    const int pth = tid - 256;
-    // V~ columns 136..143 stay zero (K~ rows 129..143 are cleared after the prologue)
-    *reinterpret_cast<uint4*>(sm.vt + cm_off(pth, 136, VT_K / 8)) = make_uint4(0u, 0u, 0u, 0u);
   }
   fence_proxy_async();
   tc_fence_before();
@@ -513,7 +533,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       uint32_t w16[16];
 #pragma unroll
       for (int g2 = 0; g2 < 4; ++g2) {
-        const uint4 v4 = *reinterpret_cast<const uint4*>(sm.qa[0] + cm_off(row, 2 * c + 8 * g2, 16));
+        const uint4 v4 = *reinterpret_cast<const uint4*>(sm.vt + cm_off(row, 2 * c + 8 * g2, 16));
         w16[4 * g2] = v4.x; w16[4 * g2 + 1] = v4.y; w16[4 * g2 + 2] = v4.z; w16[4 * g2 + 3] = v4.w;
       }
       tmem_st16(lb + c, w16);
@@ -535,8 +555,8 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   auto issue_rec = [&](int k) {
     const int s = k % REC_STAGES;
     if ((vmask >> k) & 1u) {
-      mbar_expect_tx(&sm.rec_full[s], KREC + V_REC);
-      bulk_g2s(sm.rec[s], p.pool + tab[k] * p.block_bytes + (int64_t)h * (KREC + V_REC), KREC + V_REC,
+      mbar_expect_tx(&sm.rec_full[s], KREC + VREC);
+      bulk_g2s(sm.rec[s], p.pool + tab[k] * p.block_bytes + (int64_t)h * (KREC + VREC), KREC + VREC,
                &sm.rec_full[s]);
     } else {
       set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
@@ -546,7 +566,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   if (warp == 12) {
     // ------------------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
-      const uint64_t qa_lo = umma_desc(smem_u32(sm.qa[1]), 128, 2048);
+      const uint64_t qa_lo = umma_desc(smem_u32(sm.qa_lo), 128, 2048);
       auto issue_qk = [&](int k) {  // S[k & 1] = Q' K~^T over the hi then the lo query halves
         const uint32_t kb = smem_u32(sm.kt[k & 1]), d = tmem + TM_S + TM_SSTRIDE * (k & 1);
 #pragma unroll
@@ -598,6 +618,8 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   } else if (warp >= 8) {
     // ------------------------------------------------------------ producers
     const int pth = tid - 256;
+    // V~ columns 136..143 stay zero (the buffer held the query staging until the last barrier)
+    *reinterpret_cast<uint4*>(sm.vt + cm_off(pth, 136, VT_K / 8)) = make_uint4(0u, 0u, 0u, 0u);
     bool ok = true;
     for (int k = -1; k < n_tiles; ++k) {
       const int j = k + 1;  // K~ of the next tile first, then V~ of this one
@@ -636,7 +658,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       if (k >= 0) {
         if (k >= 1) ok = wait_all(&sm.pv_done, (k - 1) & 1, p.err);
         if (!ok) break;
-        if ((vmask >> k) & 1u) unpack_v(sm.rec[k % REC_STAGES] + KREC, sm.vt, pth);
+        if ((vmask >> k) & 1u) unpack_v<VBITS>(sm.rec[k % REC_STAGES] + KREC, sm.vt, pth);
         else zero_v(sm.vt, pth);
         fence_proxy_async();
         mbar_arrive(&sm.vt_full);
@@ -885,12 +907,13 @@ __global__ void __launch_bounds__(128) mq_combine_kernel(MQParams p, int batch, 
   *reinterpret_cast<float4*>(out + (((int64_t)b * p.n_queries + qi) * p.num_q_heads + hq) * D + 4 * lane) = o;
 }
 
-template <typename E, int KBITS>
+template <typename E, int KBITS, int VBITS>
 cudaError_t launch_mq_t(const MQParams& p, int batch, float* out, cudaStream_t s) {
   const size_t smem = sizeof(MQSmem) + 128;
-  cudaError_t e = cudaFuncSetAttribute(mq_kernel<E, KBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e =
+      cudaFuncSetAttribute(mq_kernel<E, KBITS, VBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  mq_kernel<E, KBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads * p.n_rowblocks, batch), MQ_THREADS, smem, s>>>(p);
+  mq_kernel<E, KBITS, VBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads * p.n_rowblocks, batch), MQ_THREADS, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.n_queries * p.num_q_heads;
@@ -902,10 +925,13 @@ cudaError_t launch_mq_t(const MQParams& p, int batch, float* out, cudaStream_t s
 
 cudaError_t launch_multiquery(const MQParams& p, int dtype, int batch, float* out, cudaStream_t s) {
   if (p.k_bits == 2)
-    return dtype == KVARN_DTYPE_BF16 ? launch_mq_t<__nv_bfloat16, 2>(p, batch, out, s)
-                                     : launch_mq_t<__half, 2>(p, batch, out, s);
-  return dtype == KVARN_DTYPE_BF16 ? launch_mq_t<__nv_bfloat16, 4>(p, batch, out, s)
-                                   : launch_mq_t<__half, 4>(p, batch, out, s);
+    return dtype == KVARN_DTYPE_BF16 ? launch_mq_t<__nv_bfloat16, 2, 2>(p, batch, out, s)
+                                     : launch_mq_t<__half, 2, 2>(p, batch, out, s);
+  if (p.v_bits == 4)
+    return dtype == KVARN_DTYPE_BF16 ? launch_mq_t<__nv_bfloat16, 4, 4>(p, batch, out, s)
+                                     : launch_mq_t<__half, 4, 4>(p, batch, out, s);
+  return dtype == KVARN_DTYPE_BF16 ? launch_mq_t<__nv_bfloat16, 4, 2>(p, batch, out, s)
+                                   : launch_mq_t<__half, 4, 2>(p, batch, out, s);
 }
 
 size_t multiquery_ws_bytes(int batch, int num_kv_heads, int n_rowblocks, int max_blocks, int chunk_tiles) {

@@ -10,9 +10,9 @@
 namespace kvarn {
 // Bytes of one (tile, head) record of one role: a 512-byte header (per-channel
 // and per-token FP8 scales, per-token FP16 zero-points) + 128 x 128 codes of
-// `bits` bits; a head holds its key record then its 2-bit value record.
+// `bits` bits; a head holds its key record then its value record.
 __host__ __device__ constexpr int rec_bytes(int bits) { return 512 + 128 * 128 * bits / 8; }
-__host__ __device__ constexpr int head_rec(int k_bits) { return rec_bytes(k_bits) + rec_bytes(2); }
+__host__ __device__ constexpr int head_rec(int k_bits, int v_bits) { return rec_bytes(k_bits) + rec_bytes(v_bits); }
 
 struct QuantizeParams {
   const void* k;
@@ -26,7 +26,8 @@ struct QuantizeParams {
   int32_t num_kv_heads;
   int32_t num_blocks;
   int32_t iters;
-  int32_t k_bits;  // 4 (kvarn_k4v2) or 2 (K2/V2); values are always 2-bit
+  int32_t k_bits;  // key code width: 4 or 2
+  int32_t v_bits;  // value code width: 2 or 4
   int32_t* err;
 };
 struct AppendParams {
@@ -42,6 +43,7 @@ struct AppendParams {
   unsigned char* pool;
   int64_t block_bytes;
   int32_t k_bits;
+  int32_t v_bits;
   int32_t* err;
 };
 struct DecodeParams {
@@ -62,6 +64,7 @@ struct DecodeParams {
   int32_t chunk_tiles;
   int32_t n_chunks;
   int32_t k_bits;
+  int32_t v_bits;
 };
 // Multi-query causal attention: n_queries query tokens per sequence at the
 // last n_queries positions, grouped with their GQA heads into row blocks of
@@ -86,6 +89,7 @@ struct MQParams {
   int32_t chunk_tiles;
   int32_t n_chunks;
   int32_t k_bits;
+  int32_t v_bits;
 };
 
 // Per-token reconstruction errors of quantised tiles (the error study):
@@ -100,6 +104,7 @@ struct ErrParams {
   int32_t num_kv_heads;
   int32_t iters;
   int32_t k_bits;
+  int32_t v_bits;
   int32_t is_v;
   int32_t rotate;
   int32_t* err;
@@ -109,7 +114,8 @@ cudaError_t launch_token_errors(const ErrParams& p, int dtype, int n_tiles, cuda
 cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cudaStream_t s);
 cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStream_t s);
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
-                              int num_blocks, int num_kv_heads, int k_bits, float* out, int32_t* err, cudaStream_t s);
+                              int num_blocks, int num_kv_heads, int k_bits, int v_bits, float* out, int32_t* err,
+                              cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s);
 cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* out, cudaStream_t s);
 cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,

@@ -98,8 +98,11 @@ __device__ __forceinline__ float pick8(const float (&v)[8], int lane) {
 constexpr int KIND_K4 = 0;  // 4-bit keys, token-major nibbles (kvarn_k4v2 preset)
 constexpr int KIND_V2 = 1;  // 2-bit values, channel-major even/odd token half-words
 constexpr int KIND_K2 = 2;  // 2-bit keys, token-major, four codes per byte (K2/V2 preset)
-__host__ __device__ constexpr int kind_levels(int kind) { return kind == KIND_K4 ? 15 : 3; }
-__host__ __device__ constexpr int kind_rec_bytes(int kind) { return kind == KIND_K4 ? K_REC : V_REC; }
+constexpr int KIND_V4 = 3;  // 4-bit values, channel-major even/odd token half-words (K4/V4 preset)
+__host__ __device__ constexpr int kind_levels(int kind) { return (kind == KIND_K4 || kind == KIND_V4) ? 15 : 3; }
+__host__ __device__ constexpr int kind_rec_bytes(int kind) {
+  return (kind == KIND_K4 || kind == KIND_V4) ? K_REC : V_REC;
+}
 
 struct AddOp { __device__ float operator()(float a, float b) const { return a + b; } };
 struct MinOp { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
@@ -156,6 +159,27 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
       const uint32_t word = __byte_perm(__byte_perm(u[0], u[1], 0x0040), __byte_perm(u[2], u[3], 0x0040), 0x5410);
       *reinterpret_cast<uint32_t*>(rec + 512 + (tok0 + i) * 64 + 4 * cb) = word;
     }
+  } else if constexpr (KIND == KIND_V4) {
+    // the thread's 8 tokens are one 32-bit word per channel: token tok0 + u at
+    // bit 2u (u even) or 14 + 2u (u odd)
+    uint32_t word[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) word[k] = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 ta = tokv[tok0 + i];
+      const float2 nb = make_float2(-ta.x, -ta.x), ia = make_float2(ta.y, ta.y);
+      const int sh = (i & 1) ? 14 + 2 * i : 2 * i;
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const float2 q2 = code2(r[i][pp], nb, ia);
+        word[2 * pp] |= (__float_as_uint(q2.x) & 15u) << sh;
+        word[2 * pp + 1] |= (__float_as_uint(q2.y) & 15u) << sh;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      *reinterpret_cast<uint32_t*>(rec + 512 + (8 * cb + k) * 64 + 4 * (tok0 >> 3)) = word[k];
   } else {
     uint32_t half[8];  // channel 8cb + k: even-token byte in bits 0-7, odd-token byte in bits 16-23
 #pragma unroll
@@ -489,8 +513,10 @@ __global__ void __launch_bounds__(256, 2) quantize_tiles_kernel(QuantizeParams p
     return;
   }
   const E* src = static_cast<const E*>(kv ? prm.v : prm.k) + first * prm.token_stride + h * D;
-  unsigned char* dst = prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits) + kv * rec_bytes(prm.k_bits);
-  if (kv) quantize_tile_cta<E, KIND_V2>(src, prm.token_stride, dst, prm.iters, sm);
+  unsigned char* dst =
+      prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits, prm.v_bits) + kv * rec_bytes(prm.k_bits);
+  if (kv && prm.v_bits == 4) quantize_tile_cta<E, KIND_V4>(src, prm.token_stride, dst, prm.iters, sm);
+  else if (kv) quantize_tile_cta<E, KIND_V2>(src, prm.token_stride, dst, prm.iters, sm);
   else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(src, prm.token_stride, dst, prm.iters, sm);
   else quantize_tile_cta<E, KIND_K2>(src, prm.token_stride, dst, prm.iters, sm);
 }
@@ -522,8 +548,10 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
   }
   __threadfence();
   __syncthreads();
-  unsigned char* dst = prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits) + kv * rec_bytes(prm.k_bits);
-  if (kv) quantize_tile_cta<E, KIND_V2>(tile, D, dst, prm.iters, sm);
+  unsigned char* dst =
+      prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits, prm.v_bits) + kv * rec_bytes(prm.k_bits);
+  if (kv && prm.v_bits == 4) quantize_tile_cta<E, KIND_V4>(tile, D, dst, prm.iters, sm);
+  else if (kv) quantize_tile_cta<E, KIND_V2>(tile, D, dst, prm.iters, sm);
   else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(tile, D, dst, prm.iters, sm);
   else quantize_tile_cta<E, KIND_K2>(tile, D, dst, prm.iters, sm);
 }
@@ -533,7 +561,8 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
 // in-register fast Walsh-Hadamard transform.
 __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __restrict__ pool, int64_t block_bytes,
                                                          const int32_t* __restrict__ blocks, int32_t num_blocks,
-                                                         int32_t num_kv_heads, int32_t k_bits, float* __restrict__ out,
+                                                         int32_t num_kv_heads, int32_t k_bits, int32_t v_bits,
+                                                         float* __restrict__ out,
                                                          int32_t* err) {
   __shared__ __align__(16) unsigned char rec[K_REC];
   const int n = blockIdx.x, h = blockIdx.y, kv = blockIdx.z, t = threadIdx.x;
@@ -542,8 +571,8 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
     if (t == 0) set_error(err, KVARN_DEV_ERR_BLOCK_RANGE);
     return;
   }
-  const unsigned char* src = pool + blk * block_bytes + h * head_rec(k_bits) + kv * rec_bytes(k_bits);
-  const int bytes = kv ? V_REC : rec_bytes(k_bits);
+  const unsigned char* src = pool + blk * block_bytes + h * head_rec(k_bits, v_bits) + kv * rec_bytes(k_bits);
+  const int bytes = kv ? rec_bytes(v_bits) : rec_bytes(k_bits);
   for (int i = t; i < bytes / 16; i += 128)
     reinterpret_cast<uint4*>(rec)[i] = reinterpret_cast<const uint4*>(src)[i];
   __syncthreads();
@@ -552,8 +581,10 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
   float x[D];
 #pragma unroll
   for (int c = 0; c < D; ++c) {
-    const int vb = (t & 1) ? 15 + (t & 15) : (t & 15);  // bit of token t in its V word
-    int code = kv ? (rec[512 + c * 32 + 4 * (t >> 4) + (vb >> 3)] >> (vb & 7)) & 3
+    const int vb = (t & 1) ? 15 + (t & 15) : (t & 15);          // bit of token t in its 2-bit V word
+    const int vb4 = (t & 1) ? 14 + 2 * (t & 7) : 2 * (t & 7);  // bit of token t in its 4-bit V word
+    int code = kv ? (v_bits == 4 ? (rec[512 + c * 64 + 4 * (t >> 3) + (vb4 >> 3)] >> (vb4 & 7)) & 15
+                                 : (rec[512 + c * 32 + 4 * (t >> 4) + (vb >> 3)] >> (vb & 7)) & 3)
                : k_bits == 4 ? (rec[512 + t * 64 + (c >> 1)] >> (4 * (c & 1))) & 15
                              : (rec[512 + t * 32 + (c >> 2)] >> (2 * (c & 3))) & 3;
     x[c] = e4m3_to_float(rec[c]) * fmaf(a, static_cast<float>(code), b);
@@ -615,6 +646,9 @@ __global__ void __launch_bounds__(256, 2) token_errors_kernel(ErrParams prm) {
     if constexpr (KIND == KIND_V2) {
       const int vb = (t & 1) ? 15 + (t & 15) : (t & 15);  // bit of token t in its channel word
       code = (rec[512 + c * 32 + 4 * (t >> 4) + (vb >> 3)] >> (vb & 7)) & 3;
+    } else if constexpr (KIND == KIND_V4) {
+      const int vb = (t & 1) ? 14 + 2 * (t & 7) : 2 * (t & 7);
+      code = (rec[512 + c * 64 + 4 * (t >> 3) + (vb >> 3)] >> (vb & 7)) & 15;
     } else if constexpr (KIND == KIND_K4) {
       code = (rec[512 + t * 64 + (c >> 1)] >> (4 * (c & 1))) & 15;
     } else {
@@ -677,7 +711,7 @@ static cudaError_t launch_errors_k(const ErrParams& p, int n_tiles, cudaStream_t
 
 template <typename E>
 static cudaError_t launch_errors_t(const ErrParams& p, int n_tiles, cudaStream_t s) {
-  if (p.is_v) return launch_errors_k<E, KIND_V2>(p, n_tiles, s);
+  if (p.is_v) return p.v_bits == 4 ? launch_errors_k<E, KIND_V4>(p, n_tiles, s) : launch_errors_k<E, KIND_V2>(p, n_tiles, s);
   return p.k_bits == 2 ? launch_errors_k<E, KIND_K2>(p, n_tiles, s) : launch_errors_k<E, KIND_K4>(p, n_tiles, s);
 }
 
@@ -704,9 +738,10 @@ cudaError_t launch_append(const AppendParams& p, int dtype, int batch, cudaStrea
 }
 
 cudaError_t launch_dequantize(const unsigned char* pool, int64_t block_bytes, const int32_t* blocks, int n,
-                              int num_blocks, int num_kv_heads, int k_bits, float* out, int32_t* err, cudaStream_t s) {
+                              int num_blocks, int num_kv_heads, int k_bits, int v_bits, float* out, int32_t* err,
+                              cudaStream_t s) {
   dequantize_kernel<<<dim3(n, num_kv_heads, 2), 128, 0, s>>>(pool, block_bytes, blocks, num_blocks, num_kv_heads,
-                                                              k_bits, out, err);
+                                                              k_bits, v_bits, out, err);
   return cudaGetLastError();
 }
 

@@ -61,7 +61,7 @@ def measure(w, kv: str, rotate: int, iters, seqs=None, device="cuda"):
 
     seqs = list(range(w.batch)) if seqs is None else seqs
     iters = w.extra.get("iters", 8) if iters is None else iters
-    cfg = K.make_config(w.num_kv_heads, w.num_q_heads, 1, w.dtype, k_bits=w.k_bits)
+    cfg = K.make_config(w.num_kv_heads, w.num_q_heads, 1, w.dtype, k_bits=w.k_bits, v_bits=w.v_bits)
     err = torch.zeros(1, dtype=torch.int32, device=device)
     e_all, n_all = [], []
     for b in seqs:
@@ -102,13 +102,14 @@ def main():
                     choices=["single_tile", "qwen3_4b_layer", "qwen3_32b_decode_16k"])
     ap.add_argument("--kv", default="k", choices=["k", "v"])
     ap.add_argument("--k-bits", type=int, default=4, choices=[4, 2])
+    ap.add_argument("--v-bits", type=int, default=2, choices=[2, 4])
     ap.add_argument("--seqs", type=int, default=2, help="sequences of the workload to measure")
     args = ap.parse_args()
     B.build()
     w = {"single_tile": I.single_tile, "qwen3_4b_layer": I.qwen3_4b, "qwen3_32b_decode_16k": I.qwen3_32b}[args.workload]()
-    w.k_bits = args.k_bits
+    w.k_bits, w.v_bits = args.k_bits, args.v_bits
     res = ablation(w, args.kv, seqs=list(range(min(args.seqs, w.batch))))
-    print(json.dumps({"workload": w.name, "kv": args.kv, "k_bits": w.k_bits, "variants": res}))
+    print(json.dumps({"workload": w.name, "kv": args.kv, "k_bits": w.k_bits, "v_bits": w.v_bits, "variants": res}))
 
 
 if __name__ == "__main__":

@@ -116,7 +116,8 @@ class Workload:
     max_tokens: int = 0             # token stride of the generated K/V streams
     block_perm: bool = False        # physical blocks randomly permuted
     extra: dict = field(default_factory=dict)
-    k_bits: int = 4                 # key code width: 4 (kvarn_k4v2 preset) or 2 (K2/V2 preset)
+    k_bits: int = 4                 # key code width: 4 (kvarn_k4v2, K4/V4 presets) or 2 (K2/V2 preset)
+    v_bits: int = 2                 # value code width: 2, or 4 (K4/V4 preset)
 
     @property
     def G(self) -> int:

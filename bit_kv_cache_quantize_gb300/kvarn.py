@@ -28,9 +28,9 @@ def rec_bytes(bits: int) -> int:
     return 512 + 128 * 128 * bits // 8
 
 
-def head_rec(k_bits: int = 4) -> int:
-    """Bytes of one head of a block: key record then 2-bit value record."""
-    return rec_bytes(k_bits) + V_REC
+def head_rec(k_bits: int = 4, v_bits: int = 2) -> int:
+    """Bytes of one head of a block: key record then value record."""
+    return rec_bytes(k_bits) + rec_bytes(v_bits)
 
 # every function declared in include/kvarn.h
 EXPORTS = (

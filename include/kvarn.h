@@ -46,20 +46,26 @@
  *     half-word, 2 bits each.
  *   K2 record 4608 B (k_bits = 2): same 512-byte header | codes[128 tokens]
  *     [32 B], byte i of token t = sum over k < 4 of code[t][4i+k] << 2k.
+ *   V4 record 8704 B (v_bits = 4): same 512-byte header | codes[128
+ *     channels][64 B]: channel c holds 16 little-endian 32-bit words; word w
+ *     carries tokens 8w .. 8w+7, token 8w+u at bit 2u (u even) or 14+2u (u
+ *     odd), 4 bits each.
  *   Block b of the pool = for each KV head h: [K record | V record], i.e.
- *     num_kv_heads * R bytes with R = 13312 (k_bits 4) or 9216 (k_bits 2);
- *     head h of block b starts at b * kvarn_block_bytes() + h * R.
+ *     num_kv_heads * R bytes with R = 13312 (K4/V2), 9216 (K2/V2) or 17408
+ *     (K4/V4); head h of block b starts at b * kvarn_block_bytes() + h * R.
  *   Dequantised value (rotated domain): R[t][c] = g[c] * (a[t]*code + b[t]);
  *   the cache value is R H with H the 128-point Sylvester Hadamard matrix
  *   divided by sqrt(128).  4.25 bits/element for K, 2.25 for V (and for
  *   2-bit K).
  *
  * Presets: k_bits = 4, v_bits = 2 is kvarn_k4v2_g128, the one the pages
- * ship.  k_bits = 2, v_bits = 2 (2-bit keys, levels 0..3) follows the same
- * kvarn_k<bits>v<bits>_g<tile> naming ("Huawei's KVarN puts KV-cache
- * quantization inside vLLM's backend", section "What KVarN changes in
- * vLLM's serving path"); the pages name no other preset, so its record is
- * the K4 record with the code field narrowed to 2 bits.
+ * ship.  k_bits = 2, v_bits = 2 (2-bit keys) and k_bits = 4, v_bits = 4
+ * (4-bit values, levels 0..15) follow the same kvarn_k<bits>v<bits>_g<tile>
+ * naming ("Huawei's KVarN puts KV-cache quantization inside vLLM's
+ * backend", section "What KVarN changes in vLLM's serving path"); the pages
+ * name no other preset, so their records are the shipped ones with the code
+ * field narrowed or widened.  Other combinations return
+ * KVARN_ERR_UNSUPPORTED.
  */
 #ifndef KVARN_H
 #define KVARN_H
@@ -95,13 +101,14 @@ typedef struct kvarn_config {
   int32_t num_q_heads;    /* query heads; a multiple of num_kv_heads with group size <= 8 */
   int32_t num_blocks;     /* blocks in the packed block pool (device bounds check) */
   int32_t k_bits;         /* key code width; 4 or 2 */
-  int32_t v_bits;         /* value code width; must be 2 */
+  int32_t v_bits;         /* value code width; 2, or 4 with k_bits = 4 */
   int32_t sinkhorn_iters; /* normalisation iterations, 0..64 (the preset uses 8) */
   int32_t dtype;          /* kvarn_dtype of K/V/query inputs and of the open-tile buffer */
 } kvarn_config;
 
-/* Bytes of one block of the packed pool: num_kv_heads * 13312 (k_bits 4) or
- * num_kv_heads * 9216 (k_bits 2).  0 if cfg is invalid. */
+/* Bytes of one block of the packed pool: num_kv_heads * (K record + V
+ * record): 13312 (K4/V2), 9216 (K2/V2) or 17408 (K4/V4).  0 if cfg is
+ * invalid. */
 size_t kvarn_block_bytes(const kvarn_config* cfg);
 
 /* Bytes of the open-tile (tail) buffer for `batch` sequences:

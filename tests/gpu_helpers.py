@@ -35,19 +35,19 @@ def tile_values(x16: torch.Tensor, dtype: str) -> np.ndarray:
     return O.decode16(bits(x16), dtype)
 
 
-def oracle_tiles(jobs, dtype: str, iters: int = 8, k_bits: int = 4):
+def oracle_tiles(jobs, dtype: str, iters: int = 8, k_bits: int = 4, v_bits: int = 2):
     """jobs: list of (tile16 [128,128] tensor, is_v).  Returns oracle Tiles."""
     def one(job):
         x16, is_v = job
-        return O.quantize_tile(tile_values(x16, dtype), O.levels(is_v, k_bits), iters)
+        return O.quantize_tile(tile_values(x16, dtype), O.levels(is_v, k_bits, v_bits), iters)
     with concurrent.futures.ThreadPoolExecutor(NTHREADS) as ex:
         return list(ex.map(one, jobs))
 
 
-def oracle_attention_units(units, scale, k_bits: int = 4):
+def oracle_attention_units(units, scale, k_bits: int = 4, v_bits: int = 2):
     """units: list of dicts with q [G,D] fp64, krec/vrec lists, ktail/vtail
     [n,D] fp64.  Folded-form oracle attention of each unit (threads)."""
     def one(u):
-        return O.attention_folded(u["q"], u["krec"], u["vrec"], u["ktail"], u["vtail"], scale, k_bits)
+        return O.attention_folded(u["q"], u["krec"], u["vrec"], u["ktail"], u["vtail"], scale, k_bits, v_bits)
     with concurrent.futures.ThreadPoolExecutor(NTHREADS) as ex:
         return list(ex.map(one, units))

@@ -36,7 +36,7 @@ def f16_order(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
-def unpack(rec: np.ndarray, is_v: bool, k_bits: int = 4):
+def unpack(rec: np.ndarray, is_v: bool, k_bits: int = 4, v_bits: int = 2):
     rec = np.ascontiguousarray(rec, dtype=np.uint8)
     g8 = rec[:128].copy()
     a8 = rec[128:256].copy()
@@ -50,6 +50,11 @@ def unpack(rec: np.ndarray, is_v: bool, k_bits: int = 4):
         code = np.empty((T, D), np.uint8)
         code[:, 0::2] = by & 15
         code[:, 1::2] = by >> 4
+    elif v_bits == 4:
+        words = body.view("<u4").reshape(D, T // 8)   # [channel][word]: tokens 8w .. 8w+7
+        pos = np.array([2 * u if u % 2 == 0 else 14 + 2 * u for u in range(8)], dtype=np.uint32)
+        nib = (words[:, :, None] >> pos[None, None, :]) & 15  # [c][w][u] -> token 8w+u
+        code = nib.reshape(D, T).T.astype(np.uint8).copy()
     else:
         words = body.view("<u4").reshape(D, T // 16)  # [channel][word]: tokens 16w .. 16w+15
         pos = np.array([u if u % 2 == 0 else 15 + u for u in range(16)], dtype=np.uint32)
@@ -69,10 +74,11 @@ class Stats:
                 f"b_flip={self.b_flip} tie_diff={self.tie_diff} checked_vs_own_scales={self.valid_checked}")
 
 
-def compare_record(gpu_rec: np.ndarray, tile, is_v: bool, st: Stats, where: str = "", k_bits: int = 4):
+def compare_record(gpu_rec: np.ndarray, tile, is_v: bool, st: Stats, where: str = "", k_bits: int = 4,
+                   v_bits: int = 2):
     """tile: oracle.Tile of the same input."""
-    L = 3 if (is_v or k_bits == 2) else 15
-    g8, a8, b16, code = unpack(gpu_rec, is_v, k_bits)
+    L = 15 if (v_bits if is_v else k_bits) == 4 else 3
+    g8, a8, b16, code = unpack(gpu_rec, is_v, k_bits, v_bits)
     st.tiles += 1
     st.codes += code.size
     assert code.max() <= L, where

@@ -40,7 +40,10 @@ def test_sizes(lib):
     assert K.kvarn_fp16_block_bytes(cfg) == 8 * 65536
     cfg2 = K.make_config(8, 64, 100, "f16", k_bits=2)
     assert K.kvarn_block_bytes(cfg2) == 8 * 9216  # 2-bit keys: two 4608-byte records per head
-    assert K.head_rec(2) == 9216 and K.head_rec(4) == 13312
+    assert K.head_rec(2) == 9216 and K.head_rec(4) == 13312 and K.head_rec(4, 4) == 17408
+    cfg44 = K.make_config(8, 64, 100, "f16", k_bits=4, v_bits=4)
+    assert K.kvarn_block_bytes(cfg44) == 8 * 17408  # K4/V4: two 8704-byte records per head
+    assert K.kvarn_block_bytes(K.make_config(8, 64, 100, "f16", k_bits=2, v_bits=4)) == 0  # not a preset
     ws = K.kvarn_decode_workspace_bytes(cfg, 32, 128)
     assert ws == 32 * 8 * (8 + 1) * 8 * 132 * 4  # the 16-bit kernel's chunks of 16 tiles + open tile bound it
 
@@ -48,7 +51,7 @@ def test_sizes(lib):
 @pytest.mark.parametrize("field,value,status", [
     ("head_dim", 64, K.KVARN_ERR_UNSUPPORTED), ("tile_tokens", 64, K.KVARN_ERR_UNSUPPORTED),
     ("k_bits", 3, K.KVARN_ERR_UNSUPPORTED), ("k_bits", 8, K.KVARN_ERR_UNSUPPORTED),
-    ("v_bits", 4, K.KVARN_ERR_UNSUPPORTED),
+    ("v_bits", 3, K.KVARN_ERR_UNSUPPORTED), ("v_bits", 8, K.KVARN_ERR_UNSUPPORTED),
     ("num_q_heads", 12, K.KVARN_ERR_INVALID), ("num_q_heads", 128, K.KVARN_ERR_UNSUPPORTED),
     ("num_kv_heads", 0, K.KVARN_ERR_INVALID), ("dtype", 7, K.KVARN_ERR_INVALID),
     ("sinkhorn_iters", -1, K.KVARN_ERR_INVALID), ("sinkhorn_iters", 65, K.KVARN_ERR_INVALID),

@@ -57,13 +57,14 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
             for h in range(w.num_kv_heads):
                 jobs += [(full_k[:, h], 0), (full_v[:, h], 1)]
                 keys += [(b, t, h, 0), (b, t, h, 1)]
-        tiles = oracle_tiles(jobs, w.dtype, k_bits=w.k_bits)
+        tiles = oracle_tiles(jobs, w.dtype, k_bits=w.k_bits, v_bits=w.v_bits)
         for (b, t, h, kv), tl in zip(keys, tiles):
             blk = int(c.table[b, t])
             PR.compare_record(c.record(blk, h, kv).cpu().numpy(), tl, bool(kv), st,
-                              where=f"step {s} seq {b} closed tile {t} head {h} kv {kv}", k_bits=w.k_bits)
+                              where=f"step {s} seq {b} closed tile {t} head {h} kv {kv}", k_bits=w.k_bits,
+                              v_bits=w.v_bits)
             if b in ctx:  # decode parity reads oracle records only
-                rec = O.pack_record(bool(kv), tl, w.k_bits)
+                rec = O.pack_record(bool(kv), tl, w.k_bits, w.v_bits)
                 recs[(b, t, h, kv)] = rec
                 c.set_record(blk, h, kv, torch.from_numpy(rec).to(dev))
         if s % attend_every and s != steps - 1:
@@ -85,7 +86,7 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
                                   ktail=O.decode16(bits(k[nf * T:n, h]), w.dtype).reshape(-1, D),
                                   vtail=O.decode16(bits(v[nf * T:n, h]), w.dtype).reshape(-1, D)))
                 ukeys.append((b, h))
-        for (b, h), o in zip(ukeys, oracle_attention_units(units, w.scale, w.k_bits)):
+        for (b, h), o in zip(ukeys, oracle_attention_units(units, w.scale, w.k_bits, w.v_bits)):
             worst = max(worst, np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max())
     print(w.name, PR.finish(st), f"max |gpu - oracle| = {worst:.3e}")
     assert worst <= TOL
@@ -106,6 +107,13 @@ def test_k2_append_close_small():
     assert st.tiles == 4 * 2 * 2
 
 
+def test_v4_append_close_small():
+    w = I.Workload("append_small_v4", 6, 16, 2, "bf16", [125, 126, 127, 255, 300, 10], seed=49, decode_steps=4,
+                   max_tokens=310, block_perm=True, v_dist="t4", v_bits=4)
+    st = run_steps(w, 4)
+    assert st.tiles == 4 * 2 * 2
+
+
 def test_append_close_bf16():
     w = I.Workload("append_bf16", 3, 8, 2, "bf16", [127, 383, 5], seed=43, decode_steps=2, max_tokens=400,
                    v_dist="t4", k_outliers="random", block_perm=True)
@@ -114,10 +122,12 @@ def test_append_close_bf16():
 
 @pytest.mark.slow
 def test_ragged_serving_full_size_sampled():
-    """256 sequences, lengths U[128, 32768], 64 decode steps; every closing
-    tile is checked, attention on 6 sampled sequences every 16 steps."""
+    """256 sequences, lengths U[128, 32768], 64 decode steps; every tile that
+    closes (any sequence) is compared with the oracle, and attention on 8
+    sampled sequences (4 of them closing a tile during the run) after every
+    step."""
     w = I.ragged_32b()
     lens = np.array(w.seq_lens)
     closing = [b for b in range(w.batch) if (lens[b] % T) + 64 >= T][:4]
-    others = [b for b in range(w.batch) if b not in closing][:2]
-    run_steps(w, 64, check_seqs=closing + others, attend_every=16)
+    others = [b for b in range(w.batch) if b not in closing][:4]
+    run_steps(w, 64, check_seqs=closing + others, attend_every=1)

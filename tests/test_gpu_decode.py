@@ -31,9 +31,9 @@ def load_oracle_records(w, c: PagedCache, seqs, ctx):
                 for kv, src in ((0, k), (1, v)):
                     jobs.append((src[t * T:(t + 1) * T, h], kv))
                     keys.append((b, t, h, kv))
-    tiles = oracle_tiles(jobs, w.dtype, k_bits=w.k_bits)
+    tiles = oracle_tiles(jobs, w.dtype, k_bits=w.k_bits, v_bits=w.v_bits)
     for (b, t, h, kv), tl in zip(keys, tiles):
-        rec = O.pack_record(bool(kv), tl, w.k_bits)
+        rec = O.pack_record(bool(kv), tl, w.k_bits, w.v_bits)
         recs[(b, t, h, kv)] = rec
         c.set_record(int(c.table[b, t]), h, kv, torch.from_numpy(rec).to(c.device))
     for b in seqs:
@@ -62,7 +62,7 @@ def oracle_outputs(w, seqs, ctx, recs, q, lens=None):
                 ktail=O.decode16(bits(k[n_full * T:n, h]), w.dtype).reshape(-1, D),
                 vtail=O.decode16(bits(v[n_full * T:n, h]), w.dtype).reshape(-1, D)))
             keys.append((b, h))
-    outs = oracle_attention_units(units, w.scale, w.k_bits)
+    outs = oracle_attention_units(units, w.scale, w.k_bits, w.v_bits)
     return dict(zip(keys, outs))
 
 
@@ -124,6 +124,24 @@ def test_k2_qwen3_4b_layer():
 def test_k2_ragged_tails_and_empty_sequence():
     w = ragged_small()
     w.k_bits = 2
+    run_decode_case(w)
+
+
+def test_v4_single_tile():
+    w = I.single_tile()
+    w.v_bits = 4
+    run_decode_case(w)
+
+
+def test_v4_qwen3_4b_layer():
+    w = I.qwen3_4b()
+    w.v_bits = 4
+    run_decode_case(w)
+
+
+def test_v4_ragged_tails_and_empty_sequence():
+    w = ragged_small()
+    w.v_bits = 4
     run_decode_case(w)
 
 

@@ -21,7 +21,7 @@ T = D = 128
 def gpu_errors(w, x, n_tiles, is_v, rotate, iters):
     """(out [n_tiles, H, 128, 2], scratch records [n_tiles, H, record bytes])."""
     dev = device()
-    cfg = K.make_config(w.num_kv_heads, w.num_q_heads, 1, w.dtype, k_bits=w.k_bits)
+    cfg = K.make_config(w.num_kv_heads, w.num_q_heads, 1, w.dtype, k_bits=w.k_bits, v_bits=w.v_bits)
     first = torch.arange(n_tiles, dtype=torch.int64, device=dev) * T
     sb = K.kvarn_token_errors_scratch_bytes(cfg, n_tiles, is_v)
     scratch = torch.empty(sb, dtype=torch.uint8, device=dev)
@@ -34,15 +34,16 @@ def gpu_errors(w, x, n_tiles, is_v, rotate, iters):
     return out.cpu().numpy().astype(np.float64), scratch.cpu().numpy().reshape(n_tiles, w.num_kv_heads, -1)
 
 
-@pytest.mark.parametrize("kv,k_bits,dtype", [("k", 4, "bf16"), ("v", 4, "bf16"), ("k", 2, "f16")])
+@pytest.mark.parametrize("kv,k_bits,v_bits,dtype", [("k", 4, 2, "bf16"), ("v", 4, 2, "bf16"), ("k", 2, 2, "f16"),
+                                                    ("v", 4, 4, "bf16")])
 @pytest.mark.parametrize("variant", list(E.VARIANTS))
-def test_token_errors_match_oracle(kv, k_bits, dtype, variant):
+def test_token_errors_match_oracle(kv, k_bits, v_bits, dtype, variant):
     """The records the kernel quantised follow the record parity rule (scales
     within one code, flips counted; codes exact where the scales agree);
     per-token errors agree to 1e-3 wherever a token's scales and all channel
     scales of its tile agree; the distribution statistics agree to 2 %."""
     w = I.qwen3_4b() if dtype == "bf16" else I.qwen3_32b()
-    w.k_bits = k_bits
+    w.k_bits, w.v_bits = k_bits, v_bits
     rotate, iters = E.VARIANTS[variant]
     iters = 8 if iters is None else iters
     n_tiles, is_v = 3, kv == "v"
@@ -53,20 +54,20 @@ def test_token_errors_match_oracle(kv, k_bits, dtype, variant):
     def one(job):
         t, h = job
         X = tile_values(x[t * T:(t + 1) * T, h], w.dtype)
-        tl = O.quantize_tile(X, O.levels(is_v, k_bits), iters, bool(rotate))
-        return tl, O.token_errors(X, is_v, k_bits, iters, bool(rotate))
+        tl = O.quantize_tile(X, O.levels(is_v, k_bits, v_bits), iters, bool(rotate))
+        return tl, O.token_errors(X, is_v, k_bits, iters, bool(rotate), v_bits)
     with concurrent.futures.ThreadPoolExecutor(NTHREADS) as ex:
         want = dict(zip(jobs, ex.map(one, jobs)))
     st = PR.Stats()
     e_g, n_g, e_w, n_w, same = [], [], [], [], []
     for (t, h), (tl, (e2, n2)) in want.items():
         rec = recs[t, h]
-        PR.compare_record(rec, tl, is_v, st, where=f"tile {t} head {h}", k_bits=k_bits)
-        g8, a8, b16, _ = PR.unpack(rec, is_v, k_bits)
+        PR.compare_record(rec, tl, is_v, st, where=f"tile {t} head {h}", k_bits=k_bits, v_bits=v_bits)
+        g8, a8, b16, _ = PR.unpack(rec, is_v, k_bits, v_bits)
         tok_same = (a8 == tl.a8) & (b16 == tl.b16) & bool((g8 == tl.g8).all())
         e_g.append(got[t, h, :, 0]); n_g.append(got[t, h, :, 1]); e_w.append(e2); n_w.append(n2)
         same.append(tok_same)
-    print(variant, kv, k_bits, dtype, PR.finish(st))
+    print(variant, kv, k_bits, v_bits, dtype, PR.finish(st))
     e_g, n_g, e_w, n_w, same = map(np.concatenate, (e_g, n_g, e_w, n_w, same))
     assert np.all(np.abs(n_g - n_w) <= 1e-5 * n_w + 1e-30)
     close = np.abs(e_g - e_w) <= 1e-3 * e_w + 1e-6 * n_w

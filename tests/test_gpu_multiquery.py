@@ -31,7 +31,7 @@ def oracle_mq(w, seqs, ctx, recs, q, Q):
         nf = n // T
         Kc, Vc = O.cache_values([recs[(b, t, h, 0)] for t in range(nf)], [recs[(b, t, h, 1)] for t in range(nf)],
                                 O.decode16(bits(k[nf * T:, h]), w.dtype), O.decode16(bits(v[nf * T:, h]), w.dtype),
-                                w.k_bits)
+                                w.k_bits, w.v_bits)
         qq = O.decode16(bits(q[b, :, h * G:(h + 1) * G]), w.dtype).reshape(Q, G, D)
         return O.causal_attention(qq, Kc, Vc, w.scale)
 
@@ -99,6 +99,12 @@ def test_whole_sequence_is_queries():
 def test_k2_keys_group4():
     w = I.Workload("mq_k2", 3, 8, 2, "f16", [700, 129, 1500], seed=56, max_tokens=1500, block_perm=True, k_bits=2)
     run_mq_case(w, 8)
+
+
+def test_v4_values_group8():
+    w = I.Workload("mq_v4", 2, 16, 2, "bf16", [900, 400], seed=59, max_tokens=900, block_perm=True, v_dist="t4",
+                   v_bits=4)
+    run_mq_case(w, 16)
 
 
 def test_single_query_matches_decode_oracle():

@@ -35,13 +35,13 @@ def quantize_and_compare(w, seqs, sample=None, seed=0):
         rng = np.random.default_rng(seed)
         jobs = [jobs[i] for i in rng.choice(len(jobs), sample, replace=False)]
     tiles = oracle_tiles([(ctx[b][kv][t * T:(t + 1) * T, h], kv) for b, t, h, kv in jobs], w.dtype,
-                         k_bits=w.k_bits)
+                         k_bits=w.k_bits, v_bits=w.v_bits)
     st = PR.Stats()
     for (b, t, h, kv), tl in zip(jobs, tiles):
         blk = int(c.table[b, t])
         rec = c.record(blk, h, kv).cpu().numpy()
         PR.compare_record(rec, tl, bool(kv), st, where=f"seq {b} tile {t} head {h} {'V' if kv else 'K'}",
-                          k_bits=w.k_bits)
+                          k_bits=w.k_bits, v_bits=w.v_bits)
     print(w.name, PR.finish(st))
     return st
 
@@ -61,6 +61,19 @@ def test_k2_single_tile():
     w.k_bits = 2
     st = quantize_and_compare(w, [0])
     assert st.tiles == 2
+
+
+def test_v4_single_tile():
+    w = I.single_tile()
+    w.v_bits = 4
+    st = quantize_and_compare(w, [0])
+    assert st.tiles == 2
+
+
+def test_v4_qwen3_4b_layer_all_tiles():
+    w = I.qwen3_4b()
+    w.v_bits = 4
+    quantize_and_compare(w, list(range(w.batch)))
 
 
 def test_k2_qwen3_4b_layer_all_tiles():
@@ -119,12 +132,12 @@ def degenerate_tiles(dtype):
     return t.reshape(-1, 1, D)
 
 
-@pytest.mark.parametrize("dtype,k_bits", [("f16", 4), ("bf16", 4), ("f16", 2)])
-def test_degenerate_tiles(dtype, k_bits):
+@pytest.mark.parametrize("dtype,k_bits,v_bits", [("f16", 4, 2), ("bf16", 4, 2), ("f16", 2, 2), ("bf16", 4, 4)])
+def test_degenerate_tiles(dtype, k_bits, v_bits):
     dev = device()
     kv = degenerate_tiles(dtype).to(dev)
     n_tiles = kv.shape[0] // T
-    cfg = K.make_config(1, 1, n_tiles, dtype, k_bits=k_bits)
+    cfg = K.make_config(1, 1, n_tiles, dtype, k_bits=k_bits, v_bits=v_bits)
     pool = torch.zeros(n_tiles * K.kvarn_block_bytes(cfg), dtype=torch.uint8, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     first = torch.arange(n_tiles, dtype=torch.int64, device=dev) * T
@@ -133,16 +146,16 @@ def test_degenerate_tiles(dtype, k_bits):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     tiles = oracle_tiles([(kv[i * T:(i + 1) * T, 0], is_v) for i in range(n_tiles) for is_v in (0, 1)], dtype,
-                         k_bits=k_bits)
+                         k_bits=k_bits, v_bits=v_bits)
     st = PR.Stats()
     bb = K.kvarn_block_bytes(cfg)
     kr = K.rec_bytes(k_bits)
     for idx, tl in enumerate(tiles):
         i, is_v = divmod(idx, 2)
         blk = int(dst[i])
-        rec = pool[blk * bb + is_v * kr: blk * bb + is_v * kr + (K.V_REC if is_v else kr)]
+        rec = pool[blk * bb + is_v * kr: blk * bb + is_v * kr + K.rec_bytes(v_bits if is_v else k_bits)]
         PR.compare_record(rec.cpu().numpy(), tl, bool(is_v), st, where=f"degenerate tile {i} {'V' if is_v else 'K'}",
-                          k_bits=k_bits)
+                          k_bits=k_bits, v_bits=v_bits)
     print(PR.finish(st))
 
 
@@ -163,8 +176,8 @@ def test_other_sinkhorn_counts(iters):
     PR.finish(st)
 
 
-@pytest.mark.parametrize("k_bits", [4, 2])
-def test_dequantize_matches_oracle(k_bits):
+@pytest.mark.parametrize("k_bits,v_bits", [(4, 2), (2, 2), (4, 4)])
+def test_dequantize_matches_oracle(k_bits, v_bits):
     """Oracle-made records uploaded; the GPU dequantiser must rebuild the
     oracle's unrotated values."""
     dev = device()
@@ -172,7 +185,7 @@ def test_dequantize_matches_oracle(k_bits):
     k = I.kv_values(w, "k", 0, 0, 2 * T)
     v = I.kv_values(w, "v", 0, 0, 2 * T)
     H = 2
-    cfg = K.make_config(H, H, 3, "bf16", k_bits=k_bits)
+    cfg = K.make_config(H, H, 3, "bf16", k_bits=k_bits, v_bits=v_bits)
     bb = K.kvarn_block_bytes(cfg)
     pool = torch.zeros(3 * bb, dtype=torch.uint8)
     want = np.zeros((2, 2, H, T, D))
@@ -180,11 +193,11 @@ def test_dequantize_matches_oracle(k_bits):
     for n, blk in enumerate(blocks):
         for h in range(H):
             for kv, src in ((0, k), (1, v)):
-                tl = O.quantize_tile(tile_values(src[n * T:(n + 1) * T, h], "bf16"), O.levels(bool(kv), k_bits))
-                rec = O.pack_record(bool(kv), tl, k_bits)
-                off = blk * bb + h * K.head_rec(k_bits) + kv * K.rec_bytes(k_bits)
+                tl = O.quantize_tile(tile_values(src[n * T:(n + 1) * T, h], "bf16"), O.levels(bool(kv), k_bits, v_bits))
+                rec = O.pack_record(bool(kv), tl, k_bits, v_bits)
+                off = blk * bb + h * K.head_rec(k_bits, v_bits) + kv * K.rec_bytes(k_bits)
                 pool[off:off + rec.size] = torch.from_numpy(rec)
-                want[n, kv, h] = O.dequantize_record(bool(kv), rec, k_bits)
+                want[n, kv, h] = O.dequantize_record(bool(kv), rec, k_bits, v_bits=v_bits)
     pool = pool.to(dev)
     out = torch.empty(2, 2, H, T, D, dtype=torch.float32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
