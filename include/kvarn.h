@@ -24,7 +24,7 @@
  *    NULL is the legacy default stream).  Device pointers must be 16-byte
  *    aligned; the library checks this on the host.
  *  - Host-side validation fails synchronously with KVARN_ERR_INVALID (bad
- *    argument) or KVARN_ERR_UNSUPPORTED (a configuration this build does not
+ *    argument) or KVARN_ERR_UNSUPPORTED (a configuration the library does not
  *    implement) and launches nothing.  A failed launch returns
  *    KVARN_ERR_CUDA.
  *  - Faults found on the device (a block id outside [0, num_blocks), a
@@ -80,7 +80,7 @@ extern "C" {
 typedef enum kvarn_status {
   KVARN_OK = 0,
   KVARN_ERR_INVALID = 1,     /* bad pointer, size, alignment or stride */
-  KVARN_ERR_UNSUPPORTED = 2, /* valid request outside what this build implements */
+  KVARN_ERR_UNSUPPORTED = 2, /* valid request outside what the library implements */
   KVARN_ERR_CUDA = 3         /* a kernel launch or CUDA runtime call failed */
 } kvarn_status;
 
