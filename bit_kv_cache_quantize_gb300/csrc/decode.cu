@@ -157,8 +157,11 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 //     B = 2-bit codes of channel 8 nbp + g, whose 32-bit words keep even
 //     tokens in the low half and odd tokens in the high half, so each B
 //     register is one masked field of one word.
+// Two CTAs per SM at 128 registers a thread, except for the K4/V4 preset,
+// whose record buffers leave room for one CTA: that instance takes the
+// registers one CTA may have (no spills).
 template <typename E, int KBITS, int VBITS>
-__global__ void __launch_bounds__(256, 2) decode_packed_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decode_packed_kernel(DecodeParams p) {
   using KL = KeyLayout<KBITS>;
   constexpr int KREC = rec_bytes(KBITS), KROW = D * KBITS / 8;  // KROW: code bytes per token
   constexpr int VREC = rec_bytes(VBITS);
