@@ -560,8 +560,9 @@ def run_reference(args, rank, world):
 
 def profile_case(name, launches):
     """Small single-kernel workloads for ncu captures (each > L2, a few GB at
-    most): the 16K decode (436 MB packed), the 16-bit decode on the same
-    shapes (2.1 GB), or the quantiser on 4 of the 32 prefill sequences."""
+    most): the 16K decode (436 MB packed; 570 MB with the K4/V4 preset), the
+    16-bit decode on the same shapes (2.1 GB), or the quantiser on 4 of the 32
+    prefill sequences."""
     import torch
     from bit_kv_cache_quantize_gb300 import build as B
     from bit_kv_cache_quantize_gb300 import inputs as I
@@ -569,13 +570,15 @@ def profile_case(name, launches):
     from bit_kv_cache_quantize_gb300.cache import PagedCache
     B.build()
     dev = torch.device("cuda", 0)
-    if name in ("decode16k", "fp16"):
+    if name in ("decode16k", "decode16k_k4v4", "fp16"):
         w = I.qwen3_32b()
+        if name == "decode16k_k4v4":
+            w.v_bits = 4
         c = PagedCache(w, dev, fp16_pool=(name == "fp16"))
         c.prefill()
         q = I.queries(w, device=dev)
         o = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
-        fn = (lambda: c.decode(q, o)) if name == "decode16k" else (lambda: c.decode_fp16(q, o))
+        fn = (lambda: c.decode_fp16(q, o)) if name == "fp16" else (lambda: c.decode(q, o))
     elif name == "multiquery16k":
         w = I.qwen3_32b()
         c = PagedCache(w, dev)
@@ -613,7 +616,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=16)
     ap.add_argument("--ref-seqs", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode16k", "fp16", "quantize", "multiquery16k"], default=None)
+    ap.add_argument("--profile-case", choices=["decode16k", "decode16k_k4v4", "fp16", "quantize", "multiquery16k"], default=None)
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
