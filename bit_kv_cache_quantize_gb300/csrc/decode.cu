@@ -64,10 +64,7 @@ __device__ __forceinline__ float to_f(E x) {
 // tile's V record is in use and vice versa -- the query operand fragments,
 // and the cross-warp merge area (aliases the K buffers at the end).
 constexpr int DEC_WARPS = 8;
-#ifndef KVARN_PV_ILP
-#define KVARN_PV_ILP 4
-#endif
-constexpr int PV_ILP = KVARN_PV_ILP;  // independent MMA chains interleaved in PV
+constexpr int PV_ILP = 4;  // independent MMA chains interleaved in PV
 template <int KBITS, int VBITS>
 struct DecSmem {
   alignas(128) unsigned char krec[DEC_WARPS][rec_bytes(KBITS)];
