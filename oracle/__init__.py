@@ -55,7 +55,6 @@ def lib():
         L.ora_f16_encode_rd.restype = u16; L.ora_f16_encode_rd.argtypes = [dbl]
         L.ora_f16_encode_rne.restype = u16; L.ora_f16_encode_rne.argtypes = [dbl]
         L.ora_bf16_decode.restype = dbl; L.ora_bf16_decode.argtypes = [u16]
-        L.ora_f32_ru.restype = ctypes.c_float; L.ora_f32_ru.argtypes = [dbl]
         L.ora_hadamard_matrix.argtypes = [P]
         L.ora_rotate.argtypes = [P, i32, P]
         L.ora_sinkhorn.argtypes = [P, i32, P, P]
@@ -104,10 +103,6 @@ def f16_encode_rd(x: float) -> int:
 
 def f16_encode_rne(x: float) -> int:
     return int(lib().ora_f16_encode_rne(float(x)))
-
-
-def f32_ru(x: float) -> float:
-    return float(lib().ora_f32_ru(float(x)))
 
 
 def decode16(bits: np.ndarray, dtype: str) -> np.ndarray:

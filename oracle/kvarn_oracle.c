@@ -7,10 +7,11 @@
  * generator with the CUDA library.
  *
  * Arithmetic is IEEE fp64 throughout, written as the plain definition of
- * each step, with no blocking, fusion or reordering.  Where a floating-point
- * value decides an integer (an FP8/FP16 scale code, a quantisation code) the
- * decision is taken on the value rounded to fp32, the precision the GPU
- * kernel decides in; the fp64 pre-rounding value is reported beside it.
+ * each step, with no blocking, fusion or reordering.  Every integer decision
+ * (an FP8/FP16 scale code, a quantisation code) is taken on the fp64 value
+ * of its definition; the fp64 pre-rounding value of each code is reported
+ * beside it so that a comparison can tell a decision that sits on a rounding
+ * boundary from a wrong one.
  *
  * Sources (pages on the subject; titles as published):
  *  [P1] "KVarN: 2-Bit KV-Cache That Beats FP16 Throughput, and Where the
@@ -37,7 +38,7 @@
  *    are discarded.
  *  - per token: Y = R / g, zero-point b = FP16 round-down of min_c Y,
  *    step a = E4M3 round-up of (max_c Y - b) / L (floor 2^-9), L = 2^bits - 1.
- *  - code = clamp(rne((Y - b) * fp32(1/a)), 0, L), ties to even.
+ *  - code = clamp(rne((Y - b) / a), 0, L), ties to even.
  */
 #include <math.h>
 #include <stdint.h>
@@ -152,14 +153,6 @@ double ora_bf16_decode(uint16_t h)
     float f;
     memcpy(&f, &u, 4);
     return (double)f;
-}
-
-/* fp64 -> fp32 rounded up / down (directed); the cast itself is RNE. */
-float ora_f32_ru(double x)
-{
-    float f = (float)x;
-    if ((double)f < x) f = nextafterf(f, INFINITY);
-    return f;
 }
 
 /* ------------------------------------------------------------------ */
@@ -295,7 +288,7 @@ int ora_quantize_tile_ex(const double *X, int levels, int iters, int rotate,
     mv /= D;
     for (int c = 0; c < D; c++) {
         v[c] -= mv;
-        uint8_t gc = ora_e4m3_encode_rne((double)(float)exp(v[c]));
+        uint8_t gc = ora_e4m3_encode_rne(exp(v[c]));
         if (gc == 0) gc = 0x01;                       /* never a zero scale */
         g8[c] = gc;
         gval[c] = ora_e4m3_decode(gc);
@@ -303,34 +296,31 @@ int ora_quantize_tile_ex(const double *X, int levels, int iters, int rotate,
     }
 
     for (int t = 0; t < T; t++) {
-        double y64[D];
-        float y32[D], ymin = INFINITY, ymax = -INFINITY;
+        double y[D], ymin = INFINITY, ymax = -INFINITY;
         for (int c = 0; c < D; c++) {
-            y64[c] = R[t * D + c] / gval[c];
-            y32[c] = (float)y64[c];
-            if (y32[c] < ymin) ymin = y32[c];
-            if (y32[c] > ymax) ymax = y32[c];
+            y[c] = R[t * D + c] / gval[c];
+            if (y[c] < ymin) ymin = y[c];
+            if (y[c] > ymax) ymax = y[c];
         }
-        uint16_t bt = ora_f16_encode_rd((double)ymin);
+        /* zero-point: the largest FP16 value <= min Y; step: the smallest
+         * E4M3 value >= (max Y - b) / L, so that b .. b + L a covers the row */
+        uint16_t bt = ora_f16_encode_rd(ymin);
         double bval = ora_f16_decode(bt);
-        float range = ora_f32_ru((double)ymax - bval);
-        float step = ora_f32_ru((double)range / levels);
-        uint8_t at = ora_e4m3_encode_ru((double)step);
+        double step = (ymax - bval) / levels;
+        uint8_t at = ora_e4m3_encode_ru(step);
         if (at == 0) at = 0x01;                       /* floor 2^-9 */
-        if (at == 0x7E && ora_e4m3_decode(0x7E) < (double)step) flags |= ORA_FLAG_STEP_SAT;
+        if (at == 0x7E && ora_e4m3_decode(0x7E) < step) flags |= ORA_FLAG_STEP_SAT;
         double aval = ora_e4m3_decode(at);
-        float inv_a = (float)(1.0 / aval);
         b16[t] = bt;
         a8[t] = at;
         for (int c = 0; c < D; c++) {
-            float diff = (float)((double)y32[c] - bval);
-            float q = (float)((double)diff * (double)inv_a);
-            double r = rint((double)q);
+            double x = (y[c] - bval) / aval;          /* position on the level grid */
+            double r = rint(x);                       /* nearest level, ties to even */
             int k = (int)r;
             if (r < 0) { k = 0; flags |= ORA_FLAG_CLAMPED; }
             if (r > levels) { k = levels; flags |= ORA_FLAG_CLAMPED; }
             code[t * D + c] = (uint8_t)k;
-            if (pre) pre[t * D + c] = (y64[c] - bval) / aval;
+            if (pre) pre[t * D + c] = x;
         }
     }
     if (Rout) memcpy(Rout, R, sizeof(double) * T * D);

@@ -121,7 +121,7 @@ def test_e4m3_encoders():
     rng = np.random.default_rng(4)
     xs = np.concatenate([np.exp(rng.uniform(math.log(2 ** -11), math.log(448), 3000)),
                          (table[1:] + table[:-1]) / 2])              # exact midpoints too
-    xs = xs.astype(np.float32).astype(np.float64)                    # decisions are on fp32 values
+    xs = xs.astype(np.float32).astype(np.float64)                    # torch converts from fp32 exactly
     ref = torch.from_numpy(xs.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert all(O.e4m3_encode_rne(x) == r for x, r in zip(xs, ref))
     assert O.e4m3_encode_rne(1e6) == 0x7E and O.e4m3_encode_rne(-1e6) == 0xFE
@@ -153,16 +153,32 @@ def test_f16_decode_and_encoders():
     assert O.f16_encode_rd(1e9) == 0x7BFF and O.f16_encode_rd(-1e9) == 0xFBFF
 
 
-def test_f32_round_up():
-    rng = np.random.default_rng(6)
-    for x in rng.standard_normal(2000) * 10.0 ** rng.uniform(-30, 30, 2000):
-        f = np.float32(x)
-        if float(f) < x:
-            f = np.nextafter(f, np.float32(np.inf))
-        assert O.f32_ru(x) == float(f)
-
-
 # ----------------------------------------------------------------- quantiser
+E4M3 = np.array([O.e4m3_decode(c) for c in range(0x7F)])          # the non-negative finite values, ascending
+F16 = np.arange(0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)   # 0 .. 65504 ascending
+
+
+def check_scales_tight(Y, tl, levels):
+    """The per-token zero-point and step are the tightest the formats allow
+    ("Huawei's KVarN puts KV-cache quantization inside vLLM's backend",
+    "The four-stage pipeline": asymmetric round-to-nearest over each
+    token's range): b is the LARGEST FP16 value <= min Y and a the SMALLEST
+    E4M3 value with b + L a >= max Y, checked in exact rational arithmetic
+    (a step one code too high or a zero-point one ulp too low fails)."""
+    from fractions import Fraction as Fr
+    for t in range(T):
+        lo, hi = Fr(float(Y[t].min())), Fr(float(Y[t].max()))
+        b = Fr(O.f16_decode(int(tl.b16[t])))
+        assert b <= lo, t
+        nb = -F16[F16 < -float(b)].max() if b < 0 else F16[F16 > float(b)].min()
+        assert Fr(float(nb)) > lo, t                                  # the next FP16 up is above min Y
+        a = Fr(O.e4m3_decode(int(tl.a8[t])))
+        assert b + levels * a >= hi, t                                # covers max Y
+        i = int(np.searchsorted(E4M3, float(a)))
+        if i > 1:                                                      # 2^-9 is the floor
+            assert b + levels * Fr(float(E4M3[i - 1])) < hi, t       # the E4M3 value below does not
+
+
 @pytest.mark.parametrize("levels,seed", [(15, 0), (3, 1), (15, 7), (3, 9)])
 def test_quantize_tile_properties(levels, seed):
     X = key_tile(seed)
@@ -171,13 +187,12 @@ def test_quantize_tile_properties(levels, seed):
     tl = O.quantize_tile(X, levels)
     assert tl.flags == 0
     g, a, b = tl.g(), tl.a(), tl.b()
-    # gauge: centred log factors, g = E4M3_rne(fp32(exp v))
+    # gauge: centred log factors; g is the E4M3 value nearest to exp(v)
     assert abs(tl.v.sum()) < 1e-10
-    assert all(O.e4m3_encode_rne(float(np.float32(math.exp(x)))) == c for x, c in zip(tl.v, tl.g8))
+    assert (np.abs(g - np.exp(tl.v)) <= np.abs(E4M3[None, :] - np.exp(tl.v)[:, None]).min(axis=1)).all()
     Y = tl.R / g[None, :]
     assert np.abs(tl.R - O.rotate(X)).max() < 1e-12
-    # range coverage: b <= min Y, b + L a >= max Y
-    assert (b <= Y.min(axis=1)).all() and (b + levels * a >= Y.max(axis=1)).all()
+    check_scales_tight(Y, tl, levels)
     # codes in range, equal to the brute-force nearest level except at ties
     assert tl.code.max() <= levels
     levels_grid = a[:, None, None] * np.arange(levels + 1)[None, None, :] + b[:, None, None]
@@ -191,6 +206,24 @@ def test_quantize_tile_properties(levels, seed):
     Xh = O.dequantize_record(levels == 3, O.pack_record(levels == 3, tl))
     bound = 0.5 * np.sqrt(((g[None, :] * a[:, None]) ** 2).sum(axis=1)) * (1 + 1e-6)
     assert (np.linalg.norm(Xh - X, axis=1) <= bound).all()
+
+
+def test_scale_pins_reject_loose_scales():
+    """The tightness pin fails on the plausible mistakes it is there for: a
+    per-token step one E4M3 code too high, a zero-point one FP16 ulp too low."""
+    X = key_tile(3)
+    tl = O.quantize_tile(X, 15)
+    Y = tl.R / tl.g()[None, :]
+    check_scales_tight(Y, tl, 15)
+    loose_a = O.Tile(tl.g8, tl.a8.copy(), tl.b16, tl.code, tl.pre, tl.R, tl.v, 0)
+    loose_a.a8[17] += 1
+    with pytest.raises(AssertionError):
+        check_scales_tight(Y, loose_a, 15)
+    low_b = O.Tile(tl.g8, tl.a8, tl.b16.copy(), tl.code, tl.pre, tl.R, tl.v, 0)
+    b = low_b.b16[40]
+    low_b.b16[40] = b + 1 if b & 0x8000 else b - 1                   # one ulp towards -inf
+    with pytest.raises(AssertionError):
+        check_scales_tight(Y, low_b, 15)
 
 
 def test_quantize_degenerate_tiles():
@@ -429,8 +462,7 @@ def test_plain_rtn_is_per_token_min_max():
     X = rng.standard_normal((T, D))
     tl = O.quantize_tile(X, 15, 0, rotate=False)
     assert (tl.g8 == O.e4m3_encode_rne(1.0)).all()
-    a = np.array([O.e4m3_decode(c) for c in tl.a8]); b = np.array([O.f16_decode(c) for c in tl.b16])
-    assert (b <= X.min(axis=1)).all() and (b + 15 * a >= X.max(axis=1)).all()
+    check_scales_tight(X, tl, 15)
 
 
 def test_token_errors_definition_and_rotation_benefit():
