@@ -15,6 +15,12 @@ Also reported, as components: the 16K-context decode (32 x 16384 tokens) of
 the packed kernel beside the in-repo 16-bit paged decode kernel on the same
 shapes, and the write-path quantiser on 32 x 16384 x 8 heads of bf16.
 
+With N > 1 GPUs the step is split by KV head (`--shard heads`, the
+default): rank r of N owns KV heads [8r/N, 8(r+1)/N) of every sequence,
+their query heads, pool, open tiles and output slice, as tensor-parallel
+attention would place them; no data crosses ranks.  `--shard replicas` runs
+N independent serving batches instead.
+
 `--impl reference` times the CPU oracle (the plain fp64 restatement of the
 method) on the host cores on a bounded sample of the same step.
 """
@@ -100,10 +106,11 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# DRAM bytes actually moved by one decode call per algorithmic byte, from the
-# ncu capture of the 16K decode (profiles/decode_call_traffic_qwen3_32b_16k.md:
-# 449 723 392 B for 437 796 992 algorithmic bytes).  The serving step's call is
-# too large to capture, and its traffic grows with the records it reads.
+# DRAM bytes actually moved by one decode call per algorithmic byte, from an
+# ncu capture of the 16K decode call (32 x 16384 tokens, 64 q / 8 KV heads:
+# 449 662 976 B of DRAM traffic for 437 796 992 algorithmic bytes).  The
+# serving step's call is too large to capture, and its traffic grows with the
+# records it reads.
 DECODE_TRAFFIC_PER_BYTE = 449662976 / 437796992
 
 
@@ -111,25 +118,44 @@ DECODE_TRAFFIC_PER_BYTE = 449662976 / 437796992
 # 2 half-steps x 16384 elements x 3 lane operations (shifted product, sum,
 # sum of squares) plus ~6 per element for the row range and the encode.
 QUANT_LANE_OPS_PER_JOB = 8 * 2 * 16384 * 3 + 6 * 16384
-# FP32 lane operations per second: 152 SMs x 128 FP32 lanes x 2070 MHz.
-FP32_LANE_OPS_PEAK = 152 * 128 * 2.07e9
+FP32_LANES_PER_SM = 128          # FP32 lanes of one SM (4 sub-partitions x 32)
 
 
-def decode_bytes(lens, w):
-    """Algorithmic bytes of one decode call: packed records of the closed
+def fp32_lane_ops_peak(dev, sm_mhz=None):
+    """FP32 lane operations per second of the device: its SM count (from the
+    device properties) x 128 lanes x the SM clock (the median sampled under
+    load when given, else the device's maximum clock)."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    mhz = sm_mhz
+    if not mhz:
+        try:
+            mhz = float(subprocess.check_output(
+                ["nvidia-smi", "-i", str(dev.index), "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits"],
+                text=True).strip().splitlines()[0])
+        except Exception:
+            mhz = 2070.0
+    return props.multi_processor_count * FP32_LANES_PER_SM * mhz * 1e6, props.multi_processor_count, mhz
+
+
+def decode_bytes(lens, w, H=None, Hq=None):
+    """Algorithmic bytes of one decode call over H KV heads and Hq query
+    heads (default: all of the workload's): packed records of the closed
     tiles, raw open-tile tokens, queries, outputs, block ids and lengths."""
-    H = w.num_kv_heads
+    H = w.num_kv_heads if H is None else H
+    Hq = w.num_q_heads if Hq is None else Hq
     closed = sum(n // T for n in lens)
     tail = sum(n % T for n in lens)
     head_rec = 2 * 512 + T * D * (w.k_bits + w.v_bits) // 8   # K and V record of one (tile, head)
-    return (closed * H * head_rec + tail * H * 2 * D * 2 + len(lens) * w.num_q_heads * D * (2 + 4)
+    return (closed * H * head_rec + tail * H * 2 * D * 2 + len(lens) * Hq * D * (2 + 4)
             + closed * 4 + len(lens) * 4)
 
 
 # --------------------------------------------------------------------------- multi-rank host logic
 def rank_seed(rank):
-    """Seed of rank's own serving batch: every rank draws its own sequences,
-    so ranks share no (sequence, KV head) unit and exchange no data."""
+    """Seed of rank's own serving batch under `--shard replicas`: every rank
+    draws its own sequences, so ranks share no (sequence, KV head) unit and
+    exchange no data."""
     return 4 + 1000 * rank
 
 
@@ -143,9 +169,11 @@ def reduce_max_ms(ms, device=None):
     return float(t.item())
 
 
-def job_tokens_per_s(batch, steps, world, ms):
-    """Whole-job throughput: every rank decodes its own batch each step."""
-    return batch * steps * world / (ms / 1e3)
+def job_tokens_per_s(batch, steps, world, ms, shard="replicas"):
+    """Whole-job throughput in decoded tokens (one per sequence and step) per
+    second of the slowest rank: with replicas every rank decodes its own
+    batch; with KV-head sharding the ranks decode parts of the same tokens."""
+    return batch * steps * (world if shard == "replicas" else 1) / (ms / 1e3)
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -159,26 +187,30 @@ def run_gpu(args, rank, world):
     B.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
+    from bit_kv_cache_quantize_gb300 import shard as S
     hbm_peak, _, peak_src = measured_peaks()
     steps, warm = args.steps, args.warmup
     n_dec = max(64, steps + warm)
-    w = I.ragged_32b(steps=n_dec, seed=rank_seed(rank))
-    c = PagedCache(w, dev)
+    mode = args.shard if world > 1 else "single"
+    w = I.ragged_32b(steps=n_dec, seed=rank_seed(rank) if mode == "replicas" else 4)
+    h0, h1 = S.head_range(rank, world, w.num_kv_heads) if mode == "heads" else (0, w.num_kv_heads)
+    c = PagedCache(w, dev, heads=(h0, h1))
     c.prefill()
     torch.cuda.synchronize()
     assert c.check_error() == 0, "device error during prefill"
 
-    # every step's inputs, resident before timing
-    B_, H, Hq = w.batch, w.num_kv_heads, w.num_q_heads
+    # every step's inputs, resident before timing (this rank's heads only)
+    B_, H, Hq = w.batch, c.H, c.Hq
+    qh0, qh1 = h0 * w.G, h1 * w.G
     dt = I.torch_dtype(w.dtype)
     base = torch.tensor(w.seq_lens, dtype=torch.int64)
     pos_all = (base[None, :] + torch.arange(n_dec)[:, None]).to(torch.int32)          # [S, B]
     kn = torch.empty(n_dec, B_, H, D, dtype=dt, device=dev)
     vn = torch.empty_like(kn)
     for b in range(B_):
-        kn[:, b] = I.kv_values(w, "k", b, w.seq_lens[b], n_dec, dev)
-        vn[:, b] = I.kv_values(w, "v", b, w.seq_lens[b], n_dec, dev)
-    qs = torch.stack([I.queries(w, step=s + 1, device=dev) for s in range(n_dec)])
+        kn[:, b] = I.kv_values(w, "k", b, w.seq_lens[b], n_dec, dev, heads=range(h0, h1))
+        vn[:, b] = I.kv_values(w, "v", b, w.seq_lens[b], n_dec, dev, heads=range(h0, h1))
+    qs = torch.stack([I.queries(w, step=s + 1, device=dev)[:, qh0:qh1] for s in range(n_dec)]).contiguous()
     pos_d = pos_all.to(dev)
     lens_d = (pos_all + 1).to(dev)
     out = torch.empty(B_, Hq, D, dtype=torch.float32, device=dev)
@@ -214,16 +246,27 @@ def run_gpu(args, rank, world):
         ms = reduce_max_ms(ms, dev)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
     dec_avg_s = sum(dec_ms) / len(dec_ms) / 1e3
-    dec_bytes = statistics.mean(decode_bytes([int(x) + 1 for x in pos_all[warm + i]], w) for i in range(steps))
+    dec_bytes = statistics.mean(decode_bytes([int(x) + 1 for x in pos_all[warm + i]], w, H, Hq)
+                                for i in range(steps))
     achieved = dec_bytes / dec_avg_s / 1e9
-    tokens_per_s = job_tokens_per_s(B_, steps, world, ms)
+    shard_mode = "replicas" if mode == "replicas" else "heads"
+    tokens_per_s = job_tokens_per_s(B_, steps, world, ms, shard_mode)
 
     # e2e: the same steps through the public API with host buffers
     e2e = run_e2e(c, w, kn, vn, qs, pos_all, dev, warm, steps)
+    if world > 1:
+        e2e_ms = reduce_max_ms(e2e["ms_per_step"] * steps, dev)
+        e2e["value"] = job_tokens_per_s(B_, steps, world, e2e_ms, shard_mode)
+        e2e["ms_per_step"] = e2e_ms / steps
+        e2e["h2d_bytes_per_step"] *= world      # every rank copies its own slices
+        e2e["d2h_bytes_per_step"] *= world
+    parallelism = {"single": "single GPU", "replicas": f"replicas x{world}",
+                   "heads": f"KV heads split {world} ways ({H} KV / {Hq} q heads per rank), no collective"}[mode]
 
     res = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
-        "warmup": warm, "ms_per_step": ms / steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": warm, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "strong" if mode == "heads" else "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "ragged_32b_serving: 256 seqs, context U[128,32768] (never a multiple of 128), "
                                "Qwen3-32B layer 64 q / 8 KV heads, head_dim 128, fp16 inputs, K4/V2 "
@@ -231,7 +274,7 @@ def run_gpu(args, rank, world):
                                "(close+quantise full tiles) + decode attention",
                    "batch": B_, "mean_context": statistics.mean(w.seq_lens),
                    "decode_steps_appended": n_dec, "l2": "inputs larger than L2 (packed cache ~3.5 GB)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": parallelism},
         "roofline": {"kernel": "kvarn_decode_attention (split-K decode + combine)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "peak_source": peak_src, "traffic": DECODE_TRAFFIC_PER_BYTE * dec_bytes,
@@ -244,9 +287,9 @@ def run_gpu(args, rank, world):
     }
     del c, kn, vn, qs
     torch.cuda.empty_cache()
-    if not args.no_components and rank == 0:
-        res["components"] = components(dev, hbm_peak, measured_peaks()[1])
     res["clocks"] = clk.summary()
+    if not args.no_components and rank == 0:
+        res["components"] = components(dev, hbm_peak, measured_peaks()[1], res["clocks"].get("sm_mhz"))
     return res
 
 
@@ -261,13 +304,14 @@ def run_e2e(c, w, kn, vn, qs, pos_all, dev, warm, steps):
     import torch
     hk = kn.cpu().pin_memory(); hv = vn.cpu().pin_memory(); hq = qs.cpu().pin_memory()
     hp = pos_all.pin_memory(); hl = (pos_all + 1).pin_memory()
-    hout = [torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32).pin_memory() for _ in range(2)]
+    Hq = qs.shape[2]                          # query heads of this rank
+    hout = [torch.empty(w.batch, Hq, D, dtype=torch.float32).pin_memory() for _ in range(2)]
     bufs = []
     for _ in range(2):
         bufs.append(dict(k=torch.empty_like(kn[0]), v=torch.empty_like(vn[0]), q=torch.empty_like(qs[0]),
                          p=torch.empty(w.batch, dtype=torch.int32, device=dev),
                          l=torch.empty(w.batch, dtype=torch.int32, device=dev),
-                         o=torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)))
+                         o=torch.empty(w.batch, Hq, D, dtype=torch.float32, device=dev)))
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = lambda: torch.cuda.Event()
@@ -320,7 +364,7 @@ def flush_l2(buf):
     buf.zero_()
 
 
-def components(dev, hbm_peak, bf16_peak):
+def components(dev, hbm_peak, bf16_peak, sm_mhz=None):
     """16K decode (packed vs 16-bit kernel) and the prefill quantiser."""
     import torch
     from bit_kv_cache_quantize_gb300 import inputs as I
@@ -465,12 +509,14 @@ def components(dev, hbm_peak, bf16_peak):
     jobs = n_tiles * w.num_kv_heads * 2
     byt = jobs * (T * D * 2) + n_tiles * w.num_kv_heads * 13312 + n_tiles * 12
     alu_ops = jobs * QUANT_LANE_OPS_PER_JOB
+    alu_peak, sms, mhz = fp32_lane_ops_peak(dev, sm_mhz)
     out["quantizer"] = {
         "workload": "prefill_32b_16k: 32 x 16384 tokens x 8 KV heads, bf16, K and V tiles (65536 tile jobs)",
         "us": t_q * 1e6, "tiles_per_s": jobs / t_q, "GBps": byt / t_q / 1e9, "frac_hbm": byt / t_q / 1e9 / hbm_peak,
         "bytes": byt,
         "alu": {"bound": "alu", "lane_ops_per_job": QUANT_LANE_OPS_PER_JOB, "achieved_tops": alu_ops / t_q / 1e12,
-                "peak_tops": FP32_LANE_OPS_PEAK / 1e12, "frac": alu_ops / t_q / FP32_LANE_OPS_PEAK},
+                "peak_tops": alu_peak / 1e12, "frac": alu_ops / t_q / alu_peak,
+                "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz"},
     }
     return out
 
@@ -522,7 +568,33 @@ def oracle_step(w, units, threads):
                              nthreads=threads)
 
 
-def cpu_baseline(n_seqs=4, reps=1):
+def oracle_quantize_sample(n_seqs, threads):
+    """The oracle quantiser on the first n_seqs sequences of the 32 x 16K
+    bf16 prefill (every K and V tile of their 8 KV heads): (tile jobs per
+    second, jobs, seconds).  Inputs are generated on the GPU when there is
+    one (faster) and handed to the oracle as host bytes."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from bit_kv_cache_quantize_gb300 import inputs as I
+    w = I.prefill_32b()
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    n, H = w.seq_lens[0], w.num_kv_heads
+    first = np.array([t * T * H * D + h * D for t in range(n // T) for h in range(H)], np.int64)
+    srcs = []
+    for b in range(n_seqs):
+        for which in ("k", "v"):
+            x = I.kv_sequence(w, which, b, n, gen).cpu()
+            srcs.append((x.view(torch.int16).numpy().view(np.uint16).reshape(-1), which == "v"))
+    t0 = time.perf_counter()
+    for bits, is_v in srcs:
+        O.quantize_batch(bits, "bf16", first, H * D, is_v, nthreads=threads)
+    dt = time.perf_counter() - t0
+    jobs = len(srcs) * len(first)
+    return jobs / dt, jobs, dt
+
+
+def cpu_baseline(n_seqs=4, reps=1, quant_seqs=4):
     threads = os.cpu_count() or 1
     w, units = oracle_step_sample(n_seqs, threads=threads)
     t0 = time.perf_counter()
@@ -530,10 +602,15 @@ def cpu_baseline(n_seqs=4, reps=1):
         oracle_step(w, units, threads)
     dt = (time.perf_counter() - t0) / reps
     ctx = sum(w.seq_lens[:n_seqs])
+    qrate, qjobs, qdt = oracle_quantize_sample(quant_seqs, threads)
     return {"value": n_seqs / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"decode step (attention over the packed cache + open tile, folded fp64 form) of "
                       f"{n_seqs} sequences x 8 KV heads x 8 queries of the ragged serving mix "
-                      f"({ctx} context tokens); {dt:.2f} s per step on {threads} threads"}
+                      f"({ctx} context tokens); {dt:.2f} s per step on {threads} threads",
+            "quantize_tiles_per_s": qrate,
+            "quantize_sample": f"write path (rotation, 8 Sinkhorn iterations, scales, codes, packing) of every K and "
+                               f"V tile of {quant_seqs} of the 32 x 16384-token bf16 prefill sequences x 8 KV heads "
+                               f"({qjobs} tile jobs) in {qdt:.2f} s on {threads} threads"}
 
 
 def run_reference(args, rank, world):
@@ -612,10 +689,13 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="kvarn", choices=["kvarn", "reference"])
+    ap.add_argument("--shard", default="heads", choices=["heads", "replicas"],
+                    help="N > 1: split the step's KV heads over the ranks, or run N independent batches")
     ap.add_argument("--no-components", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seqs", type=int, default=16)
-    ap.add_argument("--ref-seqs", type=int, default=1)
+    ap.add_argument("--cpu-quant-seqs", type=int, default=8)
+    ap.add_argument("--ref-seqs", type=int, default=4)
     ap.add_argument("--profile-case", choices=["decode16k", "decode16k_k4v4", "fp16", "quantize", "multiquery16k"], default=None)
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
@@ -632,7 +712,7 @@ def main():
     else:
         res = run_gpu(args, rank, world)
         if rank == 0 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(args.cpu_seqs)
+            res["cpu_baseline"] = cpu_baseline(args.cpu_seqs, quant_seqs=args.cpu_quant_seqs)
     if rank == 0 and res is not None:
         print(json.dumps(res))
     if world > 1 and args.impl != "reference":

@@ -6,6 +6,7 @@
 #pragma once
 
 #include "params.h"
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 #include <cuda_fp16.h>
@@ -127,9 +128,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: false (and the error word set) if the phase never completes.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* err) {
-  for (int i = 0; i < (1 << 22); ++i)
+// Bounded wait: false (and the error word set) if the phase has not
+// completed after `polls` polls (each poll may itself wait a short,
+// hardware-defined time).
+constexpr int kWaitPolls = 1 << 22;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int32_t* err,
+                                                  int polls = kWaitPolls) {
+  for (int i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   set_error(err, KVARN_DEV_ERR_TIMEOUT);
   return false;
@@ -245,5 +250,21 @@ __device__ __forceinline__ void split_hl(float x, uint16_t& hi, uint16_t& lo) {
   lo = f2bits<E>(x - bits2f<E>(hi));
 }
 __device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+
+// ------------------------------------------------------------------ host
+// Raises the dynamic shared memory limit of one kernel to `bytes`, once per
+// device: `done` (one static per kernel instance at the call site) keeps a
+// bit per device whose attribute is already set, so the decode-step path
+// makes no attribute call after the first launch.
+inline cudaError_t smem_attr_once(std::atomic<uint64_t>& done, const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 }  // namespace kvarn

@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
   const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
+  const int polls = p.wait_polls > 0 ? p.wait_polls : kWaitPolls;
 
   // start this warp's first tile before anything else
   if (lane == 0) {
@@ -193,6 +194,8 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
   }
   __syncwarp();
   auto issue = [&](int k, bool is_v) {  // lane 0: copy the K or V record of this warp's k-th tile
+    if (p.skip_first_copy && k == 0 && !is_v && warp == 0 && chunk == 0 && h == 0 && b == 0)
+      return;  // error-path test: this copy never starts, so its wait must expire
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     if (blk >= 0 && blk < p.num_blocks) {
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
     const unsigned char* vr = sm.vrec[warp];
     // a wait that gives up ends this warp's loop (after waiting, bounded, for
     // the V copy it still has in flight); the error word is already set
-    if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.kbar[warp], k & 1, p.err))) {
+    if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.kbar[warp], k & 1, p.err, polls))) {
       mbar_wait_bounded(&sm.vbar[warp], k & 1, p.err);
       break;
     }
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
       fence_proxy_async();
       issue(k + 1, false);
     }
-    if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.vbar[warp], k & 1, p.err))) {
+    if (__any_sync(0xffffffffu, !mbar_wait_bounded(&sm.vbar[warp], k & 1, p.err, polls))) {
       if (k + 1 < my_n) mbar_wait_bounded(&sm.kbar[warp], (k + 1) & 1, p.err);
       break;
     }
@@ -815,8 +818,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
 template <typename E, int KBITS, int VBITS>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
   const size_t smem = sizeof(DecSmem<KBITS, VBITS>) + 128;
-  cudaError_t e = cudaFuncSetAttribute(decode_packed_kernel<E, KBITS, VBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = smem_attr_once(attr_done, (const void*)decode_packed_kernel<E, KBITS, VBITS>, (int)smem);
   if (e != cudaSuccess) return e;
   decode_packed_kernel<E, KBITS, VBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
   e = cudaGetLastError();
@@ -873,15 +876,18 @@ cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* o
   return launch_decode(p, dtype, batch, out, s);
 }
 
+// The driver's tensor-map encoder, looked up once (a function-local static
+// with an initialiser is initialised exactly once, even under concurrent
+// first calls).
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -899,7 +905,8 @@ static cudaError_t launch_f16_t(DecodeParams p, const void* pool16, int batch, f
                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const size_t smem = sizeof(F16Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(decode_f16_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = smem_attr_once(attr_done, (const void*)decode_f16_kernel<E>, (int)smem);
   if (e != cudaSuccess) return e;
   decode_f16_kernel<E><<<dim3(p.n_chunks, p.num_kv_heads, batch), 256, smem, s>>>(tmap, p);
   e = cudaGetLastError();

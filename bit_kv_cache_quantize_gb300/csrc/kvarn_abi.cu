@@ -10,12 +10,29 @@
 #include "params.h"
 
 namespace kvarn {
-constexpr int kChunkTiles = 16;  // fewest packed tiles per split-K CTA (sizes the workspace)
+constexpr int kChunkTiles = 16;  // packed tiles per split-K CTA of an ordinary call (sizes the workspace)
+constexpr int kSmallChunkTiles = 8;  // of a small call: one tile per warp
+// A call whose table spans fewer (sequence, KV head, tile) units than this
+// is small: 16-tile chunks would give it under three waves of two 8-warp
+// CTAs per SM on 152 SMs (3 x 304 x 16), so it takes 8-tile chunks, twice
+// the CTAs.  The rule depends only on the call's shape, so the workspace
+// size does too.
+constexpr long long kSmallCallUnits = 3LL * 304 * 16;
 
-// Packed tiles per split-K CTA for one call: 32 (longer CTAs amortise the
-// per-CTA query set-up and merge) when that still gives at least three waves
-// of CTAs at two per SM, else 16.
+static bool small_call(int batch, int num_kv_heads, int max_blocks) {
+  return (long long)batch * num_kv_heads * max_blocks < kSmallCallUnits;
+}
+
+// Fewest packed tiles per split-K CTA a call of this shape may use.
+static int min_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
+  return small_call(batch, num_kv_heads, max_blocks) ? kSmallChunkTiles : kChunkTiles;
+}
+
+// Packed tiles per split-K CTA for one call: 8 for a small call; else 32
+// (longer CTAs amortise the per-CTA query set-up and merge) when that still
+// gives at least three waves of CTAs at two per SM, else 16.
 static int choose_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
+  if (small_call(batch, num_kv_heads, max_blocks)) return kSmallChunkTiles;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -68,7 +85,8 @@ size_t kvarn_fp16_block_bytes(const kvarn_config* cfg) {
 size_t kvarn_decode_workspace_bytes(const kvarn_config* cfg, int32_t batch, int32_t max_blocks) {
   if (check_config(cfg) != KVARN_OK || batch < 0 || max_blocks < 1) return 0;
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  const size_t a = decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles);
+  const size_t a = decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks,
+                                   min_chunk_tiles(batch, cfg->num_kv_heads, max_blocks));
   const size_t b = decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kF16ChunkTiles);
   return a > b ? a : b;
 }
@@ -148,10 +166,11 @@ static kvarn_status check_decode(const kvarn_config* cfg, const void* q, const i
   return KVARN_OK;
 }
 
-kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, const int32_t* block_table,
-                                    int32_t max_blocks, const int32_t* seq_lens, int32_t batch, const void* block_pool,
-                                    const void* tail_pool, float softmax_scale, float* out, void* workspace,
-                                    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+static kvarn_status decode_call(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                int32_t max_blocks, const int32_t* seq_lens, int32_t batch, const void* block_pool,
+                                const void* tail_pool, float softmax_scale, float* out, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_err, void* stream, int32_t wait_polls,
+                                int32_t skip_first_copy) {
   kvarn_status st = check_decode(cfg, q, block_table, max_blocks, seq_lens, batch, block_pool, out, workspace,
                                  workspace_bytes);
   if (st != KVARN_OK || batch == 0) return st;
@@ -161,8 +180,26 @@ kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, cons
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
                  static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
                  max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads,
-                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits, cfg->v_bits};
+                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits, cfg->v_bits, wait_polls, skip_first_copy};
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
+}
+
+kvarn_status kvarn_decode_attention(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                    int32_t max_blocks, const int32_t* seq_lens, int32_t batch, const void* block_pool,
+                                    const void* tail_pool, float softmax_scale, float* out, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  return decode_call(cfg, q, block_table, max_blocks, seq_lens, batch, block_pool, tail_pool, softmax_scale, out,
+                     workspace, workspace_bytes, dev_err, stream, 0, 0);
+}
+
+kvarn_status kvarn_test_decode_wait_expiry(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                           int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                           const void* block_pool, const void* tail_pool, float softmax_scale,
+                                           float* out, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                           int32_t wait_polls, void* stream) {
+  if (wait_polls < 1) return KVARN_ERR_INVALID;
+  return decode_call(cfg, q, block_table, max_blocks, seq_lens, batch, block_pool, tail_pool, softmax_scale, out,
+                     workspace, workspace_bytes, dev_err, stream, wait_polls, 1);
 }
 
 // Packed tiles per split-K CTA of the multi-query kernel (one CTA per SM):
@@ -224,7 +261,9 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
   if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles) > KVARN_NOALLOC_SCRATCH_BYTES)
     return KVARN_ERR_UNSUPPORTED;  // larger than the fixed scratch: use kvarn_decode_attention
-  const int chunk = choose_chunk_tiles(batch, cfg->num_kv_heads, max_blocks);
+  int chunk = choose_chunk_tiles(batch, cfg->num_kv_heads, max_blocks);
+  if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, chunk) > KVARN_NOALLOC_SCRATCH_BYTES)
+    chunk = kChunkTiles;  // a small call's finer split does not fit: the ordinary split does
   const int n_chunks = (max_blocks + chunk - 1) / chunk;
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool, nullptr, dev_err,
                  static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale, max_blocks, cfg->num_kv_heads,

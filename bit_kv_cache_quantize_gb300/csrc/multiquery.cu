@@ -910,8 +910,8 @@ __global__ void __launch_bounds__(128) mq_combine_kernel(MQParams p, int batch, 
 template <typename E, int KBITS, int VBITS>
 cudaError_t launch_mq_t(const MQParams& p, int batch, float* out, cudaStream_t s) {
   const size_t smem = sizeof(MQSmem) + 128;
-  cudaError_t e =
-      cudaFuncSetAttribute(mq_kernel<E, KBITS, VBITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = smem_attr_once(attr_done, (const void*)mq_kernel<E, KBITS, VBITS>, (int)smem);
   if (e != cudaSuccess) return e;
   mq_kernel<E, KBITS, VBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads * p.n_rowblocks, batch), MQ_THREADS, smem, s>>>(p);
   e = cudaGetLastError();

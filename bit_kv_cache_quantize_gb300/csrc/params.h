@@ -65,6 +65,12 @@ struct DecodeParams {
   int32_t n_chunks;
   int32_t k_bits;
   int32_t v_bits;
+  // Error-path test only (both 0 in every normal call): the bounded-wait
+  // limit in polls (0 = the default) and a flag that leaves out the first
+  // key-record copy of warp 0 of the unit (chunk 0, KV head 0, sequence 0),
+  // so that its wait expires with nothing in flight.
+  int32_t wait_polls;
+  int32_t skip_first_copy;
 };
 // Multi-query causal attention: n_queries query tokens per sequence at the
 // last n_queries positions, grouped with their GQA heads into row blocks of

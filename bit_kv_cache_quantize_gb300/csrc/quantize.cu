@@ -611,7 +611,8 @@ size_t quantize_smem_bytes() { return sizeof(QSmem); }
 template <typename E>
 static cudaError_t launch_quantize_t(const QuantizeParams& p, int n_tiles, cudaStream_t s) {
   const size_t smem = sizeof(QSmem);
-  cudaError_t e = cudaFuncSetAttribute(quantize_tiles_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = smem_attr_once(attr_done, (const void*)quantize_tiles_kernel<E>, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t jobs = static_cast<int64_t>(n_tiles) * p.num_kv_heads * 2;
   quantize_tiles_kernel<E><<<static_cast<unsigned>(jobs), 256, smem, s>>>(p);
@@ -696,13 +697,13 @@ static cudaError_t launch_errors_k(const ErrParams& p, int n_tiles, cudaStream_t
   const size_t smem = sizeof(QSmem);
   const dim3 grid(n_tiles * p.num_kv_heads);
   if (p.rotate) {
-    cudaError_t e =
-        cudaFuncSetAttribute(token_errors_kernel<E, KIND, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t e = smem_attr_once(attr_done, (const void*)token_errors_kernel<E, KIND, true>, (int)smem);
     if (e != cudaSuccess) return e;
     token_errors_kernel<E, KIND, true><<<grid, 256, smem, s>>>(p);
   } else {
-    cudaError_t e =
-        cudaFuncSetAttribute(token_errors_kernel<E, KIND, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::atomic<uint64_t> attr_done{0};
+    cudaError_t e = smem_attr_once(attr_done, (const void*)token_errors_kernel<E, KIND, false>, (int)smem);
     if (e != cudaSuccess) return e;
     token_errors_kernel<E, KIND, false><<<grid, 256, smem, s>>>(p);
   }
@@ -727,7 +728,8 @@ cudaError_t launch_quantize(const QuantizeParams& p, int dtype, int n_tiles, cud
 template <typename E>
 static cudaError_t launch_append_t(const AppendParams& p, int batch, cudaStream_t s) {
   const size_t smem = sizeof(QSmem);
-  cudaError_t e = cudaFuncSetAttribute(append_tokens_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = smem_attr_once(attr_done, (const void*)append_tokens_kernel<E>, (int)smem);
   if (e != cudaSuccess) return e;
   append_tokens_kernel<E><<<dim3(batch, p.num_kv_heads, 2), 256, smem, s>>>(p);
   return cudaGetLastError();

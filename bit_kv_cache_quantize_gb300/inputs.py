@@ -211,13 +211,15 @@ def kv_values(w: Workload, which: str, b: int, t0: int, n_tok: int, device="cpu"
     return to16(x, torch_dtype(w.dtype))
 
 
-def kv_sequence(w: Workload, which: str, b: int, n_tok: int, device="cpu") -> torch.Tensor:
-    """Whole context of one sequence, [n_tok, H_kv, D], generated in chunks."""
-    out = torch.empty(n_tok, w.num_kv_heads, D, dtype=torch_dtype(w.dtype), device=device)
+def kv_sequence(w: Workload, which: str, b: int, n_tok: int, device="cpu", heads=None) -> torch.Tensor:
+    """Whole context of one sequence, [n_tok, H, D] (H = all KV heads, or
+    the listed ones), generated in chunks."""
+    heads = list(range(w.num_kv_heads)) if heads is None else list(heads)
+    out = torch.empty(n_tok, len(heads), D, dtype=torch_dtype(w.dtype), device=device)
     step = 2048
     for t0 in range(0, n_tok, step):
         n = min(step, n_tok - t0)
-        out[t0:t0 + n] = kv_values(w, which, b, t0, n, device)
+        out[t0:t0 + n] = kv_values(w, which, b, t0, n, device, heads)
     return out
 
 

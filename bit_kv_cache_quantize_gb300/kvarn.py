@@ -38,7 +38,7 @@ EXPORTS = (
     "kvarn_decode_workspace_bytes", "kvarn_decode_attention", "kvarn_dequantize",
     "kvarn_fp16_block_bytes", "kvarn_fp16_decode_attention", "kvarn_status_string",
     "kvarn_decode_attention_noalloc", "kvarn_multiquery_workspace_bytes", "kvarn_multiquery_attention",
-    "kvarn_token_errors_scratch_bytes", "kvarn_token_errors",
+    "kvarn_token_errors_scratch_bytes", "kvarn_token_errors", "kvarn_test_decode_wait_expiry",
 )
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
             "kvarn_decode_attention": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, sz, P, P]),
             "kvarn_fp16_decode_attention": (i32, [C, P, P, i32, P, i32, P, f32, P, P, sz, P, P]),
             "kvarn_decode_attention_noalloc": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, P]),
+            "kvarn_test_decode_wait_expiry": (i32, [C, P, P, i32, P, i32, P, P, f32, P, P, sz, P, i32, P]),
             "kvarn_dequantize": (i32, [C, P, P, i32, P, P, P]),
             "kvarn_multiquery_workspace_bytes": (sz, [C, i32, i32, i32]),
             "kvarn_token_errors_scratch_bytes": (sz, [C, i32, i32]),
@@ -174,6 +175,18 @@ def kvarn_decode_attention_noalloc(cfg, q, block_table, max_blocks, seq_lens, ba
                                               _p(seq_lens), int(batch), _p(block_pool), _p(tail_pool),
                                               float(softmax_scale), _p(out), _p(dev_err), _s(stream))
     return _check(st, "kvarn_decode_attention_noalloc", check)
+
+
+def kvarn_test_decode_wait_expiry(cfg, q, block_table, max_blocks, seq_lens, batch, block_pool, tail_pool,
+                                  softmax_scale, out, workspace, workspace_bytes, dev_err, wait_polls, stream=None,
+                                  check=True) -> int:
+    """Decode with one record copy left out and the copy waits limited to
+    wait_polls polls: the error path of a bounded wait (see include/kvarn.h)."""
+    st = lib().kvarn_test_decode_wait_expiry(ctypes.byref(cfg), _p(q), _p(block_table), int(max_blocks),
+                                             _p(seq_lens), int(batch), _p(block_pool), _p(tail_pool),
+                                             float(softmax_scale), _p(out), _p(workspace), int(workspace_bytes),
+                                             _p(dev_err), int(wait_polls), _s(stream))
+    return _check(st, "kvarn_test_decode_wait_expiry", check)
 
 
 def kvarn_multiquery_workspace_bytes(cfg, batch: int, max_blocks: int, n_queries: int) -> int:

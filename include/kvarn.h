@@ -18,8 +18,12 @@
  * Conventions for every entry point:
  *  - All pointers documented "device" are CUDA device pointers the caller
  *    owns and keeps alive until the stream work completes.  The library
- *    allocates nothing and keeps no global state other than the fixed
- *    scratch array of kvarn_decode_attention_noalloc.
+ *    allocates nothing.  Its only process-wide state is the fixed scratch
+ *    array of kvarn_decode_attention_noalloc and host-side caches filled on
+ *    first use and never changed afterwards: the array's device address per
+ *    device, the driver's tensor-map encoder entry point, and per kernel a
+ *    mark of the devices on which its shared-memory limit is already set.
+ *    They are safe to fill from several host threads at once.
  *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *    NULL is the legacy default stream).  Device pointers must be 16-byte
  *    aligned; the library checks this on the host.
@@ -306,6 +310,27 @@ kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q,
                                          const int32_t* seq_lens, int32_t batch, const void* fp16_pool,
                                          float softmax_scale, float* out, void* workspace,
                                          size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * Error-path test of kvarn_decode_attention (not for serving): the same call
+ * with the copy of the first key record of one unit (sequence 0, KV head 0,
+ * its first split-K chunk, first warp) left out and every wait on a record
+ * copy limited to wait_polls polls of its mbarrier.  Nothing is in flight
+ * for the left-out record, so its wait expires: the kernel stores
+ * KVARN_DEV_ERR_TIMEOUT into *dev_err, waits (bounded) for the unit's copies
+ * that did start, skips the rest of that warp's tiles and returns; the call
+ * completes and the device stays usable.  The outputs of sequence 0 are
+ * unspecified; the other sequences are decoded normally.  wait_polls >= 1
+ * (KVARN_ERR_INVALID otherwise); other arguments as kvarn_decode_attention.
+ * This is the timeout path every bounded wait of the library takes ("Kernels
+ * never trap and never wait without a bound" above); the pages describe
+ * nothing like it.
+ */
+kvarn_status kvarn_test_decode_wait_expiry(const kvarn_config* cfg, const void* q, const int32_t* block_table,
+                                           int32_t max_blocks, const int32_t* seq_lens, int32_t batch,
+                                           const void* block_pool, const void* tail_pool, float softmax_scale,
+                                           float* out, void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                           int32_t wait_polls, void* stream);
 
 /* Static description of a status code. */
 const char* kvarn_status_string(kvarn_status s);

@@ -195,6 +195,39 @@ def test_fp16_baseline_bf16_layer():
     fp16_case(I.qwen3_4b(), seqs=[0, 5])
 
 
+def test_bounded_wait_expiry_reports_timeout_and_returns():
+    """A record copy that never starts: the wait on it gives up after the
+    short poll limit, the kernel stores KVARN_DEV_ERR_TIMEOUT and returns,
+    and the device keeps working (a normal decode afterwards matches the
+    oracle)."""
+    dev = device()
+    # sequence 0 has closed tiles, so its first unit has a key-record copy to leave out
+    w = I.Workload("wait_expiry", 3, 16, 2, "f16", [700, 129, 2200], seed=23, max_tokens=2400, block_perm=True)
+    c = PagedCache(w, dev)
+    ctx = {b: (I.kv_sequence(w, "k", b, w.seq_lens[b], dev).cpu(), I.kv_sequence(w, "v", b, w.seq_lens[b], dev).cpu())
+           for b in range(w.batch)}
+    recs = load_oracle_records(w, c, list(range(w.batch)), ctx)
+    q = I.queries(w).to(dev)
+    out = torch.zeros(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    lens = c.lens.clone()
+    K.kvarn_test_decode_wait_expiry(c.cfg, q, c.table, c.max_blocks, lens, w.batch, c.pool, c.tail, w.scale, out,
+                                    c.ws, c.ws_bytes, c.err, 64)
+    torch.cuda.synchronize()                                   # the call completes
+    assert c.check_error() == K.KVARN_DEV_ERR_TIMEOUT
+    assert torch.isfinite(out[1:]).all()
+    with pytest.raises(K.KvarnError):                          # the poll limit must be positive
+        K.kvarn_test_decode_wait_expiry(c.cfg, q, c.table, c.max_blocks, lens, w.batch, c.pool, c.tail, w.scale,
+                                        out, c.ws, c.ws_bytes, c.err, 0)
+    c.err.zero_()
+    c.decode(q, out)                                           # the device still answers, correctly
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    want = oracle_outputs(w, list(range(w.batch)), ctx, recs, q.cpu())
+    got = out.cpu().numpy().astype(np.float64)
+    worst = max(np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max() for (b, h), o in want.items())
+    assert worst <= TOL
+
+
 def test_decode_device_errors():
     dev = device()
     w = ragged_small()
