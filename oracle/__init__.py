@@ -71,6 +71,7 @@ def lib():
         L.ora_attention_folded.argtypes = [P, i32, P, P, i32, P, P, i32, dbl, i32, i32, P]
         L.ora_quantize_batch.argtypes = [P, i32, P, i64, i32, i32, i32, P, P, i32]
         L.ora_attention_batch.argtypes = [P, i32, P, P, P, P, P, P, P, dbl, i32, i32, i32, P, i32]
+        L.ora_quantize_batch_fields.argtypes = [P, i32, P, i64, i32, i32, i32, P, P, P, P, P, P, P, i32]
         _lib = L
     return _lib
 
@@ -287,6 +288,26 @@ def quantize_batch(src_bits: np.ndarray, dtype: str, first: np.ndarray, row_stri
     lib().ora_quantize_batch(_p(src_bits), 1 if dtype == "bf16" else 0, _p(first), int(row_stride), n,
                              kind(is_v, k_bits, v_bits), iters, _p(rec), _p(flags), int(nthreads))
     return rec, flags
+
+
+def quantize_batch_fields(src_bits: np.ndarray, dtype: str, first: np.ndarray, row_stride: int, levels: int,
+                          iters: int = 8, nthreads: int | None = None, with_pre: bool = True, with_R: bool = True):
+    """Quantise len(first) tiles read from flat 16-bit storage (as
+    quantize_batch) and return every field unpacked: dict of g8 [n,128],
+    a8 [n,128], b16 [n,128], code [n,128,128], flags [n], and optionally the
+    pre-rounding values pre [n,128,128] and the rotated tiles R [n,128,128]."""
+    src_bits = np.ascontiguousarray(src_bits, dtype=np.uint16).reshape(-1)
+    first = np.ascontiguousarray(first, dtype=np.int64)
+    n = first.shape[0]
+    out = dict(g8=np.empty((n, D), np.uint8), a8=np.empty((n, T), np.uint8), b16=np.empty((n, T), np.uint16),
+               code=np.empty((n, T, D), np.uint8), flags=np.zeros(n, np.int32),
+               pre=np.empty((n, T, D)) if with_pre else None, R=np.empty((n, T, D)) if with_R else None)
+    nthreads = nthreads or os.cpu_count() or 1
+    lib().ora_quantize_batch_fields(_p(src_bits), 1 if dtype == "bf16" else 0, _p(first), int(row_stride), n,
+                                    int(levels), int(iters), _p(out["g8"]), _p(out["a8"]), _p(out["b16"]),
+                                    _p(out["code"]), _p(out["pre"]) if with_pre else None,
+                                    _p(out["R"]) if with_R else None, _p(out["flags"]), int(nthreads))
+    return out
 
 
 def attention_batch(q, krec_lists, vrec_lists, ktails, vtails, n_tail, scale, nthreads=None, k_bits: int = 4,

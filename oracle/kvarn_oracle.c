@@ -582,6 +582,52 @@ void ora_quantize_batch(const uint16_t *src, int dtype, const int64_t *first, in
     for (int k = 0; k < nthreads; k++) pthread_join(th[k], NULL);
 }
 
+/* The same batch with every field of each tile returned unpacked, for
+ * comparisons: tile i's g8[i][128], a8[i][128], b16[i][128] and codes
+ * code[i][128][128] (token-major), and where the pointers are not NULL the
+ * pre-rounding values pre[i][128][128] and the rotated tile R[i][128][128]. */
+typedef struct {
+    const uint16_t *src; int dtype; const int64_t *first; int64_t row_stride;
+    int n, levels, iters, nthreads, tid;
+    uint8_t *g8, *a8; uint16_t *b16; uint8_t *code; double *pre, *R; int *flags;
+} fjob;
+
+static void *fields_worker(void *arg)
+{
+    fjob *j = (fjob *)arg;
+    double *X = (double *)malloc(sizeof(double) * T * D);
+    for (int i = j->tid; i < j->n; i += j->nthreads) {
+        for (int t = 0; t < T; t++)
+            for (int c = 0; c < D; c++) {
+                uint16_t h = j->src[j->first[i] + (int64_t)t * j->row_stride + c];
+                X[t * D + c] = j->dtype ? ora_bf16_decode(h) : ora_f16_decode(h);
+            }
+        int64_t o = (int64_t)i * T * D;
+        int f = ora_quantize_tile(X, j->levels, j->iters, j->g8 + (int64_t)i * D, j->a8 + (int64_t)i * T,
+                                  j->b16 + (int64_t)i * T, j->code + o, j->pre ? j->pre + o : NULL,
+                                  j->R ? j->R + o : NULL, NULL);
+        if (j->flags) j->flags[i] = f;
+    }
+    free(X);
+    return NULL;
+}
+
+void ora_quantize_batch_fields(const uint16_t *src, int dtype, const int64_t *first, int64_t row_stride, int n,
+                               int levels, int iters, uint8_t *g8, uint8_t *a8, uint16_t *b16, uint8_t *code,
+                               double *pre, double *R, int *flags, int nthreads)
+{
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    pthread_t th[256];
+    fjob jobs[256];
+    for (int k = 0; k < nthreads; k++) {
+        jobs[k] = (fjob){src, dtype, first, row_stride, n, levels, iters, nthreads, k, g8, a8, b16, code, pre, R,
+                         flags};
+        pthread_create(&th[k], NULL, fields_worker, &jobs[k]);
+    }
+    for (int k = 0; k < nthreads; k++) pthread_join(th[k], NULL);
+}
+
 /* Decode attention for many independent units (one sequence x KV head
  * each): unit u has G queries q[u][G][D], n_tiles[u] packed K/V records
  * (pointers krec[off[u] + i], vrec[off[u] + i]) and n_tail[u] raw tail

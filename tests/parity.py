@@ -107,6 +107,71 @@ def compare_record(gpu_rec: np.ndarray, tile, is_v: bool, st: Stats, where: str 
         st.valid_checked += int(chk.sum())
 
 
+def unpack_batch(recs: np.ndarray, is_v: bool, k_bits: int = 4, v_bits: int = 2):
+    """unpack() of n records at once: recs [n, record bytes] ->
+    g8 [n,128], a8 [n,128], b16 [n,128], code [n,128,128] (token-major)."""
+    recs = np.ascontiguousarray(recs, dtype=np.uint8)
+    n = recs.shape[0]
+    g8, a8 = recs[:, :128].copy(), recs[:, 128:256].copy()
+    b16 = recs[:, 256:512].copy().view(np.uint16)
+    body = recs[:, 512:]
+    if not is_v and k_bits == 2:
+        by = body.reshape(n, T, 32)
+        code = np.stack([(by >> (2 * k)) & 3 for k in range(4)], axis=-1).reshape(n, T, D)
+    elif not is_v:
+        by = body.reshape(n, T, 64)
+        code = np.empty((n, T, D), np.uint8)
+        code[:, :, 0::2] = by & 15
+        code[:, :, 1::2] = by >> 4
+    elif v_bits == 4:
+        words = body.copy().view("<u4").reshape(n, D, T // 8)
+        pos = np.array([2 * u if u % 2 == 0 else 14 + 2 * u for u in range(8)], dtype=np.uint32)
+        nib = (words[..., None] >> pos) & 15                     # [n][c][w][u] -> token 8w+u
+        code = nib.reshape(n, D, T).transpose(0, 2, 1)
+    else:
+        words = body.copy().view("<u4").reshape(n, D, T // 16)
+        pos = np.array([u if u % 2 == 0 else 15 + u for u in range(16)], dtype=np.uint32)
+        crumbs = (words[..., None] >> pos) & 3                   # [n][c][w][u] -> token 16w+u
+        code = crumbs.reshape(n, D, T).transpose(0, 2, 1)
+    return g8, a8, b16, np.ascontiguousarray(code, dtype=np.uint8)
+
+
+def compare_batch(gpu_recs: np.ndarray, ora: dict, is_v: bool, st: Stats, where: str = "", k_bits: int = 4,
+                  v_bits: int = 2):
+    """compare_record() over n tiles at once.  ora: the oracle's fields of the
+    same inputs (oracle.quantize_batch_fields with pre and R)."""
+    L = 15 if (v_bits if is_v else k_bits) == 4 else 3
+    g8, a8, b16, code = unpack_batch(gpu_recs, is_v, k_bits, v_bits)
+    n = code.shape[0]
+    st.tiles += n
+    st.codes += code.size
+    assert code.max() <= L, where
+    dg = np.abs(g8.astype(int) - ora["g8"].astype(int))
+    da = np.abs(a8.astype(int) - ora["a8"].astype(int))
+    db = np.abs(f16_order(b16) - f16_order(ora["b16"]))
+    assert dg.max() <= 1 and da.max() <= 1 and db.max() <= 1, f"{where}: scale off by more than one code"
+    st.g_flip += int((dg > 0).sum()); st.a_flip += int((da > 0).sum()); st.b_flip += int((db > 0).sum())
+    same = (dg == 0)[:, None, :] & (da == 0)[:, :, None] & (db == 0)[:, :, None]
+    pre = ora["pre"]
+    near = np.abs(pre - np.floor(pre) - 0.5) < 1e-5
+    mism = code != ora["code"]
+    bad = mism & same & ~near
+    assert not bad.any(), f"{where}: {int(bad.sum())} codes differ with identical scales (first {np.argwhere(bad)[:3]})"
+    tie = mism & same & near
+    assert (np.abs(code.astype(int) - ora["code"].astype(int))[tie] <= 1).all(), where
+    st.tie_diff += int(tie.sum())
+    diff_tiles = np.nonzero(~same.reshape(n, -1).all(axis=1))[0]
+    for i in diff_tiles:                     # a scale differs: the GPU code is the nearest level of its own scales
+        g, a, b = e4m3(g8[i]), e4m3(a8[i]), f16(b16[i])
+        t = (ora["R"][i] / g[None, :] - b[:, None]) / a[:, None]
+        want = np.clip(np.rint(t), 0, L)
+        near2 = np.abs((t - np.floor(t)) - 0.5) < 1e-5
+        chk = ~same[i]
+        badv = chk & (code[i] != want) & ~(near2 & (np.abs(code[i] - want) <= 1))
+        assert not badv.any(), f"{where} tile {i}: {int(badv.sum())} codes are not the nearest level of their own scales"
+        st.valid_checked += int(chk.sum())
+
+
 def finish(st: Stats):
     assert st.tie_diff <= 1e-4 * max(st.codes, 1), f"too many boundary flips: {st}"
     return st

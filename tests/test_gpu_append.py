@@ -10,32 +10,37 @@ from bit_kv_cache_quantize_gb300 import kvarn as K
 from bit_kv_cache_quantize_gb300.cache import PagedCache
 
 import parity as PR
-from gpu_helpers import bits, device, oracle_attention_units, oracle_tiles
-from test_gpu_decode import load_oracle_records
+from gpu_helpers import bits, device, oracle_decode, oracle_tiles, upload_oracle_prefill
 
 pytestmark = pytest.mark.gpu
 T = D = 128
 TOL = 1e-3
 
 
-def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
+def run_steps(w, steps, check_seqs=None, attend_every=1, full_check_steps=()):
+    """Prefill, then `steps` decode steps (append one token per sequence,
+    attend).  Every tile that closes (any sequence) is compared with the
+    oracle record by record; the attention of `check_seqs` (default all) is
+    compared with the oracle's after every `attend_every`-th step and the
+    last, and that of every sequence at the steps in `full_check_steps`.
+    Sequences whose attention is checked hold oracle records only."""
     dev = device()
     c = PagedCache(w, dev)
     c.prefill()
     torch.cuda.synchronize()
     assert c.check_error() == 0
     check_seqs = list(range(w.batch)) if check_seqs is None else check_seqs
+    attend_seqs = list(range(w.batch)) if full_check_steps else check_seqs
     total = [n + steps for n in w.seq_lens]
-    # inputs generated once on the device; the oracle reads the same bytes
-    ctx = {b: (I.kv_sequence(w, "k", b, total[b], dev).cpu(), I.kv_sequence(w, "v", b, total[b], dev).cpu())
-           for b in check_seqs}
-    # closed prefill tiles of the checked sequences: oracle records
-    pre_ctx = {b: (ctx[b][0][:w.seq_lens[b]], ctx[b][1][:w.seq_lens[b]]) for b in check_seqs}
-    recs = load_oracle_records(w, c, check_seqs, pre_ctx)
+    # oracle records for the closed prefill tiles of every sequence whose
+    # attention is checked; raw tokens from its open tile on are kept on the
+    # host (inputs generated on the device; the oracle reads the same bytes)
+    recs, kept = upload_oracle_prefill(w, c, attend_seqs, keep_to=total)
     st = PR.Stats()
     lens = torch.tensor(w.seq_lens, dtype=torch.int32)
     out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
     worst = 0.0
+    n_attended = set()
     for s in range(steps):
         pos = lens.clone()
         k_new = torch.stack([I.kv_values(w, "k", b, int(pos[b]), 1, dev)[0] for b in range(w.batch)])
@@ -63,32 +68,35 @@ def run_steps(w, steps, check_seqs=None, attend_every=1, sample_seed=0):
             PR.compare_record(c.record(blk, h, kv).cpu().numpy(), tl, bool(kv), st,
                               where=f"step {s} seq {b} closed tile {t} head {h} kv {kv}", k_bits=w.k_bits,
                               v_bits=w.v_bits)
-            if b in ctx:  # decode parity reads oracle records only
+            if b in kept:  # decode parity reads oracle records only
                 rec = O.pack_record(bool(kv), tl, w.k_bits, w.v_bits)
                 recs[(b, t, h, kv)] = rec
                 c.set_record(blk, h, kv, torch.from_numpy(rec).to(dev))
-        if s % attend_every and s != steps - 1:
+        full = s in full_check_steps
+        if not full and s % attend_every and s != steps - 1:
             continue
         q = I.queries(w, step=s + 1, device=dev).cpu()
         c.decode(q.to(dev), out, lens=lens.to(dev))
         torch.cuda.synchronize()
         assert c.check_error() == 0
         got = out.cpu().numpy().astype(np.float64)
+        seqs = attend_seqs if full else check_seqs
         units, ukeys = [], []
-        for b in check_seqs:
+        for b in seqs:
             n = int(lens[b])
             nf = n // T
-            k, v = ctx[b]
+            k, v, lo = kept[b]
             for h in range(w.num_kv_heads):
-                units.append(dict(q=O.decode16(bits(q[b, h * w.G:(h + 1) * w.G]), w.dtype),
-                                  krec=[recs[(b, t, h, 0)] for t in range(nf)],
-                                  vrec=[recs[(b, t, h, 1)] for t in range(nf)],
-                                  ktail=O.decode16(bits(k[nf * T:n, h]), w.dtype).reshape(-1, D),
-                                  vtail=O.decode16(bits(v[nf * T:n, h]), w.dtype).reshape(-1, D)))
+                units.append((O.decode16(bits(q[b, h * w.G:(h + 1) * w.G]), w.dtype),
+                              [recs[(b, t, h, 0)] for t in range(nf)], [recs[(b, t, h, 1)] for t in range(nf)],
+                              O.decode16(bits(k[nf * T - lo:n - lo, h]), w.dtype).reshape(-1, D),
+                              O.decode16(bits(v[nf * T - lo:n - lo, h]), w.dtype).reshape(-1, D)))
                 ukeys.append((b, h))
-        for (b, h), o in zip(ukeys, oracle_attention_units(units, w.scale, w.k_bits, w.v_bits)):
+        want = oracle_decode(w, units, w.scale, w.k_bits, w.v_bits)
+        for (b, h), o in zip(ukeys, want):
             worst = max(worst, np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max())
-    print(w.name, PR.finish(st), f"max |gpu - oracle| = {worst:.3e}")
+            n_attended.add(b)
+    print(w.name, PR.finish(st), f"max |gpu - oracle| = {worst:.3e} over {len(n_attended)} sequences")
     assert worst <= TOL
     return st
 
@@ -121,13 +129,13 @@ def test_append_close_bf16():
 
 
 @pytest.mark.slow
-def test_ragged_serving_full_size_sampled():
-    """256 sequences, lengths U[128, 32768], 64 decode steps; every tile that
-    closes (any sequence) is compared with the oracle, and attention on 8
-    sampled sequences (4 of them closing a tile during the run) after every
-    step."""
+def test_ragged_serving_full_size():
+    """256 sequences, lengths U[128, 32768], 64 decode steps: every tile that
+    closes (any sequence) is compared with the oracle; the attention of all
+    256 sequences is compared at steps 0 and 63, and that of 8 sampled
+    sequences (4 of them closing a tile during the run) after every step."""
     w = I.ragged_32b()
     lens = np.array(w.seq_lens)
     closing = [b for b in range(w.batch) if (lens[b] % T) + 64 >= T][:4]
     others = [b for b in range(w.batch) if b not in closing][:4]
-    run_steps(w, 64, check_seqs=closing + others, attend_every=1)
+    run_steps(w, 64, check_seqs=closing + others, attend_every=1, full_check_steps=(0, 63))

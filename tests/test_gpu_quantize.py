@@ -9,7 +9,7 @@ from bit_kv_cache_quantize_gb300 import kvarn as K
 from bit_kv_cache_quantize_gb300.cache import PagedCache
 
 import parity as PR
-from gpu_helpers import device, oracle_tiles, tile_values
+from gpu_helpers import bits, device, oracle_tiles, tile_values
 
 pytestmark = pytest.mark.gpu
 T = D = 128
@@ -83,9 +83,10 @@ def test_k2_qwen3_4b_layer_all_tiles():
 
 
 @pytest.mark.slow
-def test_prefill_32b_full_size_sampled():
+def test_prefill_32b_full_size_all_tiles():
     """All 32 x 16384 tokens x 8 heads (65536 tile jobs) in the launch the
-    benchmark times, sampled tiles checked."""
+    benchmark times; every record compared with the oracle's (the oracle
+    runs on all host cores, a chunk of tiles at a time)."""
     w = I.prefill_32b()
     dev = device()
     c = PagedCache(w, dev)
@@ -101,15 +102,24 @@ def test_prefill_32b_full_size_sampled():
     K.kvarn_quantize_tiles(c.cfg, k, v, w.num_kv_heads * D, B * n, first, dst, n_tiles, c.pool, c.err)
     torch.cuda.synchronize()
     assert c.check_error() == 0
-    rng = np.random.default_rng(5)
-    picks = [(int(i) // (w.num_kv_heads * 2), int(i) // 2 % w.num_kv_heads, int(i) % 2)
-             for i in rng.choice(n_tiles * w.num_kv_heads * 2, 48, replace=False)]
-    tiles = oracle_tiles([((v if kv else k)[i * T:(i + 1) * T, h], kv) for i, h, kv in picks], w.dtype)
+    H = w.num_kv_heads
+    pool = c.pool.cpu().numpy()
+    srcs = [bits(k).reshape(-1), bits(v).reshape(-1)]
+    del k, v
+    dsth = dst.cpu().numpy().astype(np.int64)
     st = PR.Stats()
-    for (i, h, kv), tl in zip(picks, tiles):
-        rec = c.record(int(dst[i]), h, kv).cpu().numpy()
-        PR.compare_record(rec, tl, bool(kv), st, where=f"tile {i} head {h} kv {kv}")
+    CH = 64                                            # tiles per chunk (x 8 heads x K|V)
+    for t0 in range(0, n_tiles, CH):
+        tiles = np.arange(t0, min(n_tiles, t0 + CH))
+        first = (tiles[:, None] * (T * H * D) + np.arange(H)[None, :] * D).reshape(-1)
+        for kv in (0, 1):
+            ora = O.quantize_batch_fields(srcs[kv], w.dtype, first, H * D, O.levels(bool(kv)))
+            rb = K.rec_bytes(2 if kv else 4)
+            offs = (dsth[tiles][:, None] * c.block_bytes + np.arange(H)[None, :] * K.HEAD_REC + kv * K.K_REC)
+            recs = pool[offs.reshape(-1)[:, None] + np.arange(rb)[None, :]]
+            PR.compare_batch(recs, ora, bool(kv), st, where=f"tiles {t0}.. {'V' if kv else 'K'}")
     print(PR.finish(st))
+    assert st.tiles == n_tiles * H * 2 == 65536
 
 
 def degenerate_tiles(dtype):
