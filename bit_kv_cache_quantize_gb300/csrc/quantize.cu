@@ -31,6 +31,7 @@ struct QSmem {
   alignas(128) unsigned char xs[65536];
   float beta[D];                            // column factors exp(-v) of the last column step
   float inv_g[D];
+  float g[D];                               // the channel scales themselves (unrotated path)
   float vred[8];
 };
 constexpr int X_ROW = 272;                 // staging row stride: 256 B + 16 B pad
@@ -110,19 +111,29 @@ struct MaxOp { __device__ float operator()(float a, float b) const { return fmax
 
 // Step 6 for this thread's 8 tokens x 8 channels: code = rne((Y - b) * (1/a))
 // (two fp32 roundings, as written), clamped below at 0 when CLAMP; adding
-// 1.5 * 2^23 leaves the rounded integer in the low mantissa bits.  K4: byte
+// 1.5 * 2^23 leaves the rounded integer in the low mantissa bits.  With
+// EXACT (the unrotated path, whose Y are exact quotients of the 16-bit
+// inputs, so that (Y - b) / a often is exactly k + 1/2) the quotient is the
+// correctly rounded IEEE division instead, and an exact tie goes to the
+// even level as the definition says; tokv then holds a, not 1/a.  K4: byte
 // pair p of token t = code[2p] | code[2p+1] << 4.  K2: byte i of token t =
 // sum_k code[4i+k] << 2k.  V2: token 16w + u of a channel at bit u (u even)
 // or 15 + u (u odd) of the channel's word w; tokens tok0 .. tok0+7
 // (u = 8h + i) fill byte h (even i, at bit i) and byte 2 + h (odd i, at bit i - 1).
-template <int KIND, bool CLAMP>
+template <int KIND, bool CLAMP, bool EXACT = false>
 __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float2* tokv, unsigned char* rec,
                                             int tok0, int cb) {
   constexpr int L = kind_levels(KIND);
   constexpr float RNE_MAGIC = 12582912.0f;
   const float2 MAG2 = make_float2(RNE_MAGIC, RNE_MAGIC);
   auto code2 = [&](float2 y, float2 nb, float2 ia) {
-    float2 q2 = fmul2(fadd2(y, nb), ia);
+    float2 q2;
+    if constexpr (EXACT) {
+      const float2 d = fadd2(y, nb);
+      q2 = make_float2(__fdiv_rn(d.x, ia.x), __fdiv_rn(d.y, ia.y));
+    } else {
+      q2 = fmul2(fadd2(y, nb), ia);
+    }
     // a min between the product and the rounding add keeps the two from being
     // fused into one FMA (which would round once instead of twice); without
     // saturation it only ever trims L (1 + 2^-23) to L
@@ -431,6 +442,7 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
     if (gc == 0) gc = 0x01;
     rec[tid] = gc;
     sm.inv_g[tid] = __frcp_rn(e4m3_to_float(gc));
+    sm.g[tid] = e4m3_to_float(gc);
   }
   __syncthreads();
 
@@ -443,10 +455,18 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
     ig[0] = make_float2(g0.x, g0.y); ig[1] = make_float2(g0.z, g0.w);
     ig[2] = make_float2(g1.x, g1.y); ig[3] = make_float2(g1.z, g1.w);
   }
+  if constexpr (ROT) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) r[i][pp] = fmul2(r[i][pp], ig[pp]);   // r now holds Y = R / g
+      for (int pp = 0; pp < 4; ++pp) r[i][pp] = fmul2(r[i][pp], ig[pp]);   // r now holds Y = R / g
+  } else {  // unrotated: Y = X / g correctly rounded (exact whenever the quotient is an fp32 number)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp)
+        r[i][pp] = make_float2(__fdiv_rn(r[i][pp].x, sm.g[8 * cb + 2 * pp]), __fdiv_rn(r[i][pp].y, sm.g[8 * cb + 2 * pp + 1]));
+  }
   {
     float mm[8][2];
 #pragma unroll
@@ -476,15 +496,15 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
       const int tk = tok0 + ((lane & 15) >> 1);
       rec[128 + tk] = ac;
       *reinterpret_cast<__half*>(rec + 256 + 2 * tk) = bh;
-      tokv[tk] = make_float2(bv, inv_a);
+      tokv[tk] = make_float2(bv, ROT ? inv_a : e4m3_to_float(ac));
     }
   }
   const bool clamp_codes = __syncthreads_or(sat);
 
   // ---- 6. codes and packing: code = rne((Y - b) * (1/a)), clamped to [0, L]
   // only in a tile where some token saturated its zero-point or step
-  if (clamp_codes) encode_pack<KIND, true>(r, tokv, rec, tok0, cb);
-  else encode_pack<KIND, false>(r, tokv, rec, tok0, cb);
+  if (clamp_codes) encode_pack<KIND, true, !ROT>(r, tokv, rec, tok0, cb);
+  else encode_pack<KIND, false, !ROT>(r, tokv, rec, tok0, cb);
   __syncthreads();
   const int bytes = kind_rec_bytes(KIND);
   for (int i = tid; i < bytes / 16; i += 256)
