@@ -36,17 +36,30 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(OUT, exist_ok=True)
+OUT_CHECK = os.path.join(PKG, "_build_check")
+LIB_CHECK = os.path.join(OUT_CHECK, "libkvarn_check.so")
+
+
+def build_checked(force: bool = False, verbose: bool = False) -> str:
+    """The checked (debug) build: the same sources compiled with KVARN_CHECK,
+    so that every global store, partial read and bulk-copy source is tested
+    against its buffer first (an out-of-range access is skipped and reported
+    as KVARN_DEV_ERR_BOUNDS).  A separate library, libkvarn_check.so; the
+    tests load it in place of libkvarn.so."""
+    return build(force, verbose, out=OUT_CHECK, lib=LIB_CHECK, extra=["-DKVARN_CHECK"])
+
+
+def build(force: bool = False, verbose: bool = False, out: str = OUT, lib: str = LIB, extra=()) -> str:
+    os.makedirs(out, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "kvarn.h")]
     nvcc = _nvcc()
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT, src.replace(".cu", ".o"))
+        o = os.path.join(out, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
-            jobs.append(([nvcc] + NVCC_FLAGS + ["-c", s, "-o", o + ".tmp"], o))
+            jobs.append(([nvcc] + NVCC_FLAGS + list(extra) + ["-c", s, "-o", o + ".tmp"], o))
 
     def run(job):
         cmd, o = job
@@ -63,12 +76,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
             for log in ex.map(run, jobs):
                 if verbose:
                     sys.stderr.write(log)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".{os.getpid()}.tmp"
         subprocess.check_call([nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True))
+    if "--checked" in sys.argv:
+        print(build_checked(force="--force" in sys.argv, verbose=True))

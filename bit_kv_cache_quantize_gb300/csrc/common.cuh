@@ -31,6 +31,23 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Bounds check of the checked (debug) build, compiled with KVARN_CHECK: an
+// access of n bytes at p must lie inside [base, base + bytes); otherwise the
+// first error is recorded as KVARN_DEV_ERR_BOUNDS and the caller skips the
+// access.  In the normal build it is the constant true and compiles away.
+__device__ __forceinline__ bool kcheck(const void* p, size_t n, const void* base, size_t bytes, int32_t* err) {
+#ifdef KVARN_CHECK
+  const char* a = static_cast<const char*>(p);
+  const char* lo = static_cast<const char*>(base);
+  if (a >= lo && n <= bytes && static_cast<size_t>(a - lo) <= bytes - n) return true;
+  set_error(err, KVARN_DEV_ERR_BOUNDS);
+  return false;
+#else
+  (void)p; (void)n; (void)base; (void)bytes; (void)err;
+  return true;
+#endif
+}
+
 // ------------------------------------------------------------------ MMA
 // Bits of +1.0 in the 16-bit element type E.
 template <typename E> struct Bits16;

@@ -198,9 +198,9 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
       return;  // error-path test: this copy never starts, so its wait must expire
     const int32_t blk = tab[first + warp + k * DEC_WARPS];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
-    if (blk >= 0 && blk < p.num_blocks) {
-      const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * head_rec(KBITS, VBITS) + (is_v ? KREC : 0);
-      const uint32_t bytes = is_v ? VREC : KREC;
+    const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * head_rec(KBITS, VBITS) + (is_v ? KREC : 0);
+    const uint32_t bytes = is_v ? VREC : KREC;
+    if (blk >= 0 && blk < p.num_blocks && kcheck(src, bytes, p.pool, (size_t)p.num_blocks * p.block_bytes, p.err)) {
       mbar_expect_tx(bar, bytes);
       bulk_g2s(is_v ? sm.vrec[warp] : sm.krec[warp], src, bytes, bar);
     } else {
@@ -494,6 +494,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
       }
     }
     float* o = part_ptr(p, b, h, chunk, gg);
+    if (!kcheck(o, PART * sizeof(float), p.ws, (size_t)p.ws_bytes, p.err)) continue;
     if (c == 0) { o[0] = M; o[1] = Lsum; }
     o[PACC + c] = A;
   }
@@ -514,6 +515,8 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
   __syncthreads();
   const E* kt = static_cast<const E*>(p.tail) + (((int64_t)b * p.num_kv_heads + h) * 2 + 0) * (T * D);
   const E* vt = kt + T * D;
+  if (!kcheck(kt, 2 * T * D * sizeof(E), p.tail, (size_t)gridDim.z * p.num_kv_heads * 2 * T * D * sizeof(E), p.err))
+    return;
   if (tid < n) {
     float s[8];
 #pragma unroll
@@ -551,6 +554,7 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
   }
   for (int gg = 0; gg < G; ++gg) {
     float* out = part_ptr(p, b, h, p.n_chunks, gg);
+    if (!kcheck(out, PART * sizeof(float), p.ws, (size_t)p.ws_bytes, p.err)) continue;
     if (tid == 0) { out[0] = ml[2 * gg]; out[1] = ml[2 * gg + 1]; }
     out[PACC + tid] = a[gg];
   }
@@ -565,7 +569,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p, int rotate
   const int h = hq / p.G, g = hq % p.G;
   const int len = p.seq_lens[b];
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (len > 0 && len <= T * p.max_blocks) {
+  const float* plo = part_ptr(p, b, h, 0, g);
+  const size_t pspan = (size_t)(part_ptr(p, b, h, p.n_chunks, g) + PART - plo) * sizeof(float);
+  if (len > 0 && len <= T * p.max_blocks && kcheck(plo, pspan, p.ws, (size_t)p.ws_bytes, p.err)) {
     const int n_tc = rotate ? ((len / T) + p.chunk_tiles - 1) / p.chunk_tiles
                             : (((len + T - 1) / T) + p.chunk_tiles - 1) / p.chunk_tiles;
     const bool has_tail = rotate && (len % T) != 0;
@@ -612,7 +618,9 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p, int rotate
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     o = make_float4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
   }
-  *reinterpret_cast<float4*>(out + ((int64_t)b * p.num_q_heads + hq) * D + 4 * lane) = o;
+  float* dst = out + ((int64_t)b * p.num_q_heads + hq) * D + 4 * lane;
+  if (kcheck(dst, sizeof(float4), out, (size_t)batch * p.num_q_heads * D * sizeof(float), p.err))
+    *reinterpret_cast<float4*>(dst) = o;
 }
 
 // ------------------------------------------------------------------ 16-bit comparison kernel
@@ -802,6 +810,7 @@ __global__ void __launch_bounds__(256, 1) decode_f16_kernel(const __grid_constan
       }
     }
     float* o = part_ptr(p, b, h, chunk, gg);
+    if (!kcheck(o, PART * sizeof(float), p.ws, (size_t)p.ws_bytes, p.err)) continue;
     if (c == 0) { o[0] = M; o[1] = Lsum; }
     o[PACC + c] = A;
   }
@@ -873,6 +882,7 @@ cudaError_t launch_decode_noalloc(DecodeParams p, int dtype, int batch, float* o
   cudaError_t e = scratch_address(&ws);
   if (e != cudaSuccess) return e;
   p.ws = ws;
+  p.ws_bytes = KVARN_NOALLOC_SCRATCH_BYTES;
   return launch_decode(p, dtype, batch, out, s);
 }
 

@@ -180,7 +180,8 @@ static kvarn_status decode_call(const kvarn_config* cfg, const void* q, const in
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
                  static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
                  max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads,
-                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits, cfg->v_bits, wait_polls, skip_first_copy};
+                 cfg->num_blocks, chunk, n_chunks, cfg->k_bits, cfg->v_bits, wait_polls, skip_first_copy,
+                 static_cast<int64_t>(workspace_bytes)};
   return cuda_status(launch_decode(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -244,7 +245,7 @@ kvarn_status kvarn_multiquery_attention(const kvarn_config* cfg, const void* q, 
   MQParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
              static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
              max_blocks, cfg->num_kv_heads, cfg->num_q_heads, cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks,
-             n_queries, n_rb, chunk, n_chunks, cfg->k_bits, cfg->v_bits};
+             n_queries, n_rb, chunk, n_chunks, cfg->k_bits, cfg->v_bits, static_cast<int64_t>(workspace_bytes)};
   return cuda_status(launch_multiquery(p, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -282,7 +283,8 @@ kvarn_status kvarn_fp16_decode_attention(const kvarn_config* cfg, const void* q,
   const int n_chunks = (max_blocks + kF16ChunkTiles - 1) / kF16ChunkTiles;
   DecodeParams p{q, block_table, seq_lens, nullptr, nullptr, static_cast<float*>(workspace), dev_err, 0,
                  softmax_scale, max_blocks, cfg->num_kv_heads, cfg->num_q_heads,
-                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks, 16, 16};
+                 cfg->num_q_heads / cfg->num_kv_heads, cfg->num_blocks, kF16ChunkTiles, n_chunks, 16, 16, 0, 0,
+                 static_cast<int64_t>(workspace_bytes)};
   cudaError_t e = launch_decode_f16(p, fp16_pool, cfg->dtype, batch, out, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorInvalidValue) return KVARN_ERR_INVALID;
   if (e == cudaErrorNotSupported) return KVARN_ERR_UNSUPPORTED;

@@ -375,6 +375,7 @@ __device__ void mq_tail(const MQParams& p, int b, int h, int rb, int len, unsign
   }
   if (!rv) return;
   float* o = mq_part(p, b, h, rb, p.n_chunks, r);
+  if (!kcheck(o, MQ_PART * sizeof(float), p.ws, (size_t)p.ws_bytes, p.err)) return;
   if (half == 0) { o[0] = m; o[1] = l; }
 #pragma unroll
   for (int c4 = 0; c4 < 16; ++c4)
@@ -554,10 +555,10 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   // one bulk copy of the K and V records of tile k into its stage (one thread)
   auto issue_rec = [&](int k) {
     const int s = k % REC_STAGES;
-    if ((vmask >> k) & 1u) {
+    const unsigned char* src = p.pool + tab[k] * p.block_bytes + (int64_t)h * (KREC + VREC);
+    if (((vmask >> k) & 1u) && kcheck(src, KREC + VREC, p.pool, (size_t)p.num_blocks * p.block_bytes, p.err)) {
       mbar_expect_tx(&sm.rec_full[s], KREC + VREC);
-      bulk_g2s(sm.rec[s], p.pool + tab[k] * p.block_bytes + (int64_t)h * (KREC + VREC), KREC + VREC,
-               &sm.rec_full[s]);
+      bulk_g2s(sm.rec[s], src, KREC + VREC, &sm.rec_full[s]);
     } else {
       set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
       mbar_arrive(&sm.rec_full[s]);
@@ -819,7 +820,8 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
     ok = wait_all(&sm.lbar, 0, p.err) && ok;
     tc_fence_after();
     float* o = mq_part(p, b, h, rb, chunk, rv ? r : 0);
-    if (rv && half == 0) {
+    const bool wv = rv && kcheck(o, MQ_PART * sizeof(float), p.ws, (size_t)p.ws_bytes, p.err);
+    if (wv && half == 0) {
       o[0] = ok ? m_ref : -INFINITY;
       o[1] = ok ? l_sum + sm.xl[1][r] : 0.f;
     }
@@ -828,7 +830,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       uint32_t d[16];
       tmem_ld16(lane_base + TM_O + 64 * half + c, d);
       tmem_wait_ld();
-      if (rv) {
+      if (wv) {
         float* oa = o + MQ_PACC + 64 * half + c;
 #pragma unroll
         for (int i = 0; i < 16; i += 4)
@@ -855,7 +857,9 @@ __global__ void __launch_bounds__(128) mq_combine_kernel(MQParams p, int batch, 
   const int R = qi * p.G + gq, rb = R / MQ_ROWS, r = R % MQ_ROWS;
   const int len = p.seq_lens[b];
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (len >= p.n_queries && len <= T * p.max_blocks) {
+  const float* plo = mq_part(p, b, h, rb, 0, r);
+  const size_t pspan = (size_t)(mq_part(p, b, h, rb, p.n_chunks, r) + MQ_PART - plo) * sizeof(float);
+  if (len >= p.n_queries && len <= T * p.max_blocks && kcheck(plo, pspan, p.ws, (size_t)p.ws_bytes, p.err)) {
     int rows, n_need;
     mq_block_extent(p, rb, len, rows, n_need);
     const int n_c = (n_need + p.chunk_tiles - 1) / p.chunk_tiles;
@@ -904,7 +908,9 @@ __global__ void __launch_bounds__(128) mq_combine_kernel(MQParams p, int batch, 
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
     o = make_float4(x[0] * inv, x[1] * inv, x[2] * inv, x[3] * inv);
   }
-  *reinterpret_cast<float4*>(out + (((int64_t)b * p.n_queries + qi) * p.num_q_heads + hq) * D + 4 * lane) = o;
+  float* dst = out + (((int64_t)b * p.n_queries + qi) * p.num_q_heads + hq) * D + 4 * lane;
+  if (kcheck(dst, sizeof(float4), out, (size_t)batch * p.n_queries * p.num_q_heads * D * sizeof(float), p.err))
+    *reinterpret_cast<float4*>(dst) = o;
 }
 
 template <typename E, int KBITS, int VBITS>

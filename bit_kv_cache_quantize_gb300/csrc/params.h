@@ -71,6 +71,7 @@ struct DecodeParams {
   // so that its wait expires with nothing in flight.
   int32_t wait_polls;
   int32_t skip_first_copy;
+  int64_t ws_bytes;  // bytes of ws (the bounds checks of the checked build)
 };
 // Multi-query causal attention: n_queries query tokens per sequence at the
 // last n_queries positions, grouped with their GQA heads into row blocks of
@@ -96,6 +97,7 @@ struct MQParams {
   int32_t n_chunks;
   int32_t k_bits;
   int32_t v_bits;
+  int64_t ws_bytes;  // bytes of ws (the bounds checks of the checked build)
 };
 
 // Per-token reconstruction errors of quantised tiles (the error study):

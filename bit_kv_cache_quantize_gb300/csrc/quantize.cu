@@ -535,6 +535,11 @@ __global__ void __launch_bounds__(256, 2) quantize_tiles_kernel(QuantizeParams p
   const E* src = static_cast<const E*>(kv ? prm.v : prm.k) + first * prm.token_stride + h * D;
   unsigned char* dst =
       prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits, prm.v_bits) + kv * rec_bytes(prm.k_bits);
+  if (!kcheck(dst, rec_bytes(kv ? prm.v_bits : prm.k_bits), prm.pool, (size_t)prm.num_blocks * prm.block_bytes,
+              prm.err) ||
+      !kcheck(src, ((T - 1) * prm.token_stride + D) * sizeof(E), kv ? prm.v : prm.k,
+              (size_t)prm.n_tokens * prm.token_stride * sizeof(E), prm.err))
+    return;
   if (kv && prm.v_bits == 4) quantize_tile_cta<E, KIND_V4>(src, prm.token_stride, dst, prm.iters, sm);
   else if (kv) quantize_tile_cta<E, KIND_V2>(src, prm.token_stride, dst, prm.iters, sm);
   else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(src, prm.token_stride, dst, prm.iters, sm);
@@ -556,6 +561,8 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
   }
   E* tile = static_cast<E*>(prm.tail) + ((static_cast<int64_t>(b) * prm.num_kv_heads + h) * 2 + kv) * (T * D);
   const int slot = pos & (T - 1);
+  if (!kcheck(tile, T * D * sizeof(E), prm.tail, (size_t)gridDim.x * prm.num_kv_heads * 2 * T * D * sizeof(E), prm.err))
+    return;
   if (threadIdx.x < 16) {
     const E* src = static_cast<const E*>(kv ? prm.v_new : prm.k_new) + (static_cast<int64_t>(b) * prm.num_kv_heads + h) * D;
     reinterpret_cast<uint4*>(tile + slot * D)[threadIdx.x] = reinterpret_cast<const uint4*>(src)[threadIdx.x];
@@ -570,6 +577,9 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
   __syncthreads();
   unsigned char* dst =
       prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits, prm.v_bits) + kv * rec_bytes(prm.k_bits);
+  if (!kcheck(dst, rec_bytes(kv ? prm.v_bits : prm.k_bits), prm.pool, (size_t)prm.num_blocks * prm.block_bytes,
+              prm.err))
+    return;
   if (kv && prm.v_bits == 4) quantize_tile_cta<E, KIND_V4>(tile, D, dst, prm.iters, sm);
   else if (kv) quantize_tile_cta<E, KIND_V2>(tile, D, dst, prm.iters, sm);
   else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(tile, D, dst, prm.iters, sm);
@@ -593,6 +603,11 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
   }
   const unsigned char* src = pool + blk * block_bytes + h * head_rec(k_bits, v_bits) + kv * rec_bytes(k_bits);
   const int bytes = kv ? rec_bytes(v_bits) : rec_bytes(k_bits);
+  float* const o0 = out + ((static_cast<int64_t>(n) * 2 + kv) * num_kv_heads + h) * T * D;  // this CTA's rows
+  if (!kcheck(src, bytes, pool, (size_t)num_blocks * block_bytes, err) ||
+      !kcheck(o0, T * D * sizeof(float), out, (size_t)gridDim.x * 2 * num_kv_heads * T * D * sizeof(float), err))
+    return;
+  float* o = o0 + t * D;
   for (int i = t; i < bytes / 16; i += 128)
     reinterpret_cast<uint4*>(rec)[i] = reinterpret_cast<const uint4*>(src)[i];
   __syncthreads();
@@ -618,7 +633,6 @@ __global__ void __launch_bounds__(128) dequantize_kernel(const unsigned char* __
         x[i] = u + w;
         x[i + hh] = u - w;
       }
-  float* o = out + (((static_cast<int64_t>(n) * 2 + kv) * num_kv_heads + h) * T + t) * D;
 #pragma unroll
   for (int c = 0; c < D; c += 4)
     *reinterpret_cast<float4*>(o + c) =
@@ -654,6 +668,12 @@ __global__ void __launch_bounds__(256, 2) token_errors_kernel(ErrParams prm) {
   }
   const E* src = static_cast<const E*>(prm.x) + first * prm.token_stride + h * D;
   unsigned char* rec = prm.scratch + (int64_t)job * kind_rec_bytes(KIND);
+  if (!kcheck(rec, kind_rec_bytes(KIND), prm.scratch, (size_t)gridDim.x * kind_rec_bytes(KIND), prm.err) ||
+      !kcheck(prm.out + (int64_t)job * T * 2, T * 2 * sizeof(float), prm.out, (size_t)gridDim.x * T * 2 * sizeof(float),
+              prm.err) ||
+      !kcheck(src, ((T - 1) * prm.token_stride + D) * sizeof(E), prm.x,
+              (size_t)prm.n_tokens * prm.token_stride * sizeof(E), prm.err))
+    return;
   quantize_tile_cta<E, KIND, ROT>(src, prm.token_stride, rec, prm.iters, sm);
   __syncthreads();  // the record is in global memory, written by this CTA
   const int t = threadIdx.x >> 1, hf = threadIdx.x & 1;

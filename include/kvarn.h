@@ -97,6 +97,7 @@ typedef enum kvarn_dtype {
 #define KVARN_DEV_ERR_BLOCK_RANGE 1 /* a block id outside [0, num_blocks) */
 #define KVARN_DEV_ERR_TOKEN_RANGE 2 /* a token index, position or length out of range */
 #define KVARN_DEV_ERR_TIMEOUT 3     /* a bounded wait on an async copy expired */
+#define KVARN_DEV_ERR_BOUNDS 4      /* checked (debug) build only: an access outside its buffer was skipped */
 
 typedef struct kvarn_config {
   int32_t head_dim;       /* channels per head; must be 128 */
