@@ -28,17 +28,19 @@ static int min_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
   return small_call(batch, num_kv_heads, max_blocks) ? kSmallChunkTiles : kChunkTiles;
 }
 
-// Packed tiles per split-K CTA for one call: 8 for a small call; else 32
-// (longer CTAs amortise the per-CTA query set-up and merge) when that still
-// gives at least three waves of CTAs at two per SM, else 16.
+// Packed tiles per split-K CTA for one call: 8 for a small call; else the
+// longest of 64 and 32 (longer CTAs amortise the per-CTA query set-up and
+// merge) that still gives at least three waves of CTAs at two per SM, else 16.
 static int choose_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
   if (small_call(batch, num_kv_heads, max_blocks)) return kSmallChunkTiles;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return kChunkTiles;
-  const long long ctas = (long long)batch * num_kv_heads * ((max_blocks + 31) / 32);
-  return ctas >= 6LL * sms ? 32 : kChunkTiles;
+  const long long units = (long long)batch * num_kv_heads;
+  for (int chunk : {64, 32})
+    if (units * ((max_blocks + chunk - 1) / chunk) >= 6LL * sms) return chunk;
+  return kChunkTiles;
 }
 constexpr int kF16ChunkTiles = 16;
 
