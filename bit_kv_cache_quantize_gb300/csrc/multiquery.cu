@@ -18,19 +18,22 @@
 //     B = K~ with K~[t][c] = gK_c code_tc / 64 (exact in fp16) for the 128
 //     tokens and K~[128][c] = gK_c / 64, so that
 //       score_t = (64 / qs) (aK_t D[t] + bK_t D[128]).
-//   softmax (one thread per row, scores from tensor memory): running
-//     reference m per row, moved only when a tile maximum exceeds it by more
-//     than 8 (log2 units), which rescales the accumulator.
+//   softmax (two threads per row, one per 64-token half, scores from tensor
+//     memory; the halves exchange their maxima through shared memory):
+//     running reference m per row, moved only when a tile maximum exceeds it
+//     by more than 8 (log2 units), which rescales the accumulator.
 //   PV (tcgen05, bf16, M = 128 rows, N = 128 channels, K = 144):
 //     A = P~ with P~[t] = p_t aV_t (bf16 hi and lo, two passes) and
 //     P~[128], P~[129] = hi and lo of beta = sum_t p_t bV_t; B = V~ with
 //     V~[c][t] = gV_c codeV_tc and V~[c][128] = V~[c][129] = gV_c (exact in
 //     bf16), so the accumulator collects sum_t p_t gV_c (aV_t code + bV_t).
 //
-// Warp roles per CTA (one CTA per SM): warps 0-3 own one row each thread
-// (softmax), warps 4-7 unpack records into the K~ / V~ operands, warp 8
-// issues the bulk copies and the MMAs.  Operands that a later tile reuses
-// are double-buffered (K~, scales) or guarded by the previous PV (V~, P~).
+// Warp roles per CTA (13 warps, one CTA per SM): warps 0-7 run the softmax
+// (warp w: rows 32 (w & 3) .. + 31, token half w >> 2), warps 8-11 unpack
+// records into the K~ / V~ operands (their first thread refills a record
+// stage once all of them are done with it), one thread of warp 12 issues
+// the first bulk copies and the MMAs.  Operands that a later tile reuses are
+// double-buffered (K~, scores, scales) or guarded by the previous PV (V~).
 #include "common.cuh"
 #include "tcgen05.cuh"
 
