@@ -268,13 +268,7 @@ def run_gpu(args, rank, world):
         "warmup": warm, "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "strong" if mode == "heads" else "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "ragged_32b_serving: 256 seqs, context U[128,32768] (never a multiple of 128), "
-                               "Qwen3-32B layer 64 q / 8 KV heads, head_dim 128, fp16 inputs, K4/V2 "
-                               "128-token tiles, 8 Sinkhorn iterations; step = append 1 token/seq "
-                               "(close+quantise full tiles) + decode attention",
-                   "batch": B_, "mean_context": statistics.mean(w.seq_lens),
-                   "decode_steps_appended": n_dec, "l2": "inputs larger than L2 (packed cache ~3.5 GB)",
-                   "parallelism": parallelism},
+        "config": serving_config(B_, statistics.mean(w.seq_lens), n_dec, parallelism),
         "roofline": {"kernel": "kvarn_decode_attention (split-K decode + combine)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "peak_source": peak_src, "traffic": DECODE_TRAFFIC_PER_BYTE * dec_bytes,
@@ -613,6 +607,17 @@ def cpu_baseline(n_seqs=4, reps=1, quant_seqs=4):
                                f"({qjobs} tile jobs) in {qdt:.2f} s on {threads} threads"}
 
 
+def serving_config(batch, mean_context, n_dec, parallelism):
+    """The `config` object of the serving-step line (both arms)."""
+    return {"workload": "ragged_32b_serving: 256 seqs, context U[128,32768] (never a multiple of 128), "
+                        "Qwen3-32B layer 64 q / 8 KV heads, head_dim 128, fp16 inputs, K4/V2 "
+                        "128-token tiles, 8 Sinkhorn iterations; step = append 1 token/seq "
+                        "(close+quantise full tiles) + decode attention",
+            "batch": batch, "mean_context": mean_context,
+            "decode_steps_appended": n_dec, "l2": "inputs larger than L2 (packed cache ~3.5 GB)",
+            "parallelism": parallelism}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -629,8 +634,13 @@ def run_reference(args, rank, world):
               f"CPU oracle (fp64 folded attention) on {threads} threads")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "ragged_32b_serving (bounded sample, see cpu_baseline.sample)"},
+            "higher_is_better": True, "scaling": "strong" if world > 1 and args.shard == "heads" else "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": serving_config(len(w.seq_lens), statistics.mean(w.seq_lens), max(64, args.steps + args.warmup),
+                                     "single GPU" if world == 1 else
+                                     f"replicas x{world}" if args.shard == "replicas" else
+                                     f"KV heads split {world} ways ({8 // world} KV / {64 // world} q heads per rank), "
+                                     "no collective"),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
