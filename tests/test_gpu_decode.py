@@ -145,6 +145,17 @@ def test_v4_ragged_tails_and_empty_sequence():
     run_decode_case(w)
 
 
+def test_64_tile_chunks_ragged():
+    """120 ragged sequences of up to 8191 tokens (64 blocks), 64 q / 8 KV
+    heads: 120 x 8 (sequence, head) pairs give at least three waves of CTAs
+    with one 64-tile chunk each, so the call takes 64-tile chunks (partial
+    ones for every sequence), beside an empty sequence, a one-token one, one
+    of exactly 63 closed tiles and one ending one token short of 64."""
+    lens = I.ragged_lengths(31, 116, lo=1, hi=8150) + [0, 1, 63 * T, 64 * T - 1]
+    w = I.Workload("ragged_chunk64", len(lens), 64, 8, "f16", lens, seed=33, max_tokens=64 * T, block_perm=True)
+    run_decode_case(w)
+
+
 def test_group_sizes_bf16():
     for hq, hkv in ((2, 2), (4, 2), (6, 3)):
         w = I.Workload(f"g{hq // hkv}", 3, hq, hkv, "bf16", [300, 128, 77], seed=30 + hq, max_tokens=300,
