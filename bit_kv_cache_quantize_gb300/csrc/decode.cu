@@ -63,24 +63,32 @@ __device__ __forceinline__ float to_f(E x) {
 // one V-record buffer -- the next tile's K record streams in while this
 // tile's V record is in use and vice versa -- the query operand fragments,
 // and the cross-warp merge area (aliases the K buffers at the end).
-constexpr int DEC_WARPS = 8;
+// Warps per CTA: 8 (two CTAs per SM at 128 registers); the K4/V4 preset,
+// whose 17 KB records leave room for fewer buffers, runs CTAs of 4 warps at
+// the registers two such CTAs per SM may have (measured 10 % faster on the
+// 16K decode than one 8-warp CTA per SM).
+template <int KBITS, int VBITS>
+constexpr int dec_warps() { return (KBITS == 4 && VBITS == 4) ? 4 : 8; }
 constexpr int PV_ILP = 4;  // independent MMA chains interleaved in PV
 template <int KBITS, int VBITS>
 struct DecSmem {
-  alignas(128) unsigned char krec[DEC_WARPS][rec_bytes(KBITS)];
-  alignas(128) unsigned char vrec[DEC_WARPS][rec_bytes(VBITS)];
+  static constexpr int NW = dec_warps<KBITS, VBITS>();
+  alignas(128) unsigned char krec[NW][rec_bytes(KBITS)];
+  alignas(128) unsigned char vrec[NW][rec_bytes(VBITS)];
   alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order (hi, lo, hi/16, lo/16)
   alignas(16) float qr[8][D];   // rotated, scaled queries (set-up only)
   float qsi[8];                 // per query: inverse of its power-of-two operand scale
-  uint64_t kbar[DEC_WARPS];
-  uint64_t vbar[DEC_WARPS];
+  uint64_t kbar[NW];
+  uint64_t vbar[NW];
 };
+template <int NW>
 struct DecMerge {
-  float m[DEC_WARPS][8];
-  float l[DEC_WARPS][8];
-  float acc[DEC_WARPS][8][D];
+  float m[NW][8];
+  float l[NW][8];
+  float acc[NW][8][D];
 };
-static_assert(sizeof(DecMerge) <= sizeof(DecSmem<2, 2>::krec), "merge area must fit");
+static_assert(sizeof(DecMerge<8>) <= sizeof(DecSmem<2, 2>::krec), "merge area must fit");
+static_assert(sizeof(DecMerge<4>) <= sizeof(DecSmem<4, 4>::krec), "merge area must fit");
 static_assert(K_REC % 128 == 0 && K2_REC % 128 == 0 && V_REC % 128 == 0 && V4_REC % 128 == 0,
               "record buffers stay 128-byte aligned");
 
@@ -138,7 +146,7 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
   return __half2(h);
 }
 
-// grid (n_chunks + 1, H_kv, B) x 256 threads; chunk n_chunks handles the
+// grid (n_chunks + 1, H_kv, B) x 32 NW threads; chunk n_chunks handles the
 // raw open tile.  Warp w of a chunk takes its tiles first + w, first + w + 8.
 //
 // Per tile and warp, with lane = 4 g + j:
@@ -154,12 +162,12 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 //     B = 2-bit codes of channel 8 nbp + g, whose 32-bit words keep even
 //     tokens in the low half and odd tokens in the high half, so each B
 //     register is one masked field of one word.
-// Two CTAs per SM at 128 registers a thread, except for the K4/V4 preset,
-// whose record buffers leave room for one CTA: that instance takes the
-// registers one CTA may have (no spills).
+// Two CTAs per SM; 8 warps at 128 registers a thread, or for the K4/V4
+// preset 4 warps at the registers two 4-warp CTAs may have (no spills).
 template <typename E, int KBITS, int VBITS>
-__global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decode_packed_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(32 * dec_warps<KBITS, VBITS>(), 2) decode_packed_kernel(DecodeParams p) {
   using KL = KeyLayout<KBITS>;
+  constexpr int NW = dec_warps<KBITS, VBITS>();
   constexpr int KREC = rec_bytes(KBITS), KROW = D * KBITS / 8;  // KROW: code bytes per token
   constexpr int VREC = rec_bytes(VBITS);
   static_assert(KROW == 16 * KBITS, "token row");
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
   DecSmem<KBITS, VBITS>& sm = *reinterpret_cast<DecSmem<KBITS, VBITS>*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
-  const int my_n = (n_tiles > warp) ? (n_tiles - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
+  const int my_n = (n_tiles > warp) ? (n_tiles - warp + NW - 1) / NW : 0;
   const int polls = p.wait_polls > 0 ? p.wait_polls : kWaitPolls;
 
   // start this warp's first tile before anything else
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
   auto issue = [&](int k, bool is_v) {  // lane 0: copy the K or V record of this warp's k-th tile
     if (p.skip_first_copy && k == 0 && !is_v && warp == 0 && chunk == 0 && h == 0 && b == 0)
       return;  // error-path test: this copy never starts, so its wait must expire
-    const int32_t blk = tab[first + warp + k * DEC_WARPS];
+    const int32_t blk = tab[first + warp + k * NW];
     uint64_t* bar = is_v ? &sm.vbar[warp] : &sm.kbar[warp];
     const unsigned char* src = p.pool + blk * p.block_bytes + (int64_t)h * head_rec(KBITS, VBITS) + (is_v ? KREC : 0);
     const uint32_t bytes = is_v ? VREC : KREC;
@@ -210,16 +218,18 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
   };
   if (lane == 0 && my_n > 0) { issue(0, false); issue(0, true); }
 
-  // rotated, scaled queries: warp w < G rotates query w with a 128-point
-  // butterfly over 4 channels per lane; qr = qs * scale * log2(e) * (q H),
-  // qs a power of two putting max |qr| in [64, 128), so |qr gK| <= 128 * 448
-  // stays inside fp16
-  {
+  // rotated, scaled queries: warp w rotates queries w, w + NW, ... (rows past
+  // G stay zero) with a 128-point butterfly over 4 channels per lane;
+  // qr = qs * scale * log2(e) * (q H), qs a power of two putting max |qr| in
+  // [64, 128), so |qr gK| <= 128 * 448 stays inside fp16
+#pragma unroll
+  for (int it = 0; it < 8 / NW; ++it) {
+    const int qq = warp + NW * it;
     const E* qb = static_cast<const E*>(p.q) + ((int64_t)b * p.num_q_heads + (int64_t)h * G) * D;
     float x[4] = {0.f, 0.f, 0.f, 0.f};
-    if (warp < G) {
+    if (qq < G) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = to_f(qb[warp * D + 4 * lane + e]);
+      for (int e = 0; e < 4; ++e) x[e] = to_f(qb[qq * D + 4 * lane + e]);
     }
     float u = x[0], v = x[1];
     x[0] = u + v; x[1] = u - v;
@@ -250,12 +260,14 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
     int ex = 0;
     if (amax > 0.f) frexpf(amax, &ex);
     const float qs = ldexpf(1.f, 7 - ex);
-    *reinterpret_cast<float4*>(&sm.qr[warp][4 * lane]) = make_float4(x[0] * qs, x[1] * qs, x[2] * qs, x[3] * qs);
-    if (lane == 0) sm.qsi[warp] = ldexpf(1.f, ex - 7);
+    *reinterpret_cast<float4*>(&sm.qr[qq][4 * lane]) = make_float4(x[0] * qs, x[1] * qs, x[2] * qs, x[3] * qs);
+    if (lane == 0) sm.qsi[qq] = ldexpf(1.f, ex - 7);
   }
   __syncthreads();
-  {  // thread (kb = warp, lane) forms the fp16 high/low query pairs of its A-fragment slot
-    const int kb = warp, ca = 32 * j + KL::ch_a(kb), cb = 32 * j + KL::ch_b(kb);
+#pragma unroll
+  for (int it = 0; it < 8 / NW; ++it) {  // thread (kb, lane) forms the fp16 high/low query pairs of its A-fragment slot
+    const int kb = warp + NW * it;
+    const int ca = 32 * j + KL::ch_a(kb), cb = 32 * j + KL::ch_b(kb);
     const float* q = sm.qr[g];
     const float sa = KL::scale_a(kb), sb = KL::scale_b(kb);
     const float v0 = q[ca] * sa, v1 = q[ca + KL::PAIR] * sa, v2 = q[cb] * sb, v3 = q[cb + KL::PAIR] * sb;
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
   for (int nb = 0; nb < 16; ++nb) acc[nb] = make_float2(0.f, 0.f);
 
   for (int k = 0; k < my_n; ++k) {
-    const int32_t blk = tab[first + warp + k * DEC_WARPS];
+    const int32_t blk = tab[first + warp + k * NW];
     const bool valid = blk >= 0 && blk < p.num_blocks;
     const unsigned char* kr = sm.krec[warp];
     const unsigned char* vr = sm.vrec[warp];
@@ -474,20 +486,20 @@ __global__ void __launch_bounds__(256, (KBITS == 4 && VBITS == 4) ? 1 : 2) decod
 
   // ---- merge the warps and write this CTA's partial
   __syncthreads();
-  DecMerge& mg = *reinterpret_cast<DecMerge*>(sm.krec);
+  DecMerge<NW>& mg = *reinterpret_cast<DecMerge<NW>*>(sm.krec);
   if (j == 0) { mg.m[warp][g] = m_run; mg.l[warp][g] = l_run; }
 #pragma unroll
   for (int nb = 0; nb < 16; ++nb) *reinterpret_cast<float2*>(&mg.acc[warp][g][8 * nb + 2 * j]) = acc[nb];
   __syncthreads();
-  for (int i = tid; i < G * D; i += 256) {
+  for (int i = tid; i < G * D; i += 32 * NW) {
     const int gg = i / D, c = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, mg.m[w][gg]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mg.m[w][gg]);
     float Lsum = 0.f, A = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < DEC_WARPS; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float f = exp2f(mg.m[w][gg] - M);
         Lsum += f * mg.l[w][gg];
         A += f * mg.acc[w][gg][c];
@@ -830,7 +842,8 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = smem_attr_once(attr_done, (const void*)decode_packed_kernel<E, KBITS, VBITS>, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_packed_kernel<E, KBITS, VBITS><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 256, smem, s>>>(p);
+  decode_packed_kernel<E, KBITS, VBITS>
+      <<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 32 * dec_warps<KBITS, VBITS>(), smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;

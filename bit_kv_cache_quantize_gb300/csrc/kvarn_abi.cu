@@ -31,7 +31,8 @@ static int min_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
 // Packed tiles per split-K CTA for one call: 8 for a small call; else the
 // longest of 64 and 32 (longer CTAs amortise the per-CTA query set-up and
 // merge) that still gives at least three waves of CTAs at two per SM, else 16.
-static int choose_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
+// The K4/V4 preset, whose CTAs have 4 warps, stops at 32 (8 tiles a warp).
+static int choose_chunk_tiles(const kvarn_config* cfg, int batch, int num_kv_heads, int max_blocks) {
   if (small_call(batch, num_kv_heads, max_blocks)) return kSmallChunkTiles;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -39,7 +40,7 @@ static int choose_chunk_tiles(int batch, int num_kv_heads, int max_blocks) {
     return kChunkTiles;
   const long long units = (long long)batch * num_kv_heads;
   for (int chunk : {64, 32})
-    if (units * ((max_blocks + chunk - 1) / chunk) >= 6LL * sms) return chunk;
+    if ((chunk == 32 || cfg->v_bits != 4) && units * ((max_blocks + chunk - 1) / chunk) >= 6LL * sms) return chunk;
   return kChunkTiles;
 }
 constexpr int kF16ChunkTiles = 16;
@@ -177,7 +178,7 @@ static kvarn_status decode_call(const kvarn_config* cfg, const void* q, const in
                                  workspace_bytes);
   if (st != KVARN_OK || batch == 0) return st;
   if (!tail_pool || !aligned16(tail_pool)) return KVARN_ERR_INVALID;
-  const int chunk = choose_chunk_tiles(batch, cfg->num_kv_heads, max_blocks);
+  const int chunk = choose_chunk_tiles(cfg, batch, cfg->num_kv_heads, max_blocks);
   const int n_chunks = (max_blocks + chunk - 1) / chunk;
   DecodeParams p{q, block_table, seq_lens, static_cast<const unsigned char*>(block_pool), tail_pool,
                  static_cast<float*>(workspace), dev_err, static_cast<int64_t>(kvarn_block_bytes(cfg)), softmax_scale,
@@ -264,7 +265,7 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
   if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles) > KVARN_NOALLOC_SCRATCH_BYTES)
     return KVARN_ERR_UNSUPPORTED;  // larger than the fixed scratch: use kvarn_decode_attention
-  int chunk = choose_chunk_tiles(batch, cfg->num_kv_heads, max_blocks);
+  int chunk = choose_chunk_tiles(cfg, batch, cfg->num_kv_heads, max_blocks);
   if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, chunk) > KVARN_NOALLOC_SCRATCH_BYTES)
     chunk = kChunkTiles;  // a small call's finer split does not fit: the ordinary split does
   const int n_chunks = (max_blocks + chunk - 1) / chunk;
