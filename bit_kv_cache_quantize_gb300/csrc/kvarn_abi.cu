@@ -101,7 +101,7 @@ kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const 
   if (st != KVARN_OK) return st;
   if (n_tiles < 0 || n_tokens < 0) return KVARN_ERR_INVALID;
   if (n_tiles == 0) return KVARN_OK;
-  if (!k || !v || !tile_first_token || !tile_dst_block || !block_pool) return KVARN_ERR_INVALID;
+  if (!k || !v || !tile_first_token || !tile_dst_block || (!block_pool && cfg->num_blocks > 0)) return KVARN_ERR_INVALID;
   if (!aligned16(k) || !aligned16(v) || !aligned16(block_pool)) return KVARN_ERR_INVALID;
   if (token_stride_elems % 8 || token_stride_elems < static_cast<int64_t>(cfg->num_kv_heads) * 128)
     return KVARN_ERR_INVALID;
@@ -147,7 +147,7 @@ kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, con
   if (batch < 0 || max_blocks < 1) return KVARN_ERR_INVALID;
   if (batch == 0) return KVARN_OK;
   if (batch > 0x7fffffff / 1 || cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
-  if (!k_new || !v_new || !pos || !block_table || !tail_pool || !block_pool) return KVARN_ERR_INVALID;
+  if (!k_new || !v_new || !pos || !block_table || !tail_pool || (!block_pool && cfg->num_blocks > 0)) return KVARN_ERR_INVALID;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(tail_pool) || !aligned16(block_pool))
     return KVARN_ERR_INVALID;
   AppendParams p{k_new, v_new, pos, block_table, max_blocks, cfg->num_kv_heads, cfg->num_blocks, cfg->sinkhorn_iters,
@@ -163,7 +163,7 @@ static kvarn_status check_decode(const kvarn_config* cfg, const void* q, const i
   if (st != KVARN_OK) return st;
   if (batch < 0 || max_blocks < 1 || batch > 65535) return KVARN_ERR_INVALID;
   if (batch == 0) return KVARN_OK;
-  if (!q || !block_table || !seq_lens || !pool || !out || !workspace) return KVARN_ERR_INVALID;
+  if (!q || !block_table || !seq_lens || (!pool && cfg->num_blocks > 0) || !out || !workspace) return KVARN_ERR_INVALID;
   if (!aligned16(q) || !aligned16(pool) || !aligned16(out) || !aligned16(workspace)) return KVARN_ERR_INVALID;
   if (workspace_bytes < kvarn_decode_workspace_bytes(cfg, batch, max_blocks)) return KVARN_ERR_INVALID;
   return KVARN_OK;
@@ -237,7 +237,8 @@ kvarn_status kvarn_multiquery_attention(const kvarn_config* cfg, const void* q, 
   if (st != KVARN_OK) return st;
   if (batch < 0 || max_blocks < 1 || batch > 65535 || n_queries < 1 || n_queries > 4096) return KVARN_ERR_INVALID;
   if (batch == 0) return KVARN_OK;
-  if (!q || !block_table || !seq_lens || !block_pool || !tail_pool || !out || !workspace) return KVARN_ERR_INVALID;
+  if (!q || !block_table || !seq_lens || (!block_pool && cfg->num_blocks > 0) || !tail_pool || !out || !workspace)
+    return KVARN_ERR_INVALID;
   if (!aligned16(q) || !aligned16(block_pool) || !aligned16(tail_pool) || !aligned16(out) || !aligned16(workspace))
     return KVARN_ERR_INVALID;
   if (workspace_bytes < kvarn_multiquery_workspace_bytes(cfg, batch, max_blocks, n_queries)) return KVARN_ERR_INVALID;
@@ -260,7 +261,7 @@ kvarn_status kvarn_decode_attention_noalloc(const kvarn_config* cfg, const void*
   if (st != KVARN_OK) return st;
   if (batch < 0 || max_blocks < 1 || batch > 65535) return KVARN_ERR_INVALID;
   if (batch == 0) return KVARN_OK;
-  if (!q || !block_table || !seq_lens || !block_pool || !tail_pool || !out) return KVARN_ERR_INVALID;
+  if (!q || !block_table || !seq_lens || (!block_pool && cfg->num_blocks > 0) || !tail_pool || !out) return KVARN_ERR_INVALID;
   if (!aligned16(q) || !aligned16(block_pool) || !aligned16(tail_pool) || !aligned16(out)) return KVARN_ERR_INVALID;
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
   if (decode_ws_bytes(batch, cfg->num_kv_heads, G, max_blocks, kChunkTiles) > KVARN_NOALLOC_SCRATCH_BYTES)
@@ -300,7 +301,8 @@ kvarn_status kvarn_dequantize(const kvarn_config* cfg, const void* block_pool, c
   if (st != KVARN_OK) return st;
   if (n < 0) return KVARN_ERR_INVALID;
   if (n == 0) return KVARN_OK;
-  if (!block_pool || !blocks || !out || !aligned16(block_pool) || !aligned16(out)) return KVARN_ERR_INVALID;
+  if ((!block_pool && cfg->num_blocks > 0) || !blocks || !out || !aligned16(block_pool) || !aligned16(out))
+    return KVARN_ERR_INVALID;
   if (cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
   return cuda_status(launch_dequantize(static_cast<const unsigned char*>(block_pool),
                                        static_cast<int64_t>(kvarn_block_bytes(cfg)), blocks, n, cfg->num_blocks,

@@ -104,7 +104,8 @@ typedef struct kvarn_config {
   int32_t tile_tokens;    /* tokens per tile = paged block size; must be 128 */
   int32_t num_kv_heads;   /* KV heads of the layer, >= 1 */
   int32_t num_q_heads;    /* query heads; a multiple of num_kv_heads with group size <= 8 */
-  int32_t num_blocks;     /* blocks in the packed block pool (device bounds check) */
+  int32_t num_blocks;     /* blocks in the packed block pool (device bounds check); with 0 blocks
+                             the pool pointer may be NULL */
   int32_t k_bits;         /* key code width; 4 or 2 */
   int32_t v_bits;         /* value code width; 2, or 4 with k_bits = 4 */
   int32_t sinkhorn_iters; /* normalisation iterations, 0..64 (the preset uses 8) */
@@ -183,6 +184,8 @@ size_t kvarn_decode_workspace_bytes(const kvarn_config* cfg, int32_t batch, int3
  * the output.
  *
  *  q           device, 16-bit (cfg->dtype) [batch][num_q_heads][128].
+ *  block_table device int32[batch][max_blocks], max_blocks >= 1 (a batch
+ *              without a closed tile still passes one column).
  *  seq_lens    device int32[batch]; 0 gives a zero output row; must satisfy
  *              seq_lens[s] <= 128 * max_blocks.
  *  out         device float32 [batch][num_q_heads][128].
