@@ -10,6 +10,7 @@ import pytest
 
 from bit_kv_cache_quantize_gb300 import inputs as I
 
+from test_gpu_append import run_steps
 from test_gpu_decode import run_decode_case
 from test_gpu_multiquery import run_mq_case
 from test_gpu_quantize import quantize_and_compare
@@ -49,3 +50,19 @@ def test_random_case(i):
     q_tokens = int(rng.integers(1, 21))
     wm, _ = random_workload(i, min_len=q_tokens)
     run_mq_case(wm, q_tokens)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_append_steps(i):
+    """Random decode steps: append one token per sequence (closing tiles on
+    the way), attend after every step; every closed tile and every step's
+    attention against the oracle."""
+    w, rng = random_workload(100 + i)
+    steps = int(rng.integers(2, 6))
+    # start some sequences a few tokens short of a tile edge so that tiles close during the run
+    w.seq_lens = [n - (n % T) + T - int(rng.integers(1, steps + 1)) if rng.random() < 0.5 else n for n in w.seq_lens]
+    w.decode_steps = steps
+    w.max_tokens = max(w.seq_lens) + steps
+    print(f"{w.name}: B={w.batch} H_kv={w.num_kv_heads} G={w.G} {w.dtype} K{w.k_bits}/V{w.v_bits} "
+          f"lens={w.seq_lens} steps={steps}")
+    run_steps(w, steps)
