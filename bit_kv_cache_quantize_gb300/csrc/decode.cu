@@ -63,16 +63,15 @@ __device__ __forceinline__ float to_f(E x) {
 // one V-record buffer -- the next tile's K record streams in while this
 // tile's V record is in use and vice versa -- the query operand fragments,
 // and the cross-warp merge area (aliases the K buffers at the end).
-// Warps per CTA: 8 (two CTAs per SM at 128 registers); the K4/V4 preset,
-// whose 17 KB records leave room for fewer buffers, runs CTAs of 4 warps at
-// the registers two such CTAs per SM may have (measured 10 % faster on the
-// 16K decode than one 8-warp CTA per SM).
-template <int KBITS, int VBITS>
-constexpr int dec_warps() { return (KBITS == 4 && VBITS == 4) ? 4 : 8; }
+// Warps per CTA (NW): 8, two CTAs per SM at 128 registers; or 4, two CTAs
+// per SM at the registers such CTAs may have (no spills).  The K4/V4 preset,
+// whose 17 KB records leave room for fewer buffers, always takes 4 (measured
+// 10 % faster on the 16K decode than one 8-warp CTA per SM); the others take
+// 4 for small calls (8-tile chunks, 7 % faster on the Qwen3-4B layer) and 8
+// otherwise.
 constexpr int PV_ILP = 4;  // independent MMA chains interleaved in PV
-template <int KBITS, int VBITS>
+template <int KBITS, int VBITS, int NW>
 struct DecSmem {
-  static constexpr int NW = dec_warps<KBITS, VBITS>();
   alignas(128) unsigned char krec[NW][rec_bytes(KBITS)];
   alignas(128) unsigned char vrec[NW][rec_bytes(VBITS)];
   alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order (hi, lo, hi/16, lo/16)
@@ -87,8 +86,8 @@ struct DecMerge {
   float l[NW][8];
   float acc[NW][8][D];
 };
-static_assert(sizeof(DecMerge<8>) <= sizeof(DecSmem<2, 2>::krec), "merge area must fit");
-static_assert(sizeof(DecMerge<4>) <= sizeof(DecSmem<4, 4>::krec), "merge area must fit");
+static_assert(sizeof(DecMerge<8>) <= sizeof(DecSmem<2, 2, 8>::krec), "merge area must fit");
+static_assert(sizeof(DecMerge<4>) <= sizeof(DecSmem<2, 2, 4>::krec), "merge area must fit");
 static_assert(K_REC % 128 == 0 && K2_REC % 128 == 0 && V_REC % 128 == 0 && V4_REC % 128 == 0,
               "record buffers stay 128-byte aligned");
 
@@ -164,10 +163,9 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 //     register is one masked field of one word.
 // Two CTAs per SM; 8 warps at 128 registers a thread, or for the K4/V4
 // preset 4 warps at the registers two 4-warp CTAs may have (no spills).
-template <typename E, int KBITS, int VBITS>
-__global__ void __launch_bounds__(32 * dec_warps<KBITS, VBITS>(), 2) decode_packed_kernel(DecodeParams p) {
+template <typename E, int KBITS, int VBITS, int NW>
+__global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams p) {
   using KL = KeyLayout<KBITS>;
-  constexpr int NW = dec_warps<KBITS, VBITS>();
   constexpr int KREC = rec_bytes(KBITS), KROW = D * KBITS / 8;  // KROW: code bytes per token
   constexpr int VREC = rec_bytes(VBITS);
   static_assert(KROW == 16 * KBITS, "token row");
@@ -188,7 +186,8 @@ __global__ void __launch_bounds__(32 * dec_warps<KBITS, VBITS>(), 2) decode_pack
   const int n_tiles = min(p.chunk_tiles, n_closed - first);
   if (n_tiles <= 0) return;
   const uint32_t sbase = smem_u32(smem_raw);
-  DecSmem<KBITS, VBITS>& sm = *reinterpret_cast<DecSmem<KBITS, VBITS>*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
+  DecSmem<KBITS, VBITS, NW>& sm =
+      *reinterpret_cast<DecSmem<KBITS, VBITS, NW>*>(smem_raw + (((sbase + 127u) & ~127u) - sbase));
   const int G = p.G;
   const int32_t* tab = p.block_table + (int64_t)b * p.max_blocks;
   const int my_n = (n_tiles > warp) ? (n_tiles - warp + NW - 1) / NW : 0;
@@ -836,14 +835,13 @@ size_t decode_ws_bytes(int batch, int num_kv_heads, int G, int max_blocks, int c
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode();
 
-template <typename E, int KBITS, int VBITS>
+template <typename E, int KBITS, int VBITS, int NW>
 static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaStream_t s) {
-  const size_t smem = sizeof(DecSmem<KBITS, VBITS>) + 128;
+  const size_t smem = sizeof(DecSmem<KBITS, VBITS, NW>) + 128;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = smem_attr_once(attr_done, (const void*)decode_packed_kernel<E, KBITS, VBITS>, (int)smem);
+  cudaError_t e = smem_attr_once(attr_done, (const void*)decode_packed_kernel<E, KBITS, VBITS, NW>, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_packed_kernel<E, KBITS, VBITS>
-      <<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 32 * dec_warps<KBITS, VBITS>(), smem, s>>>(p);
+  decode_packed_kernel<E, KBITS, VBITS, NW><<<dim3(p.n_chunks + 1, p.num_kv_heads, batch), 32 * NW, smem, s>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
@@ -851,13 +849,23 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
   return cudaGetLastError();
 }
 
+template <typename E, int KBITS, int VBITS>
+static cudaError_t launch_decode_w(const DecodeParams& p, int batch, float* out, cudaStream_t s) {
+  if constexpr (KBITS == 4 && VBITS == 4) {
+    return launch_decode_t<E, KBITS, VBITS, 4>(p, batch, out, s);
+  } else {  // a small call's 8-tile chunks take the 4-warp CTAs too
+    return p.chunk_tiles <= 8 ? launch_decode_t<E, KBITS, VBITS, 4>(p, batch, out, s)
+                              : launch_decode_t<E, KBITS, VBITS, 8>(p, batch, out, s);
+  }
+}
+
 cudaError_t launch_decode(const DecodeParams& p, int dtype, int batch, float* out, cudaStream_t s) {
   const bool bf = dtype == KVARN_DTYPE_BF16;
   if (p.v_bits == 4)  // the K4/V4 preset
-    return bf ? launch_decode_t<__nv_bfloat16, 4, 4>(p, batch, out, s) : launch_decode_t<__half, 4, 4>(p, batch, out, s);
+    return bf ? launch_decode_w<__nv_bfloat16, 4, 4>(p, batch, out, s) : launch_decode_w<__half, 4, 4>(p, batch, out, s);
   if (p.k_bits == 2)
-    return bf ? launch_decode_t<__nv_bfloat16, 2, 2>(p, batch, out, s) : launch_decode_t<__half, 2, 2>(p, batch, out, s);
-  return bf ? launch_decode_t<__nv_bfloat16, 4, 2>(p, batch, out, s) : launch_decode_t<__half, 4, 2>(p, batch, out, s);
+    return bf ? launch_decode_w<__nv_bfloat16, 2, 2>(p, batch, out, s) : launch_decode_w<__half, 2, 2>(p, batch, out, s);
+  return bf ? launch_decode_w<__nv_bfloat16, 4, 2>(p, batch, out, s) : launch_decode_w<__half, 4, 2>(p, batch, out, s);
 }
 
 // ---- fixed-scratch variant of the packed decode (no allocation anywhere)
