@@ -146,7 +146,7 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 }
 
 // grid (n_chunks + 1, H_kv, B) x 32 NW threads; chunk n_chunks handles the
-// raw open tile.  Warp w of a chunk takes its tiles first + w, first + w + 8.
+// raw open tile.  Warp w of a chunk takes its tiles first + w, first + w + NW, ....
 //
 // Per tile and warp, with lane = 4 g + j:
 //   QK (m16n8k16, M = 8 queries hi | lo, N = 8 tokens, K = 16 channels):
@@ -161,8 +161,8 @@ __device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two) {
 //     B = 2-bit codes of channel 8 nbp + g, whose 32-bit words keep even
 //     tokens in the low half and odd tokens in the high half, so each B
 //     register is one masked field of one word.
-// Two CTAs per SM; 8 warps at 128 registers a thread, or for the K4/V4
-// preset 4 warps at the registers two 4-warp CTAs may have (no spills).
+// Two CTAs per SM: 8 warps at 128 registers a thread, or 4 warps at the
+// registers two 4-warp CTAs may have (no spills).
 template <typename E, int KBITS, int VBITS, int NW>
 __global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams p) {
   using KL = KeyLayout<KBITS>;
