@@ -92,6 +92,20 @@ def test_argument_validation_is_host_side(lib):
         K.kvarn_dequantize(cfg, 16, 16, -1, 16, 16, stream=0)
 
 
+def test_null_pool_is_invalid_when_the_pool_has_blocks(lib):
+    """With num_blocks > 0 a NULL pool is an invalid argument, found on the
+    host (every other argument of these calls is valid, so the pool is what
+    stops them; nothing launches).  A pool of 0 blocks may be NULL: the
+    kernels never touch it, since every block id is then out of range."""
+    cfg = K.make_config(8, 64, 10)
+    ws = K.kvarn_decode_workspace_bytes(cfg, 2, 4)
+    assert K.kvarn_decode_attention(cfg, 16, 16, 4, 16, 2, None, 16, 0.1, 16, 16, ws, 16, stream=0,
+                                    check=False) == K.KVARN_ERR_INVALID
+    assert K.kvarn_quantize_tiles(cfg, 16, 16, 1024, 128, 16, 16, 1, None, 16, stream=0,
+                                  check=False) == K.KVARN_ERR_INVALID
+    assert K.kvarn_dequantize(cfg, None, 16, 1, 16, 16, stream=0, check=False) == K.KVARN_ERR_INVALID
+
+
 def test_multiquery_sizes_and_validation(lib):
     cfg = K.make_config(8, 64, 100, "f16")
     # 16 queries x 8 heads = one row block; 2 sequences, 40 blocks -> 16-tile chunks (3 + the open tile)
