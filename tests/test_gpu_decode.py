@@ -277,3 +277,76 @@ def test_decode_device_errors():
     torch.cuda.synchronize()
     assert c.check_error() == K.KVARN_DEV_ERR_TOKEN_RANGE
     assert not out[1].any()
+
+
+@pytest.mark.parametrize("dtype,k_bits,v_bits", [("f16", 4, 2), ("bf16", 4, 2), ("f16", 2, 2), ("bf16", 4, 4)])
+def test_decode_over_degenerate_tiles(dtype, k_bits, v_bits):
+    """Attention over records of degenerate tiles (the quantiser's edge cases:
+    zero, identical tokens, one large or saturating outlier, values at the
+    16-bit range, tiny values, one live channel or token) against the oracle.
+    Sequence i has degenerate value tile i and a degenerate key tile, then a
+    random tile and a 5-token open tail.  Keys at the 16-bit range are left
+    out: their scores reach ~1e6 and the fp32-vs-fp64 comparison would test
+    the conditioning of the softmax, not the kernel.  The max-abs bound is
+    1e-3 scaled by max(1, max |v|) of the sequence, since values at the
+    16-bit range give outputs of that size."""
+    from test_gpu_quantize import degenerate_tiles
+    dev = device()
+    tiles = degenerate_tiles(dtype)[:, 0].reshape(-1, T, D)  # [n, T, D] 16-bit
+    n = tiles.shape[0]
+    k_ok = [i for i in range(n) if i != 4]  # index 4: values at the 16-bit range
+    rng = np.random.default_rng(5)
+    n_tok = 2 * T + 5
+    w = I.Workload(f"degenerate_{dtype}", n, 8, 1, dtype, [n_tok] * n, seed=8, k_bits=k_bits, v_bits=v_bits)
+    c = PagedCache(w, dev)
+    td = I.torch_dtype(dtype)
+    ctx = {}
+    for b in range(n):
+        rk = torch.from_numpy(rng.standard_normal((T + 5, D)).astype(np.float32)).to(td)
+        rv = torch.from_numpy(rng.standard_normal((T + 5, D)).astype(np.float32)).to(td)
+        k = torch.cat([tiles[k_ok[b % len(k_ok)]], rk]).reshape(n_tok, 1, D)
+        v = torch.cat([tiles[b], rv]).reshape(n_tok, 1, D)
+        ctx[b] = (k, v)
+    recs = load_oracle_records(w, c, list(range(n)), ctx)
+    q = I.queries(w, device=dev).cpu()
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    c.decode(q.to(dev), out)
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    want = oracle_outputs(w, list(range(n)), ctx, recs, q)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    worst = 0.0
+    for (b, h), o in want.items():
+        scale = max(1.0, float(ctx[b][1].float().abs().max()))
+        worst = max(worst, np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max() / scale)
+    print(f"{w.name} K{k_bits}/V{v_bits}: max |gpu - oracle| / max(1, max|v|) = {worst:.3e}")
+    assert worst <= TOL
+
+
+def test_shared_prefix_blocks():
+    """Sequences whose block tables share physical blocks (a common prefix
+    kept once, as a paged serving cache does) decode like sequences with
+    private copies: sequences 1 and 2 reuse the first 3 and 5 blocks of
+    sequence 0 and hold the same tokens there."""
+    dev = device()
+    lens = [1000, 700, 1300, 260]
+    w = I.Workload("shared_prefix", len(lens), 32, 4, "bf16", lens, seed=21, block_perm=True)
+    c = PagedCache(w, dev)
+    ctx = {b: [I.kv_sequence(w, "k", b, n, dev).cpu(), I.kv_sequence(w, "v", b, n, dev).cpu()]
+           for b, n in enumerate(lens)}
+    for b, nb in ((1, 3), (2, 5)):
+        for i in range(2):
+            ctx[b][i][:nb * T] = ctx[0][i][:nb * T]
+        c.table[b, :nb] = c.table[0, :nb]
+    recs = load_oracle_records(w, c, list(range(w.batch)), ctx)
+    q = I.queries(w, device=dev).cpu()
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    c.decode(q.to(dev), out)
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    want = oracle_outputs(w, list(range(w.batch)), ctx, recs, q)
+    got = out.cpu().numpy().astype(np.float64)
+    worst = max(np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max() for (b, h), o in want.items())
+    print(f"shared prefix: max |gpu - oracle| = {worst:.3e}")
+    assert worst <= TOL
