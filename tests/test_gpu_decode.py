@@ -279,6 +279,29 @@ def test_decode_device_errors():
     assert not out[1].any()
 
 
+def degenerate_context(dtype, k_bits, v_bits):
+    """One sequence per degenerate tile of the quantiser tests (1 KV head,
+    8 query heads): that tile as values, a degenerate key tile (cycling
+    through all but the one at the 16-bit range), then a random tile and a
+    5-token open tail.  Returns the workload and {b: (k, v)} [n, 1, 128]."""
+    from test_gpu_quantize import degenerate_tiles
+    tiles = degenerate_tiles(dtype)[:, 0].reshape(-1, T, D)  # [n, T, D] 16-bit
+    n = tiles.shape[0]
+    k_ok = [i for i in range(n) if i != 4]  # index 4: values at the 16-bit range
+    rng = np.random.default_rng(5)
+    n_tok = 2 * T + 5
+    w = I.Workload(f"degenerate_{dtype}", n, 8, 1, dtype, [n_tok] * n, seed=8, k_bits=k_bits, v_bits=v_bits)
+    td = I.torch_dtype(dtype)
+    ctx = {}
+    for b in range(n):
+        rk = torch.from_numpy(rng.standard_normal((T + 5, D)).astype(np.float32)).to(td)
+        rv = torch.from_numpy(rng.standard_normal((T + 5, D)).astype(np.float32)).to(td)
+        k = torch.cat([tiles[k_ok[b % len(k_ok)]], rk]).reshape(n_tok, 1, D)
+        v = torch.cat([tiles[b], rv]).reshape(n_tok, 1, D)
+        ctx[b] = (k, v)
+    return w, ctx
+
+
 @pytest.mark.parametrize("dtype,k_bits,v_bits", [("f16", 4, 2), ("bf16", 4, 2), ("f16", 2, 2), ("bf16", 4, 4)])
 def test_decode_over_degenerate_tiles(dtype, k_bits, v_bits):
     """Attention over records of degenerate tiles (the quantiser's edge cases:
@@ -290,23 +313,10 @@ def test_decode_over_degenerate_tiles(dtype, k_bits, v_bits):
     the conditioning of the softmax, not the kernel.  The max-abs bound is
     1e-3 scaled by max(1, max |v|) of the sequence, since values at the
     16-bit range give outputs of that size."""
-    from test_gpu_quantize import degenerate_tiles
     dev = device()
-    tiles = degenerate_tiles(dtype)[:, 0].reshape(-1, T, D)  # [n, T, D] 16-bit
-    n = tiles.shape[0]
-    k_ok = [i for i in range(n) if i != 4]  # index 4: values at the 16-bit range
-    rng = np.random.default_rng(5)
-    n_tok = 2 * T + 5
-    w = I.Workload(f"degenerate_{dtype}", n, 8, 1, dtype, [n_tok] * n, seed=8, k_bits=k_bits, v_bits=v_bits)
+    w, ctx = degenerate_context(dtype, k_bits, v_bits)
+    n = w.batch
     c = PagedCache(w, dev)
-    td = I.torch_dtype(dtype)
-    ctx = {}
-    for b in range(n):
-        rk = torch.from_numpy(rng.standard_normal((T + 5, D)).astype(np.float32)).to(td)
-        rv = torch.from_numpy(rng.standard_normal((T + 5, D)).astype(np.float32)).to(td)
-        k = torch.cat([tiles[k_ok[b % len(k_ok)]], rk]).reshape(n_tok, 1, D)
-        v = torch.cat([tiles[b], rv]).reshape(n_tok, 1, D)
-        ctx[b] = (k, v)
     recs = load_oracle_records(w, c, list(range(n)), ctx)
     q = I.queries(w, device=dev).cpu()
     out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)

@@ -13,7 +13,7 @@ from bit_kv_cache_quantize_gb300 import kvarn as K
 from bit_kv_cache_quantize_gb300.cache import PagedCache
 
 from gpu_helpers import NTHREADS, bits, device
-from test_gpu_decode import load_oracle_records
+from test_gpu_decode import degenerate_context, load_oracle_records
 
 pytestmark = pytest.mark.gpu
 T = D = 128
@@ -141,3 +141,29 @@ def test_device_errors():
     torch.cuda.synchronize()
     assert c.check_error() == K.KVARN_DEV_ERR_BLOCK_RANGE
     assert torch.isfinite(out[2]).all()
+
+
+@pytest.mark.parametrize("dtype,k_bits,v_bits", [("f16", 4, 2), ("bf16", 4, 2), ("f16", 2, 2), ("bf16", 4, 4)])
+def test_multiquery_over_degenerate_tiles(dtype, k_bits, v_bits):
+    """The last 8 tokens of each sequence as causal queries over records of
+    the quantiser's degenerate tiles (the decode test's sequences); the 1e-3
+    bound scaled by max(1, max |v|) of the sequence, as there."""
+    dev = device()
+    w, ctx = degenerate_context(dtype, k_bits, v_bits)
+    Q = 8
+    c = PagedCache(w, dev)
+    recs = load_oracle_records(w, c, list(range(w.batch)), ctx)
+    q = I.multi_queries(w, Q, device=dev).cpu()
+    out = torch.full((w.batch, Q, w.num_q_heads, D), float("nan"), dtype=torch.float32, device=dev)
+    c.multiquery(q.to(dev), Q, out)
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    got = out.cpu().numpy().astype(np.float64)
+    worst = 0.0
+    for (b, h), o in oracle_mq(w, list(range(w.batch)), ctx, recs, q, Q).items():
+        g = got[b, :, h * w.G:(h + 1) * w.G]
+        assert np.isfinite(g).all(), (b, h)
+        scale = max(1.0, float(ctx[b][1].float().abs().max()))
+        worst = max(worst, np.abs(g - o).max() / scale)
+    print(f"{w.name} K{k_bits}/V{v_bits} Q={Q}: max |gpu - oracle| / max(1, max|v|) = {worst:.3e}")
+    assert worst <= TOL
