@@ -31,6 +31,30 @@ __device__ __forceinline__ void set_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch.  A split-K combine is launched with
+// launch_after() so that the GPU may schedule it while the kernel ahead of it
+// in the stream is still running, once every CTA of that kernel has called
+// allow_dependents(); its threads then block in wait_prerequisite() until the
+// kernel ahead has completed and its memory is visible.  For a kernel
+// launched the ordinary way wait_prerequisite() returns at once.
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisite() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+template <typename... Params, typename... Args>
+static cudaError_t launch_after(void (*kernel)(Params...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Bounds check of the checked (debug) build, compiled with KVARN_CHECK: an
 // access of n bytes at p must lie inside [base, base + bytes); otherwise the
 // first error is recorded as KVARN_DEV_ERR_BOUNDS and the caller skips the

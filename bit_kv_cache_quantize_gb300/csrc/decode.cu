@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams 
   constexpr int VREC = rec_bytes(VBITS);
   static_assert(KROW == 16 * KBITS, "token row");
   extern __shared__ __align__(128) unsigned char smem_raw[];
+  allow_dependents();  // the combine may be scheduled once every CTA has started
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, j = lane & 3;
   const int len = p.seq_lens[b];
@@ -574,6 +575,7 @@ __device__ void tail_chunk(const DecodeParams& p, int b, int h, int len, unsigne
 // One warp per (sequence, query head): merge the split-K partials, apply
 // the inverse rotation to the packed-tile part, add the raw part, normalise.
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p, int rotate, int batch, float* __restrict__ out) {
+  wait_prerequisite();  // the split-K kernel's partials
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (wid >= batch * p.num_q_heads) return;
   const int b = wid / p.num_q_heads, hq = wid % p.num_q_heads;
@@ -661,6 +663,7 @@ __device__ __forceinline__ int f16_off(int r, int ch) {
 template <typename E>
 __global__ void __launch_bounds__(256, 1) decode_f16_kernel(const __grid_constant__ CUtensorMap tmap, DecodeParams p) {
   extern __shared__ __align__(1024) unsigned char smem_f16[];
+  allow_dependents();
   // the 128-byte TMA swizzle needs 1024-byte aligned boxes: align explicitly
   const uint32_t base = smem_u32(smem_f16);
   F16Smem& sm = *reinterpret_cast<F16Smem*>(smem_f16 + (((base + 1023u) & ~1023u) - base));
@@ -845,8 +848,7 @@ static cudaError_t launch_decode_t(DecodeParams p, int batch, float* out, cudaSt
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
-  combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, 1, batch, out);
-  return cudaGetLastError();
+  return launch_after(combine_kernel, dim3((warps + 3) / 4), dim3(128), s, p, 1, batch, out);
 }
 
 template <typename E, int KBITS, int VBITS>
@@ -943,8 +945,7 @@ static cudaError_t launch_f16_t(DecodeParams p, const void* pool16, int batch, f
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.num_q_heads;
-  combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, 0, batch, out);
-  return cudaGetLastError();
+  return launch_after(combine_kernel, dim3((warps + 3) / 4), dim3(128), s, p, 0, batch, out);
 }
 
 cudaError_t launch_decode_f16(const DecodeParams& p, const void* pool16, int dtype, int batch, float* out,

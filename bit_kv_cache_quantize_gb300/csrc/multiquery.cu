@@ -391,6 +391,7 @@ __device__ void mq_tail(const MQParams& p, int b, int h, int rb, int len, unsign
 template <typename E, int KBITS, int VBITS>
 __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
+  allow_dependents();  // the combine may be scheduled once every CTA has started
   const int chunk = blockIdx.x, h = blockIdx.y / p.n_rowblocks, rb = blockIdx.y % p.n_rowblocks, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int len = p.seq_lens[b];
@@ -852,6 +853,7 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
 // One warp per output row (sequence, query, query head): merge the split-K
 // partials, rotate the packed part back, add the raw part, normalise.
 __global__ void __launch_bounds__(128) mq_combine_kernel(MQParams p, int batch, float* __restrict__ out) {
+  wait_prerequisite();  // the split-K kernel's partial rows
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int per_seq = p.n_queries * p.num_q_heads;
   if (wid >= batch * per_seq) return;
@@ -926,8 +928,7 @@ cudaError_t launch_mq_t(const MQParams& p, int batch, float* out, cudaStream_t s
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int warps = batch * p.n_queries * p.num_q_heads;
-  mq_combine_kernel<<<(warps + 3) / 4, 128, 0, s>>>(p, batch, out);
-  return cudaGetLastError();
+  return launch_after(mq_combine_kernel, dim3((warps + 3) / 4), dim3(128), s, p, batch, out);
 }
 
 }  // namespace
