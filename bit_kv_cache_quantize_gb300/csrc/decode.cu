@@ -59,6 +59,8 @@ __device__ __forceinline__ float to_f(E x) {
   else return __bfloat162float(x);
 }
 
+constexpr int PV_ILP = 4;  // independent MMA chains interleaved in PV
+
 // Shared memory of one packed-decode CTA: per warp one K-record buffer and
 // one V-record buffer -- the next tile's K record streams in while this
 // tile's V record is in use and vice versa -- the query operand fragments,
@@ -69,12 +71,12 @@ __device__ __forceinline__ float to_f(E x) {
 // 10 % faster on the 16K decode than one 8-warp CTA per SM); the others take
 // 4 for small calls (8-tile chunks, 7 % faster on the Qwen3-4B layer) and 8
 // otherwise.
-constexpr int PV_ILP = 4;  // independent MMA chains interleaved in PV
 template <int KBITS, int VBITS, int NW>
 struct DecSmem {
   alignas(128) unsigned char krec[NW][rec_bytes(KBITS)];
   alignas(128) unsigned char vrec[NW][rec_bytes(VBITS)];
-  alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order (hi, lo, hi/16, lo/16)
+  alignas(16) uint4 qf[8][32];  // [kb][lane]: fp16 query pairs in A-fragment order: hi, lo of the first
+                                // channel pair, hi, lo of the second, each over its field multiplier
   alignas(16) float qr[8][D];   // rotated, scaled queries (set-up only)
   float qsi[8];                 // per query: inverse of its power-of-two operand scale
   uint64_t kbar[NW];
