@@ -360,3 +360,37 @@ def test_shared_prefix_blocks():
     worst = max(np.abs(got[b, h * w.G:(h + 1) * w.G] - o).max() for (b, h), o in want.items())
     print(f"shared prefix: max |gpu - oracle| = {worst:.3e}")
     assert worst <= TOL
+
+
+@pytest.mark.slow
+def test_long_context_128k():
+    """Two sequences of ~128 K tokens (1023 closed tiles and an open tail of
+    91 tokens; 1024 closed tiles): 64 split-K chunks of 16 tiles per KV head
+    plus the open tile, merged by the combine.  Every closed tile holds the
+    oracle's record and all 2 x 64 query heads are compared with the
+    oracle's attention."""
+    dev = device()
+    lens = [131072 - 37, 131072]
+    w = I.Workload("long_128k", 2, 64, 8, "f16", lens, seed=77, max_tokens=max(lens), block_perm=True)
+    c = PagedCache(w, dev)
+    recs, kept = upload_oracle_prefill(w, c, range(w.batch))
+    q = I.queries(w, device=dev)
+    out = torch.empty(w.batch, w.num_q_heads, D, dtype=torch.float32, device=dev)
+    c.decode(q, out)
+    torch.cuda.synchronize()
+    assert c.check_error() == 0
+    qh = q.cpu()
+    units = []
+    for b in range(w.batch):
+        nf = lens[b] // T
+        k, v, first = kept[b]
+        assert first == nf * T
+        for h in range(w.num_kv_heads):
+            units.append((O.decode16(bits(qh[b, h * w.G:(h + 1) * w.G]), w.dtype),
+                          [recs[(b, t, h, 0)] for t in range(nf)], [recs[(b, t, h, 1)] for t in range(nf)],
+                          O.decode16(bits(k[:, h]), w.dtype).reshape(-1, D),
+                          O.decode16(bits(v[:, h]), w.dtype).reshape(-1, D)))
+    want = oracle_decode(w, units, w.scale).reshape(w.batch, w.num_q_heads, D)
+    worst = np.abs(out.cpu().numpy().astype(np.float64) - want).max()
+    print(f"{w.name}: max |gpu - oracle| = {worst:.3e}")
+    assert worst <= TOL
