@@ -120,6 +120,17 @@ def test_qwen3_32b_16k_chunk_sampled():
     run_mq_case(w, 16, seqs=[3, 29], full_gpu_prefill=True)
 
 
+@pytest.mark.slow
+def test_long_context_128k():
+    """16 causal queries at the end of two ~128 K-token sequences (1023
+    closed tiles and a 91-token open tail; 1024 closed tiles): 32 split-K
+    chunks per (KV head, row block) plus the open tile, merged by the
+    combine; all query rows against the oracle."""
+    lens = [131072 - 37, 131072]
+    w = I.Workload("mq_long_128k", 2, 64, 8, "f16", lens, seed=78, max_tokens=max(lens), block_perm=True)
+    run_mq_case(w, 16)
+
+
 def test_device_errors():
     dev = device()
     w = I.Workload("mq_err", 3, 16, 2, "f16", [300, 3, 700], seed=58, max_tokens=700)
