@@ -394,3 +394,12 @@ def test_long_context_128k():
     worst = np.abs(out.cpu().numpy().astype(np.float64) - want).max()
     print(f"{w.name}: max |gpu - oracle| = {worst:.3e}")
     assert worst <= TOL
+
+
+@pytest.mark.parametrize("h_kv,g", [(32, 1), (16, 2)])
+def test_many_kv_heads(h_kv, g):
+    """More KV heads than the workloads above: 32 heads without grouping
+    (multi-head attention) and 16 heads in pairs, ragged lengths."""
+    w = I.Workload(f"kv{h_kv}_g{g}", 3, h_kv * g, h_kv, "bf16", [700, 129, 1500], seed=60 + h_kv, max_tokens=1500,
+                   block_perm=True, v_dist="t4", k_outliers="random")
+    run_decode_case(w)

@@ -178,3 +178,12 @@ def test_multiquery_over_degenerate_tiles(dtype, k_bits, v_bits):
         worst = max(worst, np.abs(g - o).max() / scale)
     print(f"{w.name} K{k_bits}/V{v_bits} Q={Q}: max |gpu - oracle| / max(1, max|v|) = {worst:.3e}")
     assert worst <= TOL
+
+
+@pytest.mark.parametrize("h_kv,g", [(32, 1), (16, 2)])
+def test_many_kv_heads(h_kv, g):
+    """32 KV heads without grouping and 16 in pairs: one row block per KV
+    head holds the 8 query tokens' rows."""
+    w = I.Workload(f"mq_kv{h_kv}_g{g}", 2, h_kv * g, h_kv, "f16", [900, 300], seed=70 + h_kv, max_tokens=900,
+                   block_perm=True)
+    run_mq_case(w, 8)
