@@ -235,3 +235,11 @@ def test_device_errors_skip_units():
                            torch.tensor([0, 1], dtype=torch.int32, device=dev), 2, pool, err)
     torch.cuda.synchronize()
     assert int(err.item()) == K.KVARN_DEV_ERR_TOKEN_RANGE
+
+
+@pytest.mark.parametrize("h_kv,g", [(32, 1), (16, 2)])
+def test_many_kv_heads(h_kv, g):
+    """32 and 16 KV heads: every closed tile of every head record by record."""
+    w = I.Workload(f"q_kv{h_kv}", 2, h_kv * g, h_kv, "bf16", [640, 300], seed=80 + h_kv, max_tokens=640,
+                   v_dist="t4", k_outliers="random")
+    quantize_and_compare(w, list(range(w.batch)))
