@@ -39,7 +39,16 @@ constexpr int OFF_PART = 9216;             // float2 [8 warps][128]: column (mea
 constexpr int OFF_TOK = 17408;             // float2 [128]: (zero-point, 1/step) per token
 constexpr int OFF_ROW = 18432;             // per half-warp row-step slot: 8 x 36 partials, 8 shifts, 8 factors
 constexpr int ROW_SLOT = 304;              // floats per slot
-static_assert(OFF_ROW + 16 * ROW_SLOT * 4 <= 65536 && T * 272 <= 65536, "staging reuse overflows");
+// Value codes staged for the record: channel c, word w at word
+// ((c & 7) * 16 + (c >> 3)) * stride + w, stride 9 (2-bit, 8 words per
+// channel) or 17 (4-bit, 16 words), so that the lanes of a warp, which hold
+// channels 8 apart, store into different banks (the record's own 32- or
+// 64-byte channel rows would put 16 lanes on one bank).
+constexpr int OFF_STG = 40960;
+__host__ __device__ constexpr int stg_stride(int kind_words) { return kind_words + 1; }
+__device__ __forceinline__ int stg_index(int c, int w, int stride) { return ((c & 7) * 16 + (c >> 3)) * stride + w; }
+static_assert(OFF_ROW + 16 * ROW_SLOT * 4 <= OFF_STG && T * 272 <= 65536, "staging reuse overflows");
+static_assert(OFF_STG + 4 * (127 * 17 + 16) <= 65536, "value staging overflows");
 
 // New log factor ln(std) from a population variance and mean over 128
 // values; keeps `old` when the std is at most 1e-6 of the rms (a constant or
@@ -172,7 +181,7 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
     }
   } else if constexpr (KIND == KIND_V4) {
     // the thread's 8 tokens are one 32-bit word per channel: token tok0 + u at
-    // bit 2u (u even) or 14 + 2u (u odd)
+    // bit 2u (u even) or 14 + 2u (u odd); staged, see OFF_STG
     uint32_t word[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) word[k] = 0;
@@ -188,9 +197,9 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
         word[2 * pp + 1] |= (__float_as_uint(q2.y) & 15u) << sh;
       }
     }
+    uint32_t* stg = reinterpret_cast<uint32_t*>(rec + OFF_STG);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      *reinterpret_cast<uint32_t*>(rec + 512 + (8 * cb + k) * 64 + 4 * (tok0 >> 3)) = word[k];
+    for (int k = 0; k < 8; ++k) stg[stg_index(8 * cb + k, tok0 >> 3, stg_stride(16))] = word[k];
   } else {
     uint32_t half[8];  // channel 8cb + k: even-token byte in bits 0-7, odd-token byte in bits 16-23
 #pragma unroll
@@ -207,12 +216,17 @@ __device__ __forceinline__ void encode_pack(const float2 (&r)[8][4], const float
         half[2 * pp + 1] |= (__float_as_uint(q2.y) & 3u) << sh;
       }
     }
+    // word (tok0 >> 4) of channel 8cb + k: bytes 0 / 2 from the half-warp with
+    // the first 8 tokens (even / odd), bytes 1 / 3 from the one with the next
+    // 8; the lane pair (cb, cb + 16) swaps its halves, and each lane stages
+    // four of the eight words (see OFF_STG)
     const int hb = (tok0 >> 3) & 1;
+    uint32_t* stg = reinterpret_cast<uint32_t*>(rec + OFF_STG);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      unsigned char* wp = rec + 512 + (8 * cb + k) * 32 + 4 * (tok0 >> 4);
-      wp[hb] = (unsigned char)half[k];
-      wp[2 + hb] = (unsigned char)(half[k] >> 16);
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, half[k], 16);
+      const uint32_t w = hb ? __byte_perm(other, half[k], 0x6240) : __byte_perm(half[k], other, 0x6240);
+      if ((k >> 2) == hb) stg[stg_index(8 * cb + k, tok0 >> 4, stg_stride(8))] = w;
     }
   }
 }
@@ -507,8 +521,24 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
   else encode_pack<KIND, false, !ROT>(r, tokv, rec, tok0, cb);
   __syncthreads();
   const int bytes = kind_rec_bytes(KIND);
-  for (int i = tid; i < bytes / 16; i += 256)
-    *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(rec + 16 * i);
+  if constexpr (KIND == KIND_V2 || KIND == KIND_V4) {  // header from the record, codes from the staging
+    constexpr int WPC = KIND == KIND_V2 ? 8 : 16;      // code words per channel
+    const uint32_t* stg = reinterpret_cast<const uint32_t*>(rec + OFF_STG);
+    for (int i = tid; i < bytes / 16; i += 256) {
+      uint4 v;
+      if (i < 32) {
+        v = *reinterpret_cast<const uint4*>(rec + 16 * i);
+      } else {
+        const int q = 4 * (i - 32), c = q / WPC, w = q % WPC;
+        const uint32_t* src = stg + stg_index(c, w, stg_stride(WPC));
+        v = make_uint4(src[0], src[1], src[2], src[3]);
+      }
+      *reinterpret_cast<uint4*>(dst + 16 * i) = v;
+    }
+  } else {
+    for (int i = tid; i < bytes / 16; i += 256)
+      *reinterpret_cast<uint4*>(dst + 16 * i) = *reinterpret_cast<const uint4*>(rec + 16 * i);
+  }
 }
 
 // ------------------------------------------------------------------ kernels

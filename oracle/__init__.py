@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
+import threading
 
 import numpy as np
 
@@ -26,23 +27,38 @@ FLAG_CLAMPED = 1
 FLAG_STEP_SAT = 2
 
 
+_build_lock = threading.Lock()
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle with plain IEEE semantics (no FMA contraction, which
-    gcc enables by default on aarch64)."""
-    os.makedirs(BUILD, exist_ok=True)
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
-        tmp = LIB + f".{os.getpid()}.tmp"
-        subprocess.check_call(
-            ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-             "-shared", "-Wall", "-o", tmp, SRC, "-lm", "-lpthread"])
-        os.replace(tmp, LIB)
-    return LIB
+    gcc enables by default on aarch64).  Safe to call from several threads
+    (one compiles, the others wait) and processes (each writes its own
+    temporary file and renames it into place)."""
+    with _build_lock:
+        os.makedirs(BUILD, exist_ok=True)
+        if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
+            tmp = LIB + f".{os.getpid()}.{threading.get_ident()}.tmp"
+            subprocess.check_call(
+                ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                 "-shared", "-Wall", "-o", tmp, SRC, "-lm", "-lpthread"])
+            os.replace(tmp, LIB)
+        return LIB
 
 
 _lib = None
+_lib_lock = threading.Lock()
 
 
 def lib():
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        return _load()
+
+
+def _load():
     global _lib
     if _lib is None:
         L = ctypes.CDLL(build())
