@@ -35,7 +35,11 @@ struct QSmem {
   float vred[8];
 };
 constexpr int X_ROW = 272;                 // staging row stride: 256 B + 16 B pad
-constexpr int OFF_PART = 9216;             // float2 [8 warps][128]: column (mean, M2) over 16 tokens
+constexpr int OFF_PART = 9216;             // float2 [8 warps][PART_STRIDE]: column (mean, M2) over 16 tokens
+// channel c of a warp's partials at c + c / 8: the lanes of a half-warp write
+// channels 8 apart, which the skew spreads over 16 bank pairs instead of 2
+constexpr int PART_STRIDE = 144;
+__host__ __device__ constexpr int part_slot(int c) { return c + (c >> 3); }
 constexpr int OFF_TOK = 17408;             // float2 [128]: (zero-point, 1/step) per token
 constexpr int OFF_ROW = 18432;             // per half-warp row-step slot: 8 x 36 partials, 8 shifts, 8 factors
 constexpr int ROW_SLOT = 304;              // floats per slot
@@ -48,6 +52,8 @@ constexpr int OFF_STG = 40960;
 __host__ __device__ constexpr int stg_stride(int kind_words) { return kind_words + 1; }
 __device__ __forceinline__ int stg_index(int c, int w, int stride) { return ((c & 7) * 16 + (c >> 3)) * stride + w; }
 static_assert(OFF_ROW + 16 * ROW_SLOT * 4 <= OFF_STG && T * 272 <= 65536, "staging reuse overflows");
+static_assert(OFF_PART + 8 * PART_STRIDE * 8 <= OFF_ROW && part_slot(D - 1) < PART_STRIDE,
+              "column partials overflow (they may overlap the per-token values, which step 5 writes later)");
 static_assert(OFF_STG + 4 * (127 * 17 + 16) <= 65536, "value staging overflows");
 
 // New log factor ln(std) from a population variance and mean over 128
@@ -361,8 +367,8 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
         const float2 m16 = fmul2(fadd2(km, pm), make_float2(0.5f, 0.5f));
         const float2 M16 = ffma2(fmul2(dl, make_float2(4.f, 4.f)), dl, fadd2(kM, pM));
         const int c = 8 * cb + 4 * tbl + 2 * q;
-        part[warp * D + c] = make_float2(m16.x, M16.x);
-        part[warp * D + c + 1] = make_float2(m16.y, M16.y);
+        part[warp * PART_STRIDE + part_slot(c)] = make_float2(m16.x, M16.x);
+        part[warp * PART_STRIDE + part_slot(c + 1)] = make_float2(m16.y, M16.y);
       }
     }
     __syncthreads();
@@ -370,7 +376,7 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
       float mw[8], msum = 0.f, M2 = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
-        const float2 v = part[w * D + tid];
+        const float2 v = part[w * PART_STRIDE + part_slot(tid)];
         mw[w] = v.x; msum += v.x; M2 += v.y;
       }
       const float mean = msum * 0.125f;
