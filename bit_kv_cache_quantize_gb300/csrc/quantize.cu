@@ -29,17 +29,24 @@ namespace kvarn {
 // then the packed record, the column partial sums and per-token scale pairs.
 struct QSmem {
   alignas(128) unsigned char xs[65536];
-  float beta[D];                            // column factors exp(-v) of the last column step
+  float beta[D + 12];                       // column factors exp(-v) of the last column step (beta_slot)
   float inv_g[D];
   float g[D];                               // the channel scales themselves (unrotated path)
   float vred[8];
 };
 constexpr int X_ROW = 272;                 // staging row stride: 256 B + 16 B pad
 constexpr int OFF_PART = 9216;             // float2 [8 warps][PART_STRIDE]: column (mean, M2) over 16 tokens
-// channel c of a warp's partials at c + c / 8: the lanes of a half-warp write
-// channels 8 apart, which the skew spreads over 16 bank pairs instead of 2
-constexpr int PART_STRIDE = 144;
-__host__ __device__ constexpr int part_slot(int c) { return c + (c >> 3); }
+// channel c of a warp's partials at c + c / 16: the lanes of a half-warp
+// write channels 8 apart, which the skew spreads over all 16 bank pairs
+// (without it they share 2), and the merge's 32 consecutive channels still
+// take each bank pair twice, the minimum for 256 bytes
+constexpr int PART_STRIDE = 136;
+__host__ __device__ constexpr int part_slot(int c) { return c + (c >> 4); }
+// channel c of the column factors at c + 4 (c / 32): each lane reads 8
+// channels as two float4, 8 channels apart from the next lane's; shifting
+// each 32-channel block by 4 more words spreads a half-warp over 8 bank
+// quads instead of 4
+__host__ __device__ constexpr int beta_slot(int c) { return c + 4 * (c >> 5); }
 constexpr int OFF_TOK = 17408;             // float2 [128]: (zero-point, 1/step) per token
 constexpr int OFF_ROW = 18432;             // per half-warp row-step slot: 8 x 36 partials, 8 shifts, 8 factors
 constexpr int ROW_SLOT = 304;              // floats per slot
@@ -52,6 +59,7 @@ constexpr int OFF_STG = 40960;
 __host__ __device__ constexpr int stg_stride(int kind_words) { return kind_words + 1; }
 __device__ __forceinline__ int stg_index(int c, int w, int stride) { return ((c & 7) * 16 + (c >> 3)) * stride + w; }
 static_assert(OFF_ROW + 16 * ROW_SLOT * 4 <= OFF_STG && T * 272 <= 65536, "staging reuse overflows");
+static_assert(beta_slot(D - 1) < D + 12, "column factors overflow");
 static_assert(OFF_PART + 8 * PART_STRIDE * 8 <= OFF_ROW && part_slot(D - 1) < PART_STRIDE,
               "column partials overflow (they may overlap the per-token values, which step 5 writes later)");
 static_assert(OFF_STG + 4 * (127 * 17 + 16) <= 65536, "value staging overflows");
@@ -383,7 +391,7 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
 #pragma unroll
       for (int w = 0; w < 8; ++w) M2 = fmaf(16.f * (mw[w] - mean), mw[w] - mean, M2);
       v_c = log_std_or_keep(M2 * (1.0f / 128.0f), mean, v_c);
-      sm.beta[tid] = __expf(-v_c);
+      sm.beta[beta_slot(tid)] = __expf(-v_c);
     }
     __syncthreads();
     // row step: the half-warp holding tokens tok0 .. tok0+7 reduces through
@@ -391,8 +399,8 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
     // each token's owner lanes (cb = 2i, 2i+1) sum the 16 partials of token i
     {
       float* rs = reinterpret_cast<float*>(sm.xs + OFF_ROW) + (2 * warp + tbl) * ROW_SLOT;
-      const float4 b0 = *reinterpret_cast<const float4*>(sm.beta + 8 * cb);
-      const float4 b1 = *reinterpret_cast<const float4*>(sm.beta + 8 * cb + 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(sm.beta + beta_slot(8 * cb));
+      const float4 b1 = *reinterpret_cast<const float4*>(sm.beta + beta_slot(8 * cb) + 4);
       const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
                             make_float2(b1.z, b1.w)};
       if (cb == 0) {  // channel 0 of each token: the shift of its row
