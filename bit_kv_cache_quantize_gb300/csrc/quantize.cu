@@ -302,11 +302,14 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
       }
     }
     // transpose the warp's 16 x 128 slab into 8x8 blocks through 8 KB of
-    // shared memory (XOR-swizzled columns keep both sides conflict-light)
+    // shared memory.  Column c of row r sits at c ^ 8 (r & 3) ^ 4 ((c >> 5) & 1):
+    // both sides then take the minimum number of wavefronts (the readers'
+    // 16 float4 of one row are 32 bytes apart, which without the second term
+    // shares 4 bank quads among 16 lanes)
     float* slab = reinterpret_cast<float*>(sm.xs) + warp * 2048;
 #pragma unroll
     for (int nb = 0; nb < 16; ++nb) {
-      const int col = (8 * nb + 2 * j) ^ (8 * (g & 3));
+      const int col = (8 * nb + 2 * j) ^ (8 * (g & 3)) ^ (4 * ((nb >> 2) & 1));
       *reinterpret_cast<float2*>(slab + g * 128 + col) = make_float2(acc[nb][0] * INV_SQRT_D, acc[nb][1] * INV_SQRT_D);
       *reinterpret_cast<float2*>(slab + (g + 8) * 128 + col) =
           make_float2(acc[nb][2] * INV_SQRT_D, acc[nb][3] * INV_SQRT_D);
@@ -316,7 +319,8 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
     for (int i = 0; i < 8; ++i)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const float4 v = *reinterpret_cast<const float4*>(slab + (8 * tbl + i) * 128 + ((8 * cb + 4 * hh) ^ (8 * (i & 3))));
+        const float4 v = *reinterpret_cast<const float4*>(slab + (8 * tbl + i) * 128 +
+                                                          ((8 * cb + 4 * hh) ^ (8 * (i & 3)) ^ (4 * ((cb >> 2) & 1))));
         r[i][2 * hh] = make_float2(v.x, v.y);
         r[i][2 * hh + 1] = make_float2(v.z, v.w);
       }
