@@ -5,15 +5,18 @@
 // the Catch Lives", section "What KVarN does differently"; page "Huawei's
 // KVarN puts KV-cache quantization inside vLLM's backend", sections "What
 // KVarN changes in vLLM's serving path" and "The four-stage pipeline"):
-//   1. Hadamard rotation along channels, R = X H: a 128x128x128 product on
-//      the tensor cores (A = the 16-bit tile, exact; B = the +-1 Sylvester
-//      signs generated in registers; fp32 accumulate), scaled by 1/sqrt(128).
+//   1. Hadamard rotation along channels, R = X H with the Sylvester H =
+//      H8 (x) H16: a block-diagonal product with H16 on the tensor cores
+//      (A = the 16-bit tile, exact; B = the +-1 signs generated in
+//      registers; fp32 accumulate), then an 8-point Walsh-Hadamard transform
+//      across the 16-channel groups in registers; scaled by 1/sqrt(128).
 //   2. Sinkhorn-like normalisation in log space: N iterations of a column
 //      step (log std over tokens of every channel) then a row step (log std
-//      over channels of every token).  Column steps read a channel-major
-//      register copy of R, row steps a token-major copy, so both reductions
-//      finish inside a quad of lanes.  Each std is a shifted one-pass sum
-//      (shift = the first element), exact for a constant row or column.
+//      over channels of every token).  Each thread holds an 8-token x
+//      8-channel block of R; the column step reduces across the lane pair
+//      and the 8 warps through shared memory, the row step across the 16
+//      lanes of a half-warp.  Each std is a shifted one-pass sum (shift = the
+//      first element), exact for a constant row or column.
 //   3. Column factors centred (geometric mean 1) -> FP8 E4M3 scale g.
 //   4. Per token: Y = R / g, FP16 zero-point b = round-down(min Y), FP8 step
 //      a = round-up((max Y - b) / L).
@@ -282,10 +285,15 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
     ldmatrix_x4(afr[ks], sm.xs + (16 * warp + (lane & 15)) * X_ROW + (16 * ks + (lane >> 4) * 8) * 2);
   __syncthreads();  // the staging area is reused below
 
-  // ---- 2. R = X H on the tensor cores; H[k][n] = (-1)^popcount(k & n)
-  // For k = 16ks + kk, n = 8nb + g:  popcount(k & n) = popcount(kk & g)
-  // + (kk >> 3) * (nb & 1) + popcount(ks & (nb >> 1)), so every B fragment is
-  // +-F with F the lane's base sign pair.
+  // ---- 2. R = X H; H[k][n] = (-1)^popcount(k & n) (Sylvester order)
+  // With k = 16a' + b', n = 16a + b the sign splits, popcount(k & n) =
+  // popcount(a' & a) + popcount(b' & b): H = H8 (x) H16.  So first
+  // Y = X (I8 (x) H16) on the tensor cores, one MMA per 8-column block nb
+  // (its 16-channel group a = nb >> 1 is k-block a), then R = Y (H8 (x) I16),
+  // an 8-point Walsh-Hadamard transform across the groups that each lane does
+  // in registers (it holds column 8nb + 2j (+1) of every block).  For
+  // kk = k - 16a, n = 8nb + g: the H16 sign is popcount(kk & g) +
+  // (kk >> 3)(nb & 1), so every B fragment is +-F, F the lane's base sign pair.
   {
     const uint32_t one = Bits16<E>::one;
     const uint32_t F = ((__popc((2 * j) & g) & 1) ? (one | 0x8000u) : one) |
@@ -295,12 +303,21 @@ __device__ void quantize_tile_cta(const E* __restrict__ src, int64_t row_stride,
 #pragma unroll
     for (int nb = 0; nb < 16; ++nb) {
       acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int P = __builtin_popcount(ks & (nb >> 1)) & 1;
-        mma16816<E>(acc[nb], afr[ks], P ? NF : F, (P ^ (nb & 1)) ? NF : F);
-      }
+      mma16816<E>(acc[nb], afr[nb >> 1], F, (nb & 1) ? NF : F);
     }
+#pragma unroll
+    for (int st = 1; st < 8; st <<= 1)    // butterflies over the group index a, block nb = 2a + h
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+        if (!(a & st))
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float u = acc[2 * a + h][e], v = acc[2 * (a ^ st) + h][e];
+              acc[2 * a + h][e] = u + v;
+              acc[2 * (a ^ st) + h][e] = u - v;
+            }
     // transpose the warp's 16 x 128 slab into 8x8 blocks through 8 KB of
     // shared memory.  Column c of row r sits at c ^ 8 (r & 3) ^ 4 ((c >> 5) & 1):
     // both sides then take the minimum number of wavefronts (the readers'
