@@ -34,6 +34,8 @@
 // stage once all of them are done with it), one thread of warp 12 issues
 // the first bulk copies and the MMAs.  Operands that a later tile reuses are
 // double-buffered (K~, scores, scales) or guarded by the previous PV (V~).
+#include <type_traits>
+
 #include "common.cuh"
 #include "tcgen05.cuh"
 
@@ -705,37 +707,44 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       const int nvis = ((vmask >> k) & 1u) ? min(64, pos - t0 + 1) : 0;  // tokens of this half the row sees
       const float2 d2 = make_float2(d128, d128);
       float tmax = -INFINITY;
+      // the causal mask, in a second copy of the loop that only a tile with
+      // hidden tokens takes (padded rows are never written, so they may skip it)
+      auto pass1 = [&](auto mask_c) {
+        constexpr bool MASK = decltype(mask_c)::value;
 #pragma unroll 1
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t d[16];
-        tmem_ld16(sb + 64 * half + c, d);
-        const float4* ka4 = reinterpret_cast<const float4*>(sm.ka[s] + 64 * half + c);
-        const float4* kb4 = reinterpret_cast<const float4*>(sm.kb[s] + 64 * half + c);
-        float4 a4[4], b4[4];
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t d[16];
+          tmem_ld16(sb + 64 * half + c, d);
+          const float4* ka4 = reinterpret_cast<const float4*>(sm.ka[s] + 64 * half + c);
+          const float4* kb4 = reinterpret_cast<const float4*>(sm.kb[s] + 64 * half + c);
+          float4 a4[4], b4[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { a4[j] = ka4[j]; b4[j] = kb4[j]; }
-        tmem_wait_ld();
+          for (int j = 0; j < 4; ++j) { a4[j] = ka4[j]; b4[j] = kb4[j]; }
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float2 s01 = ffma2(make_float2(a4[j].x, a4[j].y),
-                             make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
-                             fmul2(make_float2(b4[j].x, b4[j].y), d2));
-          float2 s23 = ffma2(make_float2(a4[j].z, a4[j].w),
-                             make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
-                             fmul2(make_float2(b4[j].z, b4[j].w), d2));
-          const int t = c + 4 * j;
-          if (nvis < 64) {
-            if (t >= nvis) s01.x = -INFINITY;
-            if (t + 1 >= nvis) s01.y = -INFINITY;
-            if (t + 2 >= nvis) s23.x = -INFINITY;
-            if (t + 3 >= nvis) s23.y = -INFINITY;
+          for (int j = 0; j < 4; ++j) {
+            float2 s01 = ffma2(make_float2(a4[j].x, a4[j].y),
+                               make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])),
+                               fmul2(make_float2(b4[j].x, b4[j].y), d2));
+            float2 s23 = ffma2(make_float2(a4[j].z, a4[j].w),
+                               make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])),
+                               fmul2(make_float2(b4[j].z, b4[j].w), d2));
+            const int t = c + 4 * j;
+            if (MASK && nvis < 64) {
+              if (t >= nvis) s01.x = -INFINITY;
+              if (t + 1 >= nvis) s01.y = -INFINITY;
+              if (t + 2 >= nvis) s23.x = -INFINITY;
+              if (t + 3 >= nvis) s23.y = -INFINITY;
+            }
+            tmax = fmaxf(tmax, fmaxf(fmaxf(s01.x, s01.y), fmaxf(s23.x, s23.y)));
+            d[4 * j] = __float_as_uint(s01.x); d[4 * j + 1] = __float_as_uint(s01.y);
+            d[4 * j + 2] = __float_as_uint(s23.x); d[4 * j + 3] = __float_as_uint(s23.y);
           }
-          tmax = fmaxf(tmax, fmaxf(fmaxf(s01.x, s01.y), fmaxf(s23.x, s23.y)));
-          d[4 * j] = __float_as_uint(s01.x); d[4 * j + 1] = __float_as_uint(s01.y);
-          d[4 * j + 2] = __float_as_uint(s23.x); d[4 * j + 3] = __float_as_uint(s23.y);
+          tmem_st16(sb + 64 * half + c, d);
         }
-        tmem_st16(sb + 64 * half + c, d);
-      }
+      };
+      if (__all_sync(0xffffffffu, !rv || nvis >= 64)) pass1(std::false_type{});
+      else pass1(std::true_type{});
       tmem_wait_st();
       tc_fence_before();  // both halves read D_128 before either writes beta (ordered by xbar)
       // the row maximum: exchange with the other half through shared memory
@@ -772,36 +781,43 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
       // l += sum p, beta += sum p bV
       const float2 nm2 = make_float2(-m_ref, -m_ref);
       float2 lt = make_float2(0.f, 0.f), bt = make_float2(0.f, 0.f);
+      // a row that has seen no token yet (reference still -inf) gets p = 0, in
+      // a second copy of the loop that only such tiles take
+      auto pass2 = [&](auto zero_c) {
+        constexpr bool ZERO = decltype(zero_c)::value;
 #pragma unroll 1
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t d[16];
-        tmem_ld16(sb + 64 * half + c, d);
-        const float4* va4 = reinterpret_cast<const float4*>(sm.va[s] + 64 * half + c);
-        const float4* vb4 = reinterpret_cast<const float4*>(sm.vb[s] + 64 * half + c);
-        float4 a4[4], b4[4];
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t d[16];
+          tmem_ld16(sb + 64 * half + c, d);
+          const float4* va4 = reinterpret_cast<const float4*>(sm.va[s] + 64 * half + c);
+          const float4* vb4 = reinterpret_cast<const float4*>(sm.vb[s] + 64 * half + c);
+          float4 a4[4], b4[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) { a4[j] = va4[j]; b4[j] = vb4[j]; }
-        tmem_wait_ld();
-        uint32_t pw[16];  // hi words 0..7, lo words 8..15
+          for (int j = 0; j < 4; ++j) { a4[j] = va4[j]; b4[j] = vb4[j]; }
+          tmem_wait_ld();
+          uint32_t pw[16];  // hi words 0..7, lo words 8..15
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 e01 = ffma2(cr2, make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), nm2);
-          const float2 e23 = ffma2(cr2, make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), nm2);
-          float2 p01 = make_float2(ex2_ftz(e01.x), ex2_ftz(e01.y)), p23 = make_float2(ex2_ftz(e23.x), ex2_ftz(e23.y));
-          if (!live) p01 = p23 = make_float2(0.f, 0.f);
-          lt = fadd2(lt, fadd2(p01, p23));
-          bt = ffma2(p01, make_float2(b4[j].x, b4[j].y), ffma2(p23, make_float2(b4[j].z, b4[j].w), bt));
-          const float2 x01 = fmul2(p01, make_float2(a4[j].x, a4[j].y)), x23 = fmul2(p23, make_float2(a4[j].z, a4[j].w));
-          const __nv_bfloat162 h01 = __floats2bfloat162_rn(x01.x, x01.y), h23 = __floats2bfloat162_rn(x23.x, x23.y);
-          const float2 r01 = fadd2(x01, fmul2(__bfloat1622float2(h01), make_float2(-1.f, -1.f)));
-          const float2 r23 = fadd2(x23, fmul2(__bfloat1622float2(h23), make_float2(-1.f, -1.f)));
-          pw[2 * j] = b2u(h01);
-          pw[2 * j + 1] = b2u(h23);
-          pw[8 + 2 * j] = b2u(__floats2bfloat162_rn(r01.x, r01.y));
-          pw[8 + 2 * j + 1] = b2u(__floats2bfloat162_rn(r23.x, r23.y));
+          for (int j = 0; j < 4; ++j) {
+            const float2 e01 = ffma2(cr2, make_float2(__uint_as_float(d[4 * j]), __uint_as_float(d[4 * j + 1])), nm2);
+            const float2 e23 = ffma2(cr2, make_float2(__uint_as_float(d[4 * j + 2]), __uint_as_float(d[4 * j + 3])), nm2);
+            float2 p01 = make_float2(ex2_ftz(e01.x), ex2_ftz(e01.y)), p23 = make_float2(ex2_ftz(e23.x), ex2_ftz(e23.y));
+            if (ZERO && !live) p01 = p23 = make_float2(0.f, 0.f);
+            lt = fadd2(lt, fadd2(p01, p23));
+            bt = ffma2(p01, make_float2(b4[j].x, b4[j].y), ffma2(p23, make_float2(b4[j].z, b4[j].w), bt));
+            const float2 x01 = fmul2(p01, make_float2(a4[j].x, a4[j].y)), x23 = fmul2(p23, make_float2(a4[j].z, a4[j].w));
+            const __nv_bfloat162 h01 = __floats2bfloat162_rn(x01.x, x01.y), h23 = __floats2bfloat162_rn(x23.x, x23.y);
+            const float2 r01 = fadd2(x01, fmul2(__bfloat1622float2(h01), make_float2(-1.f, -1.f)));
+            const float2 r23 = fadd2(x23, fmul2(__bfloat1622float2(h23), make_float2(-1.f, -1.f)));
+            pw[2 * j] = b2u(h01);
+            pw[2 * j + 1] = b2u(h23);
+            pw[8 + 2 * j] = b2u(__floats2bfloat162_rn(r01.x, r01.y));
+            pw[8 + 2 * j + 1] = b2u(__floats2bfloat162_rn(r23.x, r23.y));
+          }
+          tmem_st16(sb + 64 * half + c, pw);
         }
-        tmem_st16(sb + 64 * half + c, pw);
-      }
+      };
+      if (__all_sync(0xffffffffu, !rv || live)) pass2(std::false_type{});
+      else pass2(std::true_type{});
       l_sum += lt.x + lt.y;
       {
         const float beta = bt.x + bt.y;
