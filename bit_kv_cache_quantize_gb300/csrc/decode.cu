@@ -385,6 +385,7 @@ __global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams 
       const float m_new = fmaxf(m_run, tmax * qsi);
       const float corr = ex2_ftz(m_run - m_new);
       const float nm = -m_new;
+      const float2 nm2 = make_float2(nm, nm), qsi2 = make_float2(qsi, qsi);
       m_run = m_new;
       // ---- P = p aV 64 / 4^(nb & 3), hi rows 0-7 / lo rows 8-15
       uint32_t pfr[8][4];
@@ -399,7 +400,8 @@ __global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int nb = 4 * q4 + i;
-          const float2 pr = make_float2(ex2_ftz(fmaf(sc[nb].x, qsi, nm)), ex2_ftz(fmaf(sc[nb].y, qsi, nm)));
+          const float2 ea = ffma2(sc[nb], qsi2, nm2);  // per element the same fused multiply-add as fmaf
+          const float2 pr = make_float2(ex2_ftz(ea.x), ex2_ftz(ea.y));
           psum = fadd2(psum, pr);
           pb = ffma2(pr, __half22float2(u2h2(bw[i])), pb);
           // undo the field multiplier of the V operand: 4^(nb & 3) for 2-bit fields, 16^(nb & 1) for 4-bit
@@ -408,7 +410,7 @@ __global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams 
           const __half2 av = __hmul2(e4m3x2_to_half2(((i & 2) ? a8.y : a8.x) >> (16 * (i & 1))), f2);  // exact
           const float2 pa = fmul2(pr, __half22float2(av));
           const __half2 hi = __float22half2_rn(pa);
-          const float2 lo = fadd2(pa, fmul2(__half22float2(hi), make_float2(-1.f, -1.f)));
+          const float2 lo = ffma2(__half22float2(hi), make_float2(-1.f, -1.f), pa);  // pa - hi, exact product
           pfr[nb >> 1][(nb & 1) ? 2 : 0] = h22u(hi);
           pfr[nb >> 1][(nb & 1) ? 3 : 1] = h22u(__float22half2_rn(lo));
         }

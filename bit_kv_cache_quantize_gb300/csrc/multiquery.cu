@@ -806,8 +806,8 @@ __global__ void __launch_bounds__(MQ_THREADS, 1) mq_kernel(MQParams p) {
             bt = ffma2(p01, make_float2(b4[j].x, b4[j].y), ffma2(p23, make_float2(b4[j].z, b4[j].w), bt));
             const float2 x01 = fmul2(p01, make_float2(a4[j].x, a4[j].y)), x23 = fmul2(p23, make_float2(a4[j].z, a4[j].w));
             const __nv_bfloat162 h01 = __floats2bfloat162_rn(x01.x, x01.y), h23 = __floats2bfloat162_rn(x23.x, x23.y);
-            const float2 r01 = fadd2(x01, fmul2(__bfloat1622float2(h01), make_float2(-1.f, -1.f)));
-            const float2 r23 = fadd2(x23, fmul2(__bfloat1622float2(h23), make_float2(-1.f, -1.f)));
+            const float2 r01 = ffma2(__bfloat1622float2(h01), make_float2(-1.f, -1.f), x01);  // x - hi, exact product
+            const float2 r23 = ffma2(__bfloat1622float2(h23), make_float2(-1.f, -1.f), x23);
             pw[2 * j] = b2u(h01);
             pw[2 * j + 1] = b2u(h23);
             pw[8 + 2 * j] = b2u(__floats2bfloat162_rn(r01.x, r01.y));
