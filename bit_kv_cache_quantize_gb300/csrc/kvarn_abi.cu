@@ -11,7 +11,7 @@
 
 namespace kvarn {
 constexpr int kChunkTiles = 16;  // packed tiles per split-K CTA of an ordinary call (sizes the workspace)
-constexpr int kSmallChunkTiles = 8;  // of a small call: one tile per warp
+constexpr int kSmallChunkTiles = 8;  // of a small call: two tiles per warp of its 4-warp CTAs
 // A call whose table spans fewer (sequence, KV head, tile) units than this
 // is small: 16-tile chunks would give it under three waves of two 8-warp
 // CTAs per SM on 152 SMs (3 x 304 x 16), so it takes 8-tile chunks, twice
