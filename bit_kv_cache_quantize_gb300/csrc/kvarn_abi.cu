@@ -146,7 +146,7 @@ kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, con
   if (st != KVARN_OK) return st;
   if (batch < 0 || max_blocks < 1) return KVARN_ERR_INVALID;
   if (batch == 0) return KVARN_OK;
-  if (batch > 0x7fffffff / 1 || cfg->num_kv_heads > 65535) return KVARN_ERR_INVALID;
+  if (static_cast<int64_t>(batch) * cfg->num_kv_heads * 2 > 0x7fffffffLL) return KVARN_ERR_INVALID;
   if (!k_new || !v_new || !pos || !block_table || !tail_pool || (!block_pool && cfg->num_blocks > 0)) return KVARN_ERR_INVALID;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(tail_pool) || !aligned16(block_pool))
     return KVARN_ERR_INVALID;

@@ -45,6 +45,7 @@ struct AppendParams {
   int32_t k_bits;
   int32_t v_bits;
   int32_t* err;
+  int32_t batch;  // sequences (set by the launcher)
 };
 struct DecodeParams {
   const void* q;

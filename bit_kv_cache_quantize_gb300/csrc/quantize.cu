@@ -22,6 +22,8 @@
 //      a = round-up((max Y - b) / L).
 //   5. Codes rne((Y - b) * (1/a)), clamped to [0, L]; packed and stored with
 //      16-byte stores.
+#include <algorithm>
+
 #include "common.cuh"
 #include "params.h"
 
@@ -612,43 +614,72 @@ __global__ void __launch_bounds__(256, 2) quantize_tiles_kernel(QuantizeParams p
 }
 
 
-// One CTA per (sequence, head, K|V): copy the new token into the open tile;
-// the CTA whose token fills the tile quantises it into the sequence's block.
+// Append one token per (sequence, head, K|V) unit to its open tile; a token
+// that fills the tile has the whole CTA quantise it into the sequence's block.
+// The grid is at most two CTAs per SM: most units only copy 256 bytes, and a
+// grid of one 66 KB CTA per unit would take batch x heads x 2 / (2 x SMs)
+// waves to do it.
 template <typename E>
 __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   QSmem& sm = *reinterpret_cast<QSmem*>(smem_raw);
-  const int b = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
-  const int pos = prm.pos[b];
-  if (pos < 0 || pos / T >= prm.max_blocks) {
-    if (threadIdx.x == 0 && h == 0 && kv == 0) set_error(prm.err, KVARN_DEV_ERR_TOKEN_RANGE);
-    return;
+  __shared__ int32_t close_blk[16];  // per unit of the current round: block its tile closes into, or -1
+  const int64_t units = static_cast<int64_t>(prm.batch) * prm.num_kv_heads * 2;
+  const size_t tail_bytes = (size_t)units * T * D * sizeof(E);
+  const int grp = threadIdx.x >> 4, gl = threadIdx.x & 15;
+  // This CTA owns units blockIdx.x + k * gridDim.x (unit = (sequence, head,
+  // K|V)), sixteen per round.
+  for (int64_t r0 = blockIdx.x; r0 < units; r0 += 16LL * gridDim.x) {
+    // 1. sixteen threads per unit copy its token into the open tile and note
+    //    whether the token closes the tile
+    const int64_t u = r0 + static_cast<int64_t>(grp) * gridDim.x;
+    int32_t cb = -1;
+    if (u < units) {
+      const int kv = static_cast<int>(u & 1);
+      const int h = static_cast<int>((u >> 1) % prm.num_kv_heads), b = static_cast<int>((u >> 1) / prm.num_kv_heads);
+      const int pos = prm.pos[b];
+      if (pos < 0 || pos / T >= prm.max_blocks) {
+        if (gl == 0 && h == 0 && kv == 0) set_error(prm.err, KVARN_DEV_ERR_TOKEN_RANGE);
+      } else {
+        E* tile = static_cast<E*>(prm.tail) + u * (T * D);
+        const int slot = pos & (T - 1);
+        if (kcheck(tile, T * D * sizeof(E), prm.tail, tail_bytes, prm.err)) {
+          const E* src = static_cast<const E*>(kv ? prm.v_new : prm.k_new) + (u >> 1) * D;
+          reinterpret_cast<uint4*>(tile + slot * D)[gl] = reinterpret_cast<const uint4*>(src)[gl];
+          if (slot == T - 1) {
+            const int32_t blk = prm.block_table[static_cast<int64_t>(b) * prm.max_blocks + pos / T];
+            if (blk >= 0 && blk < prm.num_blocks) {
+              cb = blk;
+              __threadfence();  // the token reaches L2 before the CTA's cp.async reads the tile
+            } else if (gl == 0) {
+              set_error(prm.err, KVARN_DEV_ERR_BLOCK_RANGE);
+            }
+          }
+        }
+      }
+    }
+    if (gl == 0) close_blk[grp] = cb;
+    __syncthreads();
+    // 2. the whole CTA quantises the closed tiles one after another
+    for (int j = 0; j < 16; ++j) {
+      const int32_t blk = close_blk[j];
+      if (blk < 0) continue;
+      const int64_t uj = r0 + static_cast<int64_t>(j) * gridDim.x;
+      const int kv = static_cast<int>(uj & 1), h = static_cast<int>((uj >> 1) % prm.num_kv_heads);
+      const E* tile = static_cast<const E*>(prm.tail) + uj * (T * D);
+      unsigned char* dst =
+          prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits, prm.v_bits) + kv * rec_bytes(prm.k_bits);
+      if (!kcheck(dst, rec_bytes(kv ? prm.v_bits : prm.k_bits), prm.pool, (size_t)prm.num_blocks * prm.block_bytes,
+                  prm.err))
+        continue;
+      if (kv && prm.v_bits == 4) quantize_tile_cta<E, KIND_V4>(tile, D, dst, prm.iters, sm);
+      else if (kv) quantize_tile_cta<E, KIND_V2>(tile, D, dst, prm.iters, sm);
+      else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(tile, D, dst, prm.iters, sm);
+      else quantize_tile_cta<E, KIND_K2>(tile, D, dst, prm.iters, sm);
+      __syncthreads();  // the next tile reuses the shared memory
+    }
+    __syncthreads();  // close_blk is rewritten by the next round
   }
-  E* tile = static_cast<E*>(prm.tail) + ((static_cast<int64_t>(b) * prm.num_kv_heads + h) * 2 + kv) * (T * D);
-  const int slot = pos & (T - 1);
-  if (!kcheck(tile, T * D * sizeof(E), prm.tail, (size_t)gridDim.x * prm.num_kv_heads * 2 * T * D * sizeof(E), prm.err))
-    return;
-  if (threadIdx.x < 16) {
-    const E* src = static_cast<const E*>(kv ? prm.v_new : prm.k_new) + (static_cast<int64_t>(b) * prm.num_kv_heads + h) * D;
-    reinterpret_cast<uint4*>(tile + slot * D)[threadIdx.x] = reinterpret_cast<const uint4*>(src)[threadIdx.x];
-  }
-  if (slot != T - 1) return;
-  const int32_t blk = prm.block_table[static_cast<int64_t>(b) * prm.max_blocks + pos / T];
-  if (blk < 0 || blk >= prm.num_blocks) {
-    if (threadIdx.x == 0) set_error(prm.err, KVARN_DEV_ERR_BLOCK_RANGE);
-    return;
-  }
-  __threadfence();
-  __syncthreads();
-  unsigned char* dst =
-      prm.pool + blk * prm.block_bytes + h * head_rec(prm.k_bits, prm.v_bits) + kv * rec_bytes(prm.k_bits);
-  if (!kcheck(dst, rec_bytes(kv ? prm.v_bits : prm.k_bits), prm.pool, (size_t)prm.num_blocks * prm.block_bytes,
-              prm.err))
-    return;
-  if (kv && prm.v_bits == 4) quantize_tile_cta<E, KIND_V4>(tile, D, dst, prm.iters, sm);
-  else if (kv) quantize_tile_cta<E, KIND_V2>(tile, D, dst, prm.iters, sm);
-  else if (prm.k_bits == 4) quantize_tile_cta<E, KIND_K4>(tile, D, dst, prm.iters, sm);
-  else quantize_tile_cta<E, KIND_K2>(tile, D, dst, prm.iters, sm);
 }
 
 // Dequantise (tests): one CTA of 128 threads per (block, head, K|V); thread
@@ -836,7 +867,17 @@ static cudaError_t launch_append_t(const AppendParams& p, int batch, cudaStream_
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = smem_attr_once(attr_done, (const void*)append_tokens_kernel<E>, (int)smem);
   if (e != cudaSuccess) return e;
-  append_tokens_kernel<E><<<dim3(batch, p.num_kv_heads, 2), 256, smem, s>>>(p);
+  // at most two CTAs per SM (the 66 KB of shared memory a closing tile needs)
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  AppendParams q = p;
+  q.batch = batch;
+  const long long units = (long long)batch * p.num_kv_heads * 2;
+  int grid = (int)std::min<long long>(units, 2LL * std::max(sms, 1));
+  if (grid > 1 && grid % 2 == 0) --grid;  // odd: each CTA's units alternate K and V tiles
+  append_tokens_kernel<E><<<grid, 256, smem, s>>>(q);
   return cudaGetLastError();
 }
 

@@ -162,6 +162,7 @@ kvarn_status kvarn_quantize_tiles(const kvarn_config* cfg, const void* k, const 
  *  tail_pool     device, kvarn_tail_bytes(cfg, batch) bytes (layout above).
  *  block_pool    device packed pool.
  * Out-of-range positions or blocks set *dev_err and skip that sequence.
+ * KVARN_ERR_INVALID if batch * num_kv_heads * 2 exceeds 2^31 - 1.
  */
 kvarn_status kvarn_append_tokens(const kvarn_config* cfg, const void* k_new, const void* v_new,
                                  const int32_t* pos, const int32_t* block_table, int32_t max_blocks,

@@ -86,6 +86,10 @@ def test_argument_validation_is_host_side(lib):
                                     check=False) == K.KVARN_ERR_INVALID
     assert K.kvarn_append_tokens(cfg, 16, 16, 16, 16, 4, 0, 16, 16, 16, stream=0, check=False) == 0
     assert K.kvarn_append_tokens(cfg, 8, 16, 16, 16, 4, 1, 16, 16, 16, stream=0, check=False) == K.KVARN_ERR_INVALID
+    # the append walks batch x heads x (K, V) units with a 32-bit count
+    big = 0x7fffffff // (2 * 8) + 1
+    assert K.kvarn_append_tokens(cfg, 16, 16, 16, 16, 4, big, 16, 16, 16, stream=0,
+                                 check=False) == K.KVARN_ERR_INVALID
     assert K.kvarn_dequantize(cfg, 16, 16, -1, 16, 16, stream=0, check=False) == K.KVARN_ERR_INVALID
     assert K.kvarn_status_string(K.KVARN_ERR_UNSUPPORTED) == "unsupported configuration"
     with pytest.raises(K.KvarnError):
