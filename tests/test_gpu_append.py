@@ -128,6 +128,19 @@ def test_append_close_bf16():
     run_steps(w, 2)
 
 
+def test_append_every_sequence_closes():
+    """320 sequences x 8 KV heads = 5120 (sequence, head, K|V) units, more
+    than the grid's CTAs take in one round of sixteen, and every sequence
+    closes a tile on the same step: CTAs quantise up to sixteen tiles one
+    after another and go round twice.  Every closed tile is compared with
+    the oracle."""
+    lens = [127 + 128 * (b % 3) for b in range(320)]
+    w = I.Workload("append_all_close", len(lens), 16, 8, "bf16", lens, seed=53, decode_steps=1, max_tokens=400,
+                   block_perm=True)
+    st = run_steps(w, 1, check_seqs=[0, 1, 2, 319])
+    assert st.tiles == 2 * 8 * len(lens)
+
+
 @pytest.mark.slow
 def test_ragged_serving_full_size():
     """256 sequences, lengths U[128, 32768], 64 decode steps: every tile that
