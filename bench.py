@@ -648,8 +648,10 @@ def run_reference(args, rank, world):
 def profile_case(name, launches):
     """Small single-kernel workloads for ncu captures (each > L2, a few GB at
     most): the 16K decode (436 MB packed; 570 MB with the K4/V4 preset), the
-    16-bit decode on the same shapes (2.1 GB), or the quantiser on 4 of the 32
-    prefill sequences."""
+    16-bit decode on the same shapes (2.1 GB), the quantiser on 4 of the 32
+    prefill sequences, or the serving step's append (256 sequences x 8 KV
+    heads with the ragged mix's open-tile fill, two of them closing a tile;
+    134 MB of open tiles)."""
     import torch
     from bit_kv_cache_quantize_gb300 import build as B
     from bit_kv_cache_quantize_gb300 import inputs as I
@@ -673,6 +675,19 @@ def profile_case(name, launches):
         q = I.multi_queries(w, 16, device=dev)
         o = torch.empty(w.batch, 16, w.num_q_heads, D, dtype=torch.float32, device=dev)
         fn = lambda: c.multiquery(q, 16, o)
+    elif name == "append":
+        full = I.ragged_32b()
+        r = [n % T for n in full.seq_lens]
+        s = next(s for s in range(T) if sum((x + s) % T == T - 1 for x in r) == 2)
+        lens = [T + (x + s) % T for x in r]  # the mix's open-tile fill s steps on, over one closed tile
+        w = I.Workload("append_ragged_mix", full.batch, full.num_q_heads, full.num_kv_heads, full.dtype, lens,
+                       seed=full.seed, decode_steps=1, max_tokens=2 * T, block_perm=True)
+        c = PagedCache(w, dev)
+        c.prefill()
+        pos = torch.tensor(lens, dtype=torch.int32, device=dev)
+        kn = torch.stack([I.kv_values(w, "k", b, lens[b], 1, dev)[0] for b in range(w.batch)])
+        vn = torch.stack([I.kv_values(w, "v", b, lens[b], 1, dev)[0] for b in range(w.batch)])
+        fn = lambda: c.append(kn, vn, pos)
     else:
         w = I.prefill_32b()
         w.batch = 4
@@ -706,7 +721,7 @@ def main():
     ap.add_argument("--cpu-seqs", type=int, default=16)
     ap.add_argument("--cpu-quant-seqs", type=int, default=8)
     ap.add_argument("--ref-seqs", type=int, default=4)
-    ap.add_argument("--profile-case", choices=["decode16k", "decode16k_k4v4", "fp16", "quantize", "multiquery16k"], default=None)
+    ap.add_argument("--profile-case", choices=["decode16k", "decode16k_k4v4", "fp16", "quantize", "multiquery16k", "append"], default=None)
     ap.add_argument("--profile-launches", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
