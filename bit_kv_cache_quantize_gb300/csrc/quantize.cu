@@ -623,12 +623,12 @@ template <typename E>
 __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   QSmem& sm = *reinterpret_cast<QSmem*>(smem_raw);
-  __shared__ int32_t close_blk[16];  // per unit of the current round: block its tile closes into, or -1
+  __shared__ int32_t close_blk[16];  // per unit of the current pass: block its tile closes into, or -1
   const int64_t units = static_cast<int64_t>(prm.batch) * prm.num_kv_heads * 2;
   const size_t tail_bytes = (size_t)units * T * D * sizeof(E);
   const int grp = threadIdx.x >> 4, gl = threadIdx.x & 15;
   // This CTA owns units blockIdx.x + k * gridDim.x (unit = (sequence, head,
-  // K|V)), sixteen per round.
+  // K|V)), sixteen per pass.
   for (int64_t r0 = blockIdx.x; r0 < units; r0 += 16LL * gridDim.x) {
     // 1. sixteen threads per unit copy its token into the open tile and note
     //    whether the token closes the tile
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(256, 2) append_tokens_kernel(AppendParams prm)
       else quantize_tile_cta<E, KIND_K2>(tile, D, dst, prm.iters, sm);
       __syncthreads();  // the next tile reuses the shared memory
     }
-    __syncthreads();  // close_blk is rewritten by the next round
+    __syncthreads();  // close_blk is rewritten by the next pass
   }
 }
 

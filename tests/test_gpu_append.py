@@ -130,9 +130,9 @@ def test_append_close_bf16():
 
 def test_append_every_sequence_closes():
     """320 sequences x 8 KV heads = 5120 (sequence, head, K|V) units, more
-    than the grid's CTAs take in one round of sixteen, and every sequence
+    than the grid's CTAs take in one pass of sixteen, and every sequence
     closes a tile on the same step: CTAs quantise up to sixteen tiles one
-    after another and go round twice.  Every closed tile is compared with
+    after another and make two passes.  Every closed tile is compared with
     the oracle."""
     lens = [127 + 128 * (b % 3) for b in range(320)]
     w = I.Workload("append_all_close", len(lens), 16, 8, "bf16", lens, seed=53, decode_steps=1, max_tokens=400,
