@@ -108,10 +108,10 @@ class ClockSampler:
 
 # DRAM bytes actually moved by one decode call per algorithmic byte, from an
 # ncu capture of the 16K decode call (32 x 16384 tokens, 64 q / 8 KV heads:
-# 449 705 472 B of DRAM traffic for 437 796 992 algorithmic bytes).  The
+# 446 744 832 B of DRAM traffic for 437 796 992 algorithmic bytes).  The
 # serving step's call is too large to capture, and its traffic grows with the
 # records it reads.
-DECODE_TRAFFIC_PER_BYTE = 449705472 / 437796992
+DECODE_TRAFFIC_PER_BYTE = 446744832 / 437796992
 
 
 # The quantiser's FP32 work per (tile, head) job: 8 normalisation iterations x

@@ -148,6 +148,19 @@ __device__ __forceinline__ void bulk_g2s(void* smem, const void* gmem, uint32_t 
       : "memory");
 }
 
+// The same copy for data read once (the decode's record stream): the L2
+// lines it brings in are the first evicted, which keeps the split-K
+// partials and the other small buffers of the step resident.
+__device__ __forceinline__ void bulk_g2s_stream(void* smem, const void* gmem, uint32_t bytes, uint64_t* bar) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          smem_u32(smem)),
+      "l"(gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
 // 2-D tiled TMA load global -> shared (box and swizzle from the tensor map),
 // completion counted on an mbarrier.  x * element size must be a multiple of
 // 16 bytes.

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(32 * NW, 2) decode_packed_kernel(DecodeParams 
     const uint32_t bytes = is_v ? VREC : KREC;
     if (blk >= 0 && blk < p.num_blocks && kcheck(src, bytes, p.pool, (size_t)p.num_blocks * p.block_bytes, p.err)) {
       mbar_expect_tx(bar, bytes);
-      bulk_g2s(is_v ? sm.vrec[warp] : sm.krec[warp], src, bytes, bar);
+      bulk_g2s_stream(is_v ? sm.vrec[warp] : sm.krec[warp], src, bytes, bar);
     } else {
       set_error(p.err, KVARN_DEV_ERR_BLOCK_RANGE);
       asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
