@@ -52,3 +52,35 @@ def test_reference_arm_under_torchrun_prints_from_rank_0_only():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], 2)
+
+
+def _bench_module():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_clock_record_from_nvidia_smi_samples():
+    """The clock record: median SM clock, the highest max clock, and every
+    throttle reason seen active in any sample; lines that are not samples
+    (short, or with fields nvidia-smi could not read) are skipped."""
+    B = _bench_module()
+    cs = B.ClockSampler(0)
+    cs.lines = [
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+        "",
+    ]
+    s = cs.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    cs.lines.append("0, 1200, 2070, 700.0, 0x8, Active, Not Active, Active, Not Active")
+    s = cs.summary()
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"] and s["samples"] == 4
+    assert s["sm_mhz"] == 2025.0
+    cs.lines = []
+    assert cs.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
