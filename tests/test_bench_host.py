@@ -84,3 +84,22 @@ def test_clock_record_from_nvidia_smi_samples():
     assert s["sm_mhz"] == 2025.0
     cs.lines = []
     assert cs.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+
+def test_decode_algorithmic_bytes():
+    """The roofline's numerator for a decode call: the 16K decode's
+    437 796 992 B (the figure its DRAM-traffic capture is compared with);
+    per closed tile one record per KV head of the size the C library gives a
+    block (every preset); 512 B per raw open-tile token and KV head."""
+    from bit_kv_cache_quantize_gb300 import build as Bld, inputs as I, kvarn as K
+    B = _bench_module()
+    w = I.qwen3_32b()
+    assert B.decode_bytes(w.seq_lens, w) == 437_796_992
+    Bld.build()
+    for kb, vb in ((4, 2), (2, 2), (4, 4)):
+        w = I.qwen3_32b()
+        w.k_bits, w.v_bits = kb, vb
+        cfg = K.make_config(w.num_kv_heads, w.num_q_heads, 1, w.dtype, k_bits=kb, v_bits=vb)
+        one = B.decode_bytes([128], w) - B.decode_bytes([0], w)
+        assert one == K.kvarn_block_bytes(cfg) + 4, (kb, vb)
+        assert B.decode_bytes([128 + 5], w) - B.decode_bytes([128], w) == 5 * w.num_kv_heads * 2 * 128 * 2
