@@ -128,15 +128,16 @@ def test_append_close_bf16():
     run_steps(w, 2)
 
 
-def test_append_every_sequence_closes():
+@pytest.mark.parametrize("k_bits,v_bits", [(4, 2), (2, 2), (4, 4)])
+def test_append_every_sequence_closes(k_bits, v_bits):
     """320 sequences x 8 KV heads = 5120 (sequence, head, K|V) units, more
     than the grid's CTAs take in one pass of sixteen, and every sequence
     closes a tile on the same step: CTAs quantise up to sixteen tiles one
-    after another and make two passes.  Every closed tile is compared with
-    the oracle."""
+    after another and make two passes, in each preset.  Every closed tile
+    is compared with the oracle."""
     lens = [127 + 128 * (b % 3) for b in range(320)]
-    w = I.Workload("append_all_close", len(lens), 16, 8, "bf16", lens, seed=53, decode_steps=1, max_tokens=400,
-                   block_perm=True)
+    w = I.Workload(f"append_all_close_k{k_bits}v{v_bits}", len(lens), 16, 8, "bf16", lens, seed=53, decode_steps=1,
+                   max_tokens=400, block_perm=True, k_bits=k_bits, v_bits=v_bits)
     st = run_steps(w, 1, check_seqs=[0, 1, 2, 319])
     assert st.tiles == 2 * 8 * len(lens)
 
